@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantize-once activation path on GB300.
+
+Workload (one "step"), Q4_0 weights, T = 8 tokens, seeded synthetic data:
+  A. RMSNorm*w producer over x[8, 3584] writing F32 y and ONE Q8_1 image,
+     then q [3584->3584], k and v [3584->512] reading that image in one
+     grouped MMVQ launch (the shared-image attention projections);
+  B. the standalone ordinary K=8192, N=8192, T=8 matvec: the Q8_1 quantiser on
+     x2[8, 8192], then the MMVQ reading it.
+Each component is captured as a CUDA graph (the pages time warmed graph
+replays). Weights rotate over R replicas totalling more than 3x the L2, so
+every step streams its weights from HBM. The timed region is bracketed by a
+barrier and device synchronisation; all K steps are enqueued behind a short
+bounded GPU sleep so the device runs them back to back, and CUDA events on
+the launching stream time each component.
+
+metric/value: weight-stream GB/s of the whole step (weight bytes / step
+time). Per-component microseconds, bytes and HBM fractions are reported in
+"components". "e2e" repeats the step through the C ABI with host buffers:
+pinned host->device copies of x and x2 and device->host copies of all four
+outputs inside the timed region.
+
+--impl reference times the CPU oracle (test infrastructure, plain C) on this
+host for the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+T = 8
+D_ATTN = 3584
+QKV = (("q", 3584), ("k", 512), ("v", 512))
+K_BIG = N_BIG = 8192
+Q4_BYTES_PER_WEIGHT = 18 / 32
+METRIC = "µs per fused component and weight-stream GB/s (% of HBM peak), Q4_0 T=8"
+UNIT = "GB/s"
+
+
+def weight_bytes(N: int, K: int) -> int:
+    return N * (K // 32) * 18
+
+
+W_QKV = sum(weight_bytes(N, D_ATTN) for _, N in QKV)          # 9,289,728
+W_BIG = weight_bytes(N_BIG, K_BIG)                             # 37,748,736
+W_STEP = W_QKV + W_BIG
+# algorithmic bytes of the standalone MMVQ launch: weights + its image + F32 output
+IMG_BIG = T * (K_BIG // 32) * 36
+MMVQ_BIG_BYTES = W_BIG + IMG_BIG + T * N_BIG * 4
+IMG_ATTN = T * (D_ATTN // 32) * 36
+MMVQ_QKV_BYTES = W_QKV + IMG_ATTN + T * sum(N for _, N in QKV) * 4
+RMS_BYTES = T * D_ATTN * 4 * 2 + D_ATTN * 4 + IMG_ATTN          # x in, w in, y out, image out
+QUANT_BIG_BYTES = T * K_BIG * 4 + IMG_BIG
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names[1:], parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank: int, world: int) -> dict | None:
+    import torch
+
+    from quantized_activation_q4_gb300 import binding as qk
+    from quantized_activation_q4_gb300 import synth
+
+    dev_index = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev_index)
+    qk.load(build_if_missing=True)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    l2 = torch.cuda.get_device_properties(dev_index).L2_cache_size
+    R = max(2, -(-3 * l2 // W_STEP))                # replicas: >= 3x L2 of weights in rotation
+
+    # inputs (seeded; the same on every rank -- replicas)
+    x = dev(synth.activations(100, T, D_ATTN))
+    w = dev(synth.norm_weight(101, D_ATTN))
+    x2 = dev(synth.activations(102, T, K_BIG))
+    y = torch.empty((T, D_ATTN), dtype=torch.float32, device="cuda")
+    img = torch.empty((T * (D_ATTN // 32) * 36,), dtype=torch.uint8, device="cuda")
+    img2 = torch.empty((IMG_BIG,), dtype=torch.uint8, device="cuda")
+    outs = {name: torch.empty((T, N), dtype=torch.float32, device="cuda") for name, N in QKV}
+    out_big = torch.empty((T, N_BIG), dtype=torch.float32, device="cuda")
+
+    def packed(seed, N, K):
+        nbytes = qk.qk_weight_packed_bytes("q4_0", N, K)
+        buf = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
+        qk.qk_weight_pack("q4_0", dev(synth.q4_0_weight(seed, N, K).reshape(-1)), N, K, buf, nbytes)
+        return buf
+
+    reps = []
+    for r in range(R):
+        reps.append({"qkv": [packed(200 + 10 * r + i, N, D_ATTN) for i, (_, N) in enumerate(QKV)],
+                     "big": packed(300 + r, N_BIG, K_BIG)})
+    torch.cuda.synchronize()
+
+    def comp_a(r):
+        qk.qk_rmsnorm_q8_1(x, T, D_ATTN, D_ATTN, "mul", w, None, 1.0, 1e-6, y, D_ATTN, img, D_ATTN // 32)
+        qk.qk_mmvq(img, D_ATTN // 32, T, [qk.make_proj("q4_0", reps[r]["qkv"][i], N, D_ATTN, outs[name], N)
+                                           for i, (name, N) in enumerate(QKV)])
+
+    def comp_q():
+        qk.qk_quantize_q8_1(x2, T, K_BIG, K_BIG, img2, K_BIG // 32)
+
+    def comp_m(r):
+        qk.qk_mmvq(img2, K_BIG // 32, T, [qk.make_proj("q4_0", reps[r]["big"], N_BIG, K_BIG, out_big, N_BIG)])
+
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in range(R):                       # eager warm-up of every path
+            comp_a(r); comp_q(); comp_m(r)
+    torch.cuda.synchronize()
+    n0 = qk.launch_count()
+    for r in range(R):
+        ga, gq, gm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, stream=stream):
+            comp_a(r)
+        with torch.cuda.graph(gq, stream=stream):
+            comp_q()
+        with torch.cuda.graph(gm, stream=stream):
+            comp_m(r)
+        graphs.append((ga, gq, gm))
+    kernels_per_step = (qk.launch_count() - n0) // R
+
+    def enqueue_steps(n, evs=None, start=0):
+        for i in range(n):
+            ga, gq, gm = graphs[(start + i) % R]
+            if evs: evs[i][0].record(stream)
+            ga.replay()
+            if evs: evs[i][1].record(stream)
+            gq.replay()
+            if evs: evs[i][2].record(stream)
+            gm.replay()
+            if evs: evs[i][3].record(stream)
+
+    with torch.cuda.stream(stream):
+        enqueue_steps(args.warmup)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(4e6 + 250_000 * K))  # hold the stream while the host enqueues (bounded)
+            enqueue_steps(K, evs, start=args.warmup)
+        torch.cuda.synchronize()
+        time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    t_a = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in range(K)]    # µs
+    t_q = [evs[i][1].elapsed_time(evs[i][2]) * 1e3 for i in range(K)]
+    t_m = [evs[i][2].elapsed_time(evs[i][3]) * 1e3 for i in range(K)]
+    total_ms = evs[0][0].elapsed_time(evs[K - 1][3])
+    ms_per_step = total_ms / K
+    if world > 1:
+        t = torch.tensor([ms_per_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    # ---------------------------------------------------------------- e2e through the C ABI, host buffers
+    xh = torch.empty((T, D_ATTN), dtype=torch.float32).pin_memory()
+    x2h = torch.empty((T, K_BIG), dtype=torch.float32).pin_memory()
+    xh.copy_(torch.from_numpy(synth.activations(100, T, D_ATTN)))
+    x2h.copy_(torch.from_numpy(synth.activations(102, T, K_BIG)))
+    outh = {name: torch.empty((T, N), dtype=torch.float32).pin_memory() for name, N in QKV}
+    bigh = torch.empty((T, N_BIG), dtype=torch.float32).pin_memory()
+    h2d = xh.numel() * 4 + x2h.numel() * 4
+    d2h = sum(v.numel() * 4 for v in outh.values()) + bigh.numel() * 4
+
+    def e2e_step(i):
+        r = i % R
+        x.copy_(xh, non_blocking=True)
+        x2.copy_(x2h, non_blocking=True)
+        ga, gq, gm = graphs[r]
+        ga.replay(); gq.replay(); gm.replay()
+        for name, _ in QKV:
+            outh[name].copy_(outs[name], non_blocking=True)
+        bigh.copy_(out_big, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(K):
+            e2e_step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+
+    peaks = measured_peaks()
+    hbm = peaks["hbm_gbs"]
+    med = statistics.median
+    us_a, us_q, us_m = med(t_a), med(t_q), med(t_m)
+    avg_m = sum(t_m) / K
+    achieved = MMVQ_BIG_BYTES / (avg_m * 1e-6) / 1e9
+    value = world * W_STEP / (ms_per_step * 1e-3) / 1e9
+    clocks = clk.summary()
+    if rank != 0:
+        return None
+    comp = {
+        "rms_image_qkv": {"us_median": us_a, "weight_bytes": W_QKV,
+                          "weight_gbs": W_QKV / (us_a * 1e-6) / 1e9,
+                          "hbm_frac_weights": W_QKV / (us_a * 1e-6) / 1e9 / hbm,
+                          "kernels": ["rmsnorm_q8_1", "mmvq(q,k,v)"]},
+        "quantize_q8_1_8192": {"us_median": us_q, "bytes": QUANT_BIG_BYTES},
+        "mmvq_8192x8192": {"us_median": us_m, "us_mean": avg_m, "weight_bytes": W_BIG,
+                           "weight_gbs": W_BIG / (us_m * 1e-6) / 1e9,
+                           "hbm_frac_weights": W_BIG / (us_m * 1e-6) / 1e9 / hbm},
+        "ordinary_k8192_component": {"us_median": us_q + us_m,
+                                     "weight_gbs": W_BIG / ((us_q + us_m) * 1e-6) / 1e9},
+    }
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "q4_0 weights x q8_1 image (f16 MMA, f32 accum)",
+        "data": "synthetic (seeded; N(0,1) activations, uniform-nibble Q4_0 weights with half scales U[0.002,0.02])",
+        "config": {"workload": "shared-image attention projections, Qwen2-7B-like d=3584 T=8 "
+                               "(RMSNorm*w -> Q8_1 image -> q 3584x3584, k/v 512x3584) + ordinary "
+                               "K=8192 N=8192 T=8 matvec",
+                   "weight_replicas": R, "weight_bytes_in_rotation": R * W_STEP,
+                   "l2_policy": f"weights rotate over {R} replicas ({R * W_STEP / 1e6:.0f} MB > 3x L2 "
+                                f"{l2 / 1e6:.0f} MB); activations and images are small and stay resident",
+                   "graphs": "each component captured as a CUDA graph, replayed",
+                   "parallelism": "replicas only" if world > 1 else "single GPU"},
+        "components": comp,
+        "roofline": {"kernel": "mmvq (Q4_0, K=N=8192, T=8)", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy burst)",
+                     "algorithmic_bytes_per_launch": MMVQ_BIG_BYTES, "traffic": None},
+        "e2e": {"value": round(W_STEP / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": kernels_per_step * K,
+        "clocks": clocks,
+    }
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_step(inputs, full: bool = True):
+    """One config-1 step on the host with the oracle: RMS (binary64), image of its
+    binary32 rounding, q/k/v and the K8192 matvec on the quantised path."""
+    from oracle import oracle as O
+    x, w, x2, Wq, Wbig, big_rows = inputs
+    yd = O.rmsnorm(x, "mul", w=w, eps=1e-6)
+    img = O.quantize_q8_1(yd.astype(np.float32))
+    for (_, N), W in zip(QKV, Wq):
+        O.proj_q8_1("q4_0", W, N, D_ATTN, img, D_ATTN // 32)
+    img2 = O.quantize_q8_1(x2)
+    O.proj_q8_1("q4_0", Wbig[:big_rows], big_rows, K_BIG, img2, K_BIG // 32)
+
+
+def oracle_inputs(big_rows: int):
+    from quantized_activation_q4_gb300 import synth
+    x = synth.activations(100, T, D_ATTN)
+    w = synth.norm_weight(101, D_ATTN)
+    x2 = synth.activations(102, T, K_BIG)
+    Wq = [synth.q4_0_weight(200 + i, N, D_ATTN) for i, (_, N) in enumerate(QKV)]
+    Wbig = synth.q4_0_weight(300, big_rows, K_BIG)
+    return x, w, x2, Wq, Wbig, big_rows
+
+
+def cpu_baseline(big_rows: int = 2048, budget_s: float = 10.0) -> dict:
+    inputs = oracle_inputs(big_rows)
+    oracle_step(inputs)                       # build + warm
+    reps = 0
+    t0 = time.perf_counter()
+    while reps < 2 or time.perf_counter() - t0 < budget_s:
+        oracle_step(inputs)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    wbytes = W_QKV + weight_bytes(big_rows, K_BIG)
+    return {"value": round(wbytes / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"full q/k/v component + {big_rows} of 8192 rows of the K8192 matvec per step "
+                      f"({wbytes / 1e6:.1f} MB of weights), {reps} steps, single thread",
+            "seconds_per_sample_step": round(dt, 3)}
+
+
+def run_reference(args, rank: int) -> dict | None:
+    if rank != 0:
+        return None
+    big_rows = 2048
+    inputs = oracle_inputs(big_rows)
+    for _ in range(args.warmup):
+        oracle_step(inputs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(inputs)
+    dt = (time.perf_counter() - t0) / args.steps
+    wbytes = W_QKV + weight_bytes(big_rows, K_BIG)
+    v = wbytes / dt / 1e9
+    sample = (f"each step: full q/k/v component + {big_rows} of 8192 rows of the K8192 matvec "
+              f"({wbytes / 1e6:.1f} MB of weights), single thread")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulation (oracle)",
+            "data": "synthetic (seeded)",
+            "config": {"workload": "shared-image attention projections d=3584 T=8 + ordinary K=8192 N=8192 T=8 "
+                                   "(CPU oracle sample)"},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        out = run_reference(args, rank)
+        if out:
+            print(json.dumps(out), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    out = run_gpu(args, rank, world)
+    if out is not None:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,309 @@
+/*
+ * qk.h -- C ABI of libqk: quantize-once activation images for GB300 (sm_103a).
+ *
+ * An F32 activation is quantised once into a 32-element-block Q8 "image" by
+ * the kernel that produces it (an RMSNorm or a GLU), and that one image is
+ * then read by every quantised-weight projection that consumes the
+ * activation: q/k/v or gate/up, ordinary (MUL_MAT) or routed per expert
+ * (MUL_MAT_ID).
+ *
+ * Sources (page titles and sections):
+ *   llama.cpp PR #117 "activation image emission" -- Overview and Coverage:
+ *     the shared Q8_1 image, RMS/GLU producers that emit it beside their
+ *     original F32 output, ordinary and routed MMVQ readers.
+ *   minfer doc 52 "r49 A-quantize prepass shared-A dedup" -- sections 1-3:
+ *     the prefill Q8_0 prepass read by the MMQ GEMMs, once per distinct A;
+ *     out-of-pool scratch; errors surfaced at entry, before any launch.
+ *   TensorFold PR #1047 "padding rows no longer go through routed experts"
+ *     -- "The fix": a device-side live-row count read by every kernel at
+ *     each graph replay, launches sized for the bucket, stable grouped plan.
+ *
+ * Conventions (every call):
+ *   - Pointers named x, w, img, y, ids ... are DEVICE pointers owned by the
+ *     caller; the library never frees or keeps them after the call.
+ *   - The library allocates no memory and never synchronises; each call
+ *     validates its arguments on the host, then enqueues its kernel(s) on
+ *     `stream` (NULL = the legacy default stream) and returns.
+ *   - On an invalid argument nothing is launched and a status other than
+ *     QK_OK is returned; qk_last_error() gives a one-line reason (per host
+ *     thread).
+ *   - d_live_rows: optional DEVICE pointer to one int32, the number of live
+ *     rows. Kernels read it on the device at every launch or graph replay;
+ *     rows at or past it (clamped to [0, rows]) are not read for work and
+ *     their outputs are not written. NULL means every row is live. Grids are
+ *     always sized for `rows`, so a captured CUDA graph stays valid while the
+ *     count changes between replays.
+ *   - Results depend only on the input bytes and shape arguments (no state
+ *     kept between calls, no cross-call caching; an image is rebuilt on every
+ *     call and replay).
+ *   - Strides are in elements of the pointed-to type unless named *_blocks.
+ */
+#ifndef QK_H
+#define QK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QK_API __attribute__((visibility("default")))
+#else
+#define QK_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *qk_stream; /* a cudaStream_t */
+
+typedef enum qk_status {
+    QK_OK = 0,
+    QK_ERR_ARG = 1,         /* null pointer, negative size or bad enum */
+    QK_ERR_SHAPE = 2,       /* a width that must be whole 32-blocks is not, or a stride too small */
+    QK_ERR_ALIAS = 3,       /* an output overlaps an input or another output */
+    QK_ERR_WORKSPACE = 4,   /* a packed buffer or workspace is too small */
+    QK_ERR_UNSUPPORTED = 5, /* a size outside what the kernel supports (e.g. T > 8) */
+    QK_ERR_CUDA = 6         /* a CUDA launch failed; see qk_last_error() */
+} qk_status;
+
+typedef enum qk_norm_kind {
+    QK_NORM_PLAIN = 0,   /* y = x * r               */
+    QK_NORM_MUL = 1,     /* y = (x * r) * w          */
+    QK_NORM_MUL_ADD = 2, /* y = (x * r) * w + b      */
+    QK_NORM_SCALE = 3    /* y = (x * r) * scale      */
+} qk_norm_kind;
+
+typedef enum qk_glu_kind {
+    QK_GLU_SWIGLU = 0,     /* out = g * sigmoid(g) * u */
+    QK_GLU_GEGLU_TANH = 1, /* out = 0.5 g (1 + tanh(sqrt(2/pi)(g + 0.044715 g^3))) * u */
+    QK_GLU_REGLU = 2       /* out = max(g, 0) * u */
+} qk_glu_kind;
+
+typedef enum qk_glu_layout {
+    QK_GLU_SEPARATE = 0,      /* g rows at a (a_stride), u rows at b (b_stride) */
+    QK_GLU_PACKED = 1,        /* row of a = [g (N) | u (N)]; b unused          */
+    QK_GLU_PACKED_SWAPPED = 2 /* row of a = [u (N) | g (N)]; b unused          */
+} qk_glu_layout;
+
+typedef enum qk_wtype {
+    QK_W_Q4_0 = 0, /* 18-byte blocks: half d, 16 nibble bytes; value (nibble - 8) * d */
+    QK_W_Q8_0 = 1  /* 34-byte blocks: half d, 32 int8; value q * d                    */
+} qk_wtype;
+
+/* ------------------------------------------------------------------ misc */
+
+/* Short name of a status code (static string). */
+QK_API const char *qk_status_string(qk_status s);
+
+/* One-line reason for the last non-QK_OK status returned on this host thread. */
+QK_API const char *qk_last_error(void);
+
+/* Number of kernels this library has launched in this process (all threads). */
+QK_API uint64_t qk_launch_count(void);
+
+/* ------------------------------------------------------------ the image */
+
+/*
+ * Q8_1 activation image (llama.cpp PR #117, Coverage: the "standard Q8_1
+ * activation image" read by every MMVQ weight format).
+ *
+ * Layout: img[t] is a row of img_row_blocks blocks of 36 bytes, rows back to
+ * back (row stride 36 * img_row_blocks bytes). Block b of row t covers
+ * activation columns 32b .. 32b+31:
+ *   bytes 0-1  d  = half(amax / 127), amax = max |x| over the block, binary32
+ *   bytes 2-3  s  = half(d * sum(q)), product in binary32
+ *   bytes 4-35 q_i = rint(x_i / d) in binary32, ties to even, int8 in [-127, 127]
+ * An all-zero block has d = s = 0 and q = 0. Columns past K inside the last
+ * block are taken as 0; blocks ceil(K/32) .. img_row_blocks-1 are written as
+ * 36 zero bytes. Halves are IEEE binary16, round to nearest even, little
+ * endian.
+ */
+#define QK_Q8_1_BLOCK_BYTES 36
+
+/*
+ * qk_quantize_q8_1 -- standalone quantiser (the separate launch that producer
+ * emission replaces; kept for unfused use and as the fused kernels' control).
+ *   x        [T][x_stride] F32, columns 0..K-1 read
+ *   img      [T][img_row_blocks] Q8_1 blocks, img_row_blocks >= ceil(K/32)
+ * Errors: QK_ERR_ARG (null, T < 0, K < 1), QK_ERR_SHAPE (x_stride < K,
+ * img_row_blocks < ceil(K/32)), QK_ERR_ALIAS (img overlaps x).
+ */
+QK_API qk_status qk_quantize_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride,
+                           void *img, int64_t img_row_blocks,
+                           const int32_t *d_live_rows, qk_stream stream);
+
+/*
+ * qk_quantize_q8_0 -- the prefill prepass (minfer doc 52, section 1: per
+ * 32-block amax, rintf scaling, zero pad). Same d and codes as the Q8_1
+ * image, no s, stored as two planes so tensor-core tiles load rows directly:
+ *   qs  [T][row_blocks * 32] int8 codes
+ *   d   [T][row_blocks]      binary16 bits (uint16)
+ * Blocks ceil(K/32) .. row_blocks-1 are zero. Errors as qk_quantize_q8_1.
+ */
+QK_API qk_status qk_quantize_q8_0(const float *x, int64_t T, int64_t K, int64_t x_stride,
+                           int8_t *qs, uint16_t *d, int64_t row_blocks,
+                           const int32_t *d_live_rows, qk_stream stream);
+
+/* ------------------------------------------------------- the producers */
+
+/*
+ * qk_rmsnorm_q8_1 -- RMS producer that emits the image (llama.cpp PR #117,
+ * Coverage: RMS-alone, RMS+MUL, RMS+MUL+ADD and RMS+SCALE producers emit
+ * images while keeping their original F32 output).
+ *   r = 1 / sqrt(sum(x^2)/K + eps) per row (binary32 arithmetic)
+ *   y = x*r, (x*r)*w, (x*r)*w + b, or (x*r)*scale  by `kind`
+ *   y   [T][y_stride] F32, written for live rows, columns 0..K-1
+ *   img the Q8_1 image of exactly the stored y values (bit-identical to
+ *       qk_quantize_q8_1 applied to y)
+ *   w, b: [K] F32, required by MUL / MUL_ADD (b only by MUL_ADD), else ignored
+ * Errors: QK_ERR_ARG, QK_ERR_SHAPE (K % 32 != 0: the producer's width must be
+ * whole Q8_1 blocks; strides too small), QK_ERR_ALIAS (y or img overlapping
+ * x, w, b or each other).
+ */
+QK_API qk_status qk_rmsnorm_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride,
+                          qk_norm_kind kind, const float *w, const float *b,
+                          float scale, float eps,
+                          float *y, int64_t y_stride, void *img, int64_t img_row_blocks,
+                          const int32_t *d_live_rows, qk_stream stream);
+
+/*
+ * qk_glu_q8_1 -- GLU producer that emits the image (llama.cpp PR #117,
+ * Coverage: F32 ReGLU, GeGLU, SwiGLU with separate, packed and packed-swapped
+ * inputs and independent source row strides; output width whole Q8_1 blocks).
+ *   out [T][out_stride] F32 = act(g) * u for live rows, columns 0..N-1
+ *   img the Q8_1 image of exactly the stored out values
+ *   SEPARATE: g = a + t*a_stride, u = b + t*b_stride
+ *   PACKED: g = a + t*a_stride, u = g + N;  PACKED_SWAPPED: u = a + t*a_stride, g = u + N
+ * Errors: QK_ERR_ARG, QK_ERR_SHAPE (N % 32 != 0, strides too small),
+ * QK_ERR_ALIAS (out or img overlapping the inputs or each other).
+ */
+QK_API qk_status qk_glu_q8_1(qk_glu_kind kind, qk_glu_layout layout,
+                      const float *a, int64_t a_stride, const float *b, int64_t b_stride,
+                      int64_t T, int64_t N,
+                      float *out, int64_t out_stride, void *img, int64_t img_row_blocks,
+                      const int32_t *d_live_rows, qk_stream stream);
+
+/* ------------------------------------------------------------- weights */
+
+/*
+ * Weights arrive as canonical row-major blocks ([N][K/32] blocks of
+ * QK_W_Q4_0 or QK_W_Q8_0 bytes; Q4_0 element j < 16 is the low nibble of byte
+ * j, element j+16 its high nibble). qk_weight_pack rearranges them once into
+ * the device layout the projection kernels stream with 128-bit loads. The
+ * packed layout is private to this library and may change between versions;
+ * its size is qk_weight_packed_bytes(). K must be a multiple of 32.
+ */
+QK_API size_t qk_weight_packed_bytes(qk_wtype wtype, int64_t N, int64_t K);
+
+QK_API qk_status qk_weight_pack(qk_wtype wtype, const void *blocks, int64_t N, int64_t K,
+                         void *packed, size_t packed_bytes, qk_stream stream);
+
+/* ---------------------------------------------------------- projections */
+
+/* One projection read from a shared image: y[t][n] = sum_k W[n][k] x_t[k]. */
+typedef struct qk_proj {
+    int32_t wtype;     /* qk_wtype */
+    int32_t reserved;  /* 0 */
+    const void *w;     /* packed weights (qk_weight_pack) */
+    int64_t N;         /* output features */
+    int64_t K;         /* input features, multiple of 32 */
+    float *y;          /* [T][y_stride] F32 output */
+    int64_t y_stride;  /* >= N */
+} qk_proj;
+
+/*
+ * qk_mmvq -- ordinary MUL_MAT on one shared Q8_1 image, several projections
+ * in ONE launch (llama.cpp PR #117, Overview/Coverage: q/k/v or gate/up read
+ * the same image; the page's "Ordinary, K8192 / T8" component).
+ * Per 32-block b, from the stored halves (exact integer block dot D):
+ *   Q4_0: y += d_w * (d_a * D - 8 * s_a),  D = sum nibble_i * q_i
+ *   Q8_0: y += d_w * d_a * D,              D = sum w_i * q_i
+ *   img  [T][img_row_blocks] Q8_1; every projection's K <= 32*img_row_blocks
+ *   T    1..8 image rows (tokens); rows >= *d_live_rows are not written
+ *   projs host array of n_proj (1..8) descriptors; outputs must not overlap
+ * Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED (T > 8 or n_proj > 8),
+ * QK_ERR_SHAPE (K % 32, K beyond the image, y_stride < N), QK_ERR_ALIAS.
+ */
+QK_API qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T,
+                  int32_t n_proj, const qk_proj *projs,
+                  const int32_t *d_live_rows, qk_stream stream);
+
+/* ---------------------------------------------------------- routing */
+
+/*
+ * qk_topk_route -- router probabilities and top-k experts for the live rows
+ * (TensorFold PR #1047, "The fix": tf_moe_router and tf_moe_topk skip rows
+ * from the live count up).
+ *   logits [rows][E] F32; ids [rows][k] int32; wts [rows][k] F32
+ *   experts ranked by logit, larger first, equal logits to the lower index;
+ *   ids in rank order; wts = softmax(logits)[id] (not renormalised).
+ * Rows >= *d_live_rows keep their previous ids/wts bytes.
+ * Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED (E > 256, k > 32, k > E).
+ */
+QK_API qk_status qk_topk_route(const float *logits, int64_t rows, int32_t E, int32_t k,
+                        int32_t *ids, float *wts,
+                        const int32_t *d_live_rows, qk_stream stream);
+
+/*
+ * qk_moe_plan -- stable grouped plan of the live pairs (TensorFold PR #1047,
+ * "The fix": counts and ranks, exclusive-scan offsets, scatter, over the
+ * first live*k pairs only).
+ *   pairs p = row*k + slot for rows < live; expert ids[p]
+ *   counts [E]   pairs per expert
+ *   offsets[E+1] exclusive scan of counts, offsets[E] = live*k
+ *   items  [rows*k] positions 0..live*k-1 hold the pairs grouped by expert,
+ *          ascending p within each expert; positions past live*k untouched
+ * One launch for any width. Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED
+ * (E > 1024), QK_ERR_ALIAS.
+ */
+QK_API qk_status qk_moe_plan(const int32_t *ids, int64_t rows, int32_t k, int32_t E,
+                      int32_t *counts, int32_t *offsets, int32_t *items,
+                      const int32_t *d_live_rows, qk_stream stream);
+
+/* One routed projection: E experts' packed weights back to back. */
+typedef struct qk_proj_id {
+    int32_t wtype;          /* qk_wtype */
+    int32_t n_experts;      /* E */
+    const void *w;          /* expert e at w + e * qk_weight_packed_bytes(wtype, N, K) */
+    int64_t N;              /* output features per expert */
+    int64_t K;              /* input features, multiple of 32 */
+    float *y;               /* [rows*k][N] F32, pair p at row p */
+} qk_proj_id;
+
+/*
+ * qk_mmvq_id -- routed MUL_MAT_ID reading the one shared image (llama.cpp
+ * PR #117, Coverage: the image is independent of route ids; TensorFold PR
+ * #1047: padding rows get no plan items and no expert work).
+ * For every expert e and every planned item p in items[offsets[e] ..
+ * offsets[e+1]): y[p][:] = W_e * image row (p / k), with the per-block
+ * arithmetic of qk_mmvq. Experts with no items read no weights; pairs not in
+ * the plan are not written. The plan (counts/offsets/items, device) is the
+ * output of qk_moe_plan; ids is not needed.
+ *   rows: bucket rows (image rows >= rows never read); n_proj 1..8
+ * Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED (n_experts > 1024), QK_ERR_SHAPE,
+ * QK_ERR_ALIAS.
+ */
+QK_API qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k,
+                     int32_t n_proj, const qk_proj_id *projs,
+                     const int32_t *counts, const int32_t *offsets, const int32_t *items,
+                     qk_stream stream);
+
+/* ---------------------------------------------------------- prefill */
+
+/*
+ * qk_mmq -- prefill dense contraction on a Q8_0 image (minfer doc 52,
+ * sections 1 and 5: the q/k/v and gate/up GEMMs that share one quantised A).
+ *   qs [T][row_blocks*32] int8 and d [T][row_blocks] half: qk_quantize_q8_0
+ *   C[t][n] = sum_b d_w[n][b] * d_a[t][b] * sum_{i in b} w_i * q_i
+ *   (Q4_0: w_i = nibble - 8) written to projs[j].y ([T][y_stride] F32)
+ * Errors: QK_ERR_ARG, QK_ERR_SHAPE, QK_ERR_UNSUPPORTED, QK_ERR_ALIAS.
+ */
+QK_API qk_status qk_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int64_t T,
+                 int32_t n_proj, const qk_proj *projs, qk_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QK_H */

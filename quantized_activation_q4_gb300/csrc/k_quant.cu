@@ -1,0 +1,271 @@
+// Q8 activation images and the producers that emit them.
+//
+//   quantize_q8_1 / quantize_q8_0 : standalone quantisers (llama.cpp PR #117
+//       "activation image emission", Coverage: the standard Q8_1 image;
+//       minfer doc 52 "r49 A-quantize prepass shared-A dedup", section 1: the
+//       Q8_0 prepass with per-32-block amax, rintf scaling and zero pad).
+//   rmsnorm_q8_1 / glu_q8_1       : producers that write their original F32
+//       output and the Q8_1 image of exactly the stored values (PR #117,
+//       Coverage: RMS and F32 GLU producers emit the image).
+//
+// Work layout: every quant block of 32 elements is handled by 8 consecutive
+// lanes, 4 elements each, so a warp quantises 4 blocks at once with 3-step
+// xor shuffles for the block max and the code sum. All block arithmetic is
+// binary32 with IEEE division (no fast-math in this file), the codes use
+// round-to-nearest-even and the halves use __float2half_rn.
+
+#include "qk_internal.cuh"
+
+namespace qk {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// Four consecutive floats from p (16-byte aligned fast path, else scalar with
+// a bound: elements at index >= n read as 0).
+__device__ __forceinline__ void load4(const float *p, int n, float v[4]) {
+    if (n >= 4 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+        float4 t = __ldg(reinterpret_cast<const float4 *>(p));
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) v[i] = i < n ? __ldg(p + i) : 0.0f;
+    }
+}
+
+__device__ __forceinline__ void store4(float *p, const float v[4]) {
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) p[i] = v[i];
+    }
+}
+
+// Quantises one 32-element block held by 8 lanes (4 values each; j8 = the
+// lane's index in its group). All 32 lanes of the warp must call this.
+// Returns the binary32 scale d; codes are packed little-endian into *codes
+// and the block's code sum into *sum.
+__device__ __forceinline__ float q8_block(const float v[4], uint32_t *codes, int *sum) {
+    float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
+    const float d = a / 127.0f;
+    int q[4] = {0, 0, 0, 0};
+    if (a != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) q[i] = __float2int_rn(v[i] / d);
+    }
+    int s = q[0] + q[1] + q[2] + q[3];
+    s += __shfl_xor_sync(FULL, s, 1);
+    s += __shfl_xor_sync(FULL, s, 2);
+    s += __shfl_xor_sync(FULL, s, 4);
+    *codes = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) |
+             ((uint32_t)(q[2] & 0xff) << 16) | ((uint32_t)(q[3] & 0xff) << 24);
+    *sum = s;
+    return d;
+}
+
+// Writes lane j8's share of a Q8_1 block: codes at bytes 4+4*j8, and for
+// j8 == 0 the header [half d][half d*sum].
+__device__ __forceinline__ void put_q8_1(uint8_t *blk, int j8, float d, uint32_t codes, int sum) {
+    reinterpret_cast<uint32_t *>(blk + 4)[j8] = codes;
+    if (j8 == 0) {
+        __half2 h = __halves2half2(__float2half_rn(d), __float2half_rn(d * (float)sum));
+        *reinterpret_cast<__half2 *>(blk) = h;
+    }
+}
+
+// ---------------------------------------------------------------- quantizers
+// grid (ceil(row_blocks/32), T), 256 threads: warp w, lane group m handles
+// block 32*blockIdx.x + 4*w + m of row blockIdx.y.
+template <bool Q81>
+__global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__ x, int K,
+                                                       int64_t x_stride, uint8_t *__restrict__ out,
+                                                       int8_t *__restrict__ qs, uint16_t *__restrict__ dh,
+                                                       int64_t row_blocks, int T, const int32_t *live) {
+    const int t = blockIdx.y;
+    if (t >= live_rows(live, T)) return;
+    const int lane = threadIdx.x & 31, j8 = lane & 7;
+    const int64_t b = (int64_t)blockIdx.x * 32 + (threadIdx.x >> 5) * 4 + (lane >> 3);
+    const bool in_row = b < row_blocks;          // whole 8-lane group agrees
+    const int64_t col = b * QB + 4 * j8;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (in_row && col < K) load4(x + t * x_stride + col, (int)(K - col < 4 ? K - col : 4), v);
+    uint32_t codes;
+    int sum;
+    const float d = q8_block(v, &codes, &sum);  // all lanes take part in the shuffles
+    if (!in_row) return;
+    if (Q81) {
+        put_q8_1(out + (t * row_blocks + b) * Q8_1_BYTES, j8, d, codes, sum);
+    } else {
+        reinterpret_cast<uint32_t *>(qs + (t * row_blocks + b) * QB)[j8] = codes;
+        if (j8 == 0) dh[t * row_blocks + b] = __half_as_ushort(__float2half_rn(d));
+    }
+}
+
+// ---------------------------------------------------------------- RMS producer
+// One CTA of 256 threads per row. Thread i handles columns 4i + 1024*it.
+__global__ void __launch_bounds__(256) rmsnorm_q8_1_kernel(
+    const float *__restrict__ x, int K, int64_t x_stride, int kind, const float *__restrict__ w,
+    const float *__restrict__ bias, float scale, float eps, float *__restrict__ y, int64_t y_stride,
+    uint8_t *__restrict__ img, int64_t row_blocks, int T, const int32_t *live) {
+    const int t = blockIdx.x;
+    if (t >= live_rows(live, T)) return;
+    const float *xr = x + t * x_stride;
+    const int tid = threadIdx.x, lane = tid & 31, j8 = lane & 7;
+
+    float ss = 0.0f;
+    for (int c = 4 * tid; c < K; c += 1024) {
+        float v[4];
+        load4(xr + c, K - c, v);
+        ss += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+    __shared__ float red[8];
+    __shared__ float rs;
+    if (lane == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float tot = 0.0f;
+        for (int i = 0; i < 8; i++) tot += red[i];
+        rs = 1.0f / sqrtf(tot / (float)K + eps);
+    }
+    __syncthreads();
+    const float r = rs;
+
+    float *yr = y + t * y_stride;
+    uint8_t *ir = img + t * row_blocks * Q8_1_BYTES;
+    const int iters = (int)((K + 1023) / 1024);
+    for (int it = 0; it < iters; it++) {           // uniform trip count: shuffles stay full-warp
+        const int c = 4 * tid + 1024 * it;
+        const bool ok = c < K;                     // K % 32 == 0: whole 8-lane groups agree
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ok) {
+            load4(xr + c, 4, v);
+            float wv[4], bv[4];
+            if (kind == QK_NORM_MUL || kind == QK_NORM_MUL_ADD) load4(w + c, 4, wv);
+            if (kind == QK_NORM_MUL_ADD) load4(bias + c, 4, bv);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                float o = v[i] * r;
+                if (kind == QK_NORM_MUL) o = o * wv[i];
+                else if (kind == QK_NORM_MUL_ADD) o = o * wv[i] + bv[i];
+                else if (kind == QK_NORM_SCALE) o = o * scale;
+                v[i] = o;
+            }
+            store4(yr + c, v);
+        }
+        uint32_t codes;
+        int sum;
+        const float d = q8_block(v, &codes, &sum);
+        if (ok) put_q8_1(ir + (int64_t)(c / QB) * Q8_1_BYTES, j8, d, codes, sum);
+    }
+    // zero blocks of the row padding
+    const int kb = K / QB;
+    for (int64_t bb = kb + tid; bb < row_blocks; bb += 256) {
+        uint32_t *p = reinterpret_cast<uint32_t *>(ir + bb * Q8_1_BYTES);
+#pragma unroll
+        for (int i = 0; i < 9; i++) p[i] = 0u;
+    }
+}
+
+// ---------------------------------------------------------------- GLU producer
+__device__ __forceinline__ float glu_act(int kind, float g) {
+    if (kind == QK_GLU_SWIGLU) return g / (1.0f + expf(-g));
+    if (kind == QK_GLU_GEGLU_TANH) {
+        const float c = 0.7978845608028654f;  // sqrt(2/pi)
+        return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
+    }
+    return fmaxf(g, 0.0f);
+}
+
+// grid (ceil(N/1024), T), 256 threads; thread i handles columns 1024*bx + 4i.
+__global__ void __launch_bounds__(256) glu_q8_1_kernel(
+    int kind, int layout, const float *__restrict__ a, int64_t a_stride, const float *__restrict__ b,
+    int64_t b_stride, int N, float *__restrict__ out, int64_t out_stride, uint8_t *__restrict__ img,
+    int64_t row_blocks, int T, const int32_t *live) {
+    const int t = blockIdx.y;
+    if (t >= live_rows(live, T)) return;
+    const int tid = threadIdx.x, j8 = tid & 7;
+    const int c = blockIdx.x * 1024 + 4 * tid;
+    const float *g, *u;
+    if (layout == QK_GLU_SEPARATE) {
+        g = a + t * a_stride;
+        u = b + t * b_stride;
+    } else if (layout == QK_GLU_PACKED) {
+        g = a + t * a_stride;
+        u = g + N;
+    } else {
+        u = a + t * a_stride;
+        g = u + N;
+    }
+    const bool ok = c < N;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
+        float gv[4], uv[4];
+        load4(g + c, 4, gv);
+        load4(u + c, 4, uv);
+#pragma unroll
+        for (int i = 0; i < 4; i++) v[i] = glu_act(kind, gv[i]) * uv[i];
+        store4(out + t * out_stride + c, v);
+    }
+    uint32_t codes;
+    int sum;
+    const float d = q8_block(v, &codes, &sum);
+    uint8_t *ir = img + t * row_blocks * Q8_1_BYTES;
+    if (ok) put_q8_1(ir + (int64_t)(c / QB) * Q8_1_BYTES, j8, d, codes, sum);
+    if (blockIdx.x == 0) {  // zero blocks of the row padding
+        for (int64_t bb = N / QB + tid; bb < row_blocks; bb += 256) {
+            uint32_t *p = reinterpret_cast<uint32_t *>(ir + bb * Q8_1_BYTES);
+#pragma unroll
+            for (int i = 0; i < 9; i++) p[i] = 0u;
+        }
+    }
+}
+
+}  // namespace
+
+qk_status launch_quantize_q8_1(const float *x, int T, int K, int64_t x_stride, uint8_t *img,
+                               int64_t row_blocks, const int32_t *live, cudaStream_t s) {
+    if (T == 0) return QK_OK;
+    dim3 grid((unsigned)ceil_div(row_blocks, 32), (unsigned)T);
+    quantize_kernel<true><<<grid, 256, 0, s>>>(x, K, x_stride, img, nullptr, nullptr, row_blocks, T, live);
+    count_launch();
+    return check_launch("quantize_q8_1");
+}
+
+qk_status launch_quantize_q8_0(const float *x, int T, int K, int64_t x_stride, int8_t *qs,
+                               uint16_t *d, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
+    if (T == 0) return QK_OK;
+    dim3 grid((unsigned)ceil_div(row_blocks, 32), (unsigned)T);
+    quantize_kernel<false><<<grid, 256, 0, s>>>(x, K, x_stride, nullptr, qs, d, row_blocks, T, live);
+    count_launch();
+    return check_launch("quantize_q8_0");
+}
+
+qk_status launch_rmsnorm_q8_1(const float *x, int T, int K, int64_t x_stride, int kind,
+                              const float *w, const float *b, float scale, float eps, float *y,
+                              int64_t y_stride, uint8_t *img, int64_t row_blocks,
+                              const int32_t *live, cudaStream_t s) {
+    if (T == 0) return QK_OK;
+    rmsnorm_q8_1_kernel<<<T, 256, 0, s>>>(x, K, x_stride, kind, w, b, scale, eps, y, y_stride, img,
+                                          row_blocks, T, live);
+    count_launch();
+    return check_launch("rmsnorm_q8_1");
+}
+
+qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride, const float *b,
+                          int64_t b_stride, int T, int N, float *out, int64_t out_stride,
+                          uint8_t *img, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
+    if (T == 0) return QK_OK;
+    dim3 grid((unsigned)ceil_div(N, 1024), (unsigned)T);
+    glu_q8_1_kernel<<<grid, 256, 0, s>>>(kind, layout, a, a_stride, b, b_stride, N, out, out_stride,
+                                         img, row_blocks, T, live);
+    count_launch();
+    return check_launch("glu_q8_1");
+}
+
+}  // namespace qk

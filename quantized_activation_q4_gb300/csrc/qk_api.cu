@@ -1,0 +1,315 @@
+// libqk C ABI: argument checks on the host, then the kernel launchers.
+//
+// Every check happens before anything is enqueued, so a bad call leaves the
+// stream untouched (minfer doc 52 "r49 A-quantize prepass shared-A dedup",
+// section 3.1: errors surface at entry, not as a fault in a later launch).
+// Aliasing outputs are refused (llama.cpp PR #117 "activation image
+// emission", Coverage: unsafe input/output aliases keep the original path).
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "qk_internal.cuh"
+
+namespace qk {
+
+static thread_local char g_err[512] = "";
+static std::atomic<uint64_t> g_launches{0};
+
+qk_status fail(qk_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+qk_status check_launch(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(QK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return QK_OK;
+}
+
+void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace qk
+
+using namespace qk;
+
+#define REQUIRE(cond, status, ...) \
+    do {                           \
+        if (!(cond)) return fail(status, __VA_ARGS__); \
+    } while (0)
+
+static bool aligned(const void *p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+extern "C" {
+
+const char *qk_status_string(qk_status s) {
+    switch (s) {
+        case QK_OK: return "QK_OK";
+        case QK_ERR_ARG: return "QK_ERR_ARG";
+        case QK_ERR_SHAPE: return "QK_ERR_SHAPE";
+        case QK_ERR_ALIAS: return "QK_ERR_ALIAS";
+        case QK_ERR_WORKSPACE: return "QK_ERR_WORKSPACE";
+        case QK_ERR_UNSUPPORTED: return "QK_ERR_UNSUPPORTED";
+        case QK_ERR_CUDA: return "QK_ERR_CUDA";
+    }
+    return "QK_ERR_UNKNOWN";
+}
+
+const char *qk_last_error(void) { return g_err; }
+
+uint64_t qk_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+// ------------------------------------------------------------------ image
+static qk_status check_quant_in(const float *x, int64_t T, int64_t K, int64_t x_stride) {
+    REQUIRE(T >= 0 && T <= INT32_MAX, QK_ERR_ARG, "T=%lld out of range", (long long)T);
+    REQUIRE(K >= 1 && K <= (1LL << 30), QK_ERR_ARG, "K=%lld out of range", (long long)K);
+    REQUIRE(x || T == 0, QK_ERR_ARG, "x is null");
+    REQUIRE(x_stride >= K, QK_ERR_SHAPE, "x_stride=%lld < K=%lld", (long long)x_stride, (long long)K);
+    REQUIRE(aligned(x, 4), QK_ERR_ARG, "x not 4-byte aligned");
+    return QK_OK;
+}
+
+qk_status qk_quantize_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride, void *img,
+                           int64_t img_row_blocks, const int32_t *d_live_rows, qk_stream stream) {
+    qk_status st = check_quant_in(x, T, K, x_stride);
+    if (st != QK_OK) return st;
+    REQUIRE(img || T == 0, QK_ERR_ARG, "img is null");
+    REQUIRE(aligned(img, 4), QK_ERR_ARG, "img not 4-byte aligned");
+    REQUIRE(img_row_blocks >= ceil_div(K, QB), QK_ERR_SHAPE, "img_row_blocks=%lld < ceil(K/32)=%lld",
+            (long long)img_row_blocks, (long long)ceil_div(K, QB));
+    Span sx = span(x, rows_span(T, x_stride * 4, K * 4));
+    Span si = span(img, (size_t)(T * img_row_blocks * Q8_1_BYTES));
+    REQUIRE(!overlap(sx, si), QK_ERR_ALIAS, "img overlaps x");
+    return launch_quantize_q8_1(x, (int)T, (int)K, x_stride, static_cast<uint8_t *>(img), img_row_blocks,
+                                d_live_rows, (cudaStream_t)stream);
+}
+
+qk_status qk_quantize_q8_0(const float *x, int64_t T, int64_t K, int64_t x_stride, int8_t *qs,
+                           uint16_t *d, int64_t row_blocks, const int32_t *d_live_rows, qk_stream stream) {
+    qk_status st = check_quant_in(x, T, K, x_stride);
+    if (st != QK_OK) return st;
+    REQUIRE((qs && d) || T == 0, QK_ERR_ARG, "qs or d is null");
+    REQUIRE(aligned(qs, 4) && aligned(d, 2), QK_ERR_ARG, "qs must be 4-byte and d 2-byte aligned");
+    REQUIRE(row_blocks >= ceil_div(K, QB), QK_ERR_SHAPE, "row_blocks=%lld < ceil(K/32)", (long long)row_blocks);
+    Span sx = span(x, rows_span(T, x_stride * 4, K * 4));
+    Span sq = span(qs, (size_t)(T * row_blocks * QB));
+    Span sd = span(d, (size_t)(T * row_blocks * 2));
+    REQUIRE(!overlap(sx, sq) && !overlap(sx, sd) && !overlap(sq, sd), QK_ERR_ALIAS, "qs/d overlap x or each other");
+    return launch_quantize_q8_0(x, (int)T, (int)K, x_stride, qs, d, row_blocks, d_live_rows, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ producers
+qk_status qk_rmsnorm_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride, qk_norm_kind kind,
+                          const float *w, const float *b, float scale, float eps, float *y,
+                          int64_t y_stride, void *img, int64_t img_row_blocks,
+                          const int32_t *d_live_rows, qk_stream stream) {
+    qk_status st = check_quant_in(x, T, K, x_stride);
+    if (st != QK_OK) return st;
+    REQUIRE(kind >= QK_NORM_PLAIN && kind <= QK_NORM_SCALE, QK_ERR_ARG, "bad norm kind %d", (int)kind);
+    REQUIRE(K % QB == 0, QK_ERR_SHAPE, "K=%lld is not a whole number of 32-blocks", (long long)K);
+    REQUIRE((y && img) || T == 0, QK_ERR_ARG, "y or img is null");
+    const bool need_w = kind == QK_NORM_MUL || kind == QK_NORM_MUL_ADD;
+    REQUIRE(!need_w || w, QK_ERR_ARG, "w is null for a MUL kind");
+    REQUIRE(kind != QK_NORM_MUL_ADD || b, QK_ERR_ARG, "b is null for MUL_ADD");
+    REQUIRE(y_stride >= K, QK_ERR_SHAPE, "y_stride < K");
+    REQUIRE(img_row_blocks >= K / QB, QK_ERR_SHAPE, "img_row_blocks < K/32");
+    REQUIRE(aligned(y, 4) && aligned(img, 4) && aligned(w, 4) && aligned(b, 4), QK_ERR_ARG, "misaligned pointer");
+    Span sx = span(x, rows_span(T, x_stride * 4, K * 4));
+    Span sy = span(y, rows_span(T, y_stride * 4, K * 4));
+    Span si = span(img, (size_t)(T * img_row_blocks * Q8_1_BYTES));
+    Span sw = span(need_w ? w : nullptr, need_w ? (size_t)K * 4 : 0);
+    Span sb = span(kind == QK_NORM_MUL_ADD ? b : nullptr, kind == QK_NORM_MUL_ADD ? (size_t)K * 4 : 0);
+    REQUIRE(!overlap(sy, sx) && !overlap(sy, si) && !overlap(si, sx) && !overlap(sy, sw) && !overlap(sy, sb) &&
+                !overlap(si, sw) && !overlap(si, sb),
+            QK_ERR_ALIAS, "y or img overlaps an input or each other");
+    return launch_rmsnorm_q8_1(x, (int)T, (int)K, x_stride, (int)kind, w, b, scale, eps, y, y_stride,
+                               static_cast<uint8_t *>(img), img_row_blocks, d_live_rows, (cudaStream_t)stream);
+}
+
+qk_status qk_glu_q8_1(qk_glu_kind kind, qk_glu_layout layout, const float *a, int64_t a_stride,
+                      const float *b, int64_t b_stride, int64_t T, int64_t N, float *out,
+                      int64_t out_stride, void *img, int64_t img_row_blocks, const int32_t *d_live_rows,
+                      qk_stream stream) {
+    REQUIRE(kind >= QK_GLU_SWIGLU && kind <= QK_GLU_REGLU, QK_ERR_ARG, "bad glu kind %d", (int)kind);
+    REQUIRE(layout >= QK_GLU_SEPARATE && layout <= QK_GLU_PACKED_SWAPPED, QK_ERR_ARG, "bad glu layout %d", (int)layout);
+    REQUIRE(T >= 0 && T <= INT32_MAX && N >= 1 && N <= (1LL << 30), QK_ERR_ARG, "T or N out of range");
+    REQUIRE(N % QB == 0, QK_ERR_SHAPE, "N=%lld is not a whole number of 32-blocks", (long long)N);
+    REQUIRE((a && out && img && (layout != QK_GLU_SEPARATE || b)) || T == 0, QK_ERR_ARG, "null pointer");
+    const int64_t a_row = layout == QK_GLU_SEPARATE ? N : 2 * N;
+    REQUIRE(a_stride >= a_row, QK_ERR_SHAPE, "a_stride too small");
+    REQUIRE(layout != QK_GLU_SEPARATE || b_stride >= N, QK_ERR_SHAPE, "b_stride < N");
+    REQUIRE(out_stride >= N && img_row_blocks >= N / QB, QK_ERR_SHAPE, "out_stride or img_row_blocks too small");
+    REQUIRE(aligned(a, 4) && aligned(b, 4) && aligned(out, 4) && aligned(img, 4), QK_ERR_ARG, "misaligned pointer");
+    Span sa = span(a, rows_span(T, a_stride * 4, a_row * 4));
+    Span sb = span(layout == QK_GLU_SEPARATE ? b : nullptr,
+                   layout == QK_GLU_SEPARATE ? rows_span(T, b_stride * 4, N * 4) : 0);
+    Span so = span(out, rows_span(T, out_stride * 4, N * 4));
+    Span si = span(img, (size_t)(T * img_row_blocks * Q8_1_BYTES));
+    REQUIRE(!overlap(so, sa) && !overlap(so, sb) && !overlap(so, si) && !overlap(si, sa) && !overlap(si, sb),
+            QK_ERR_ALIAS, "out or img overlaps an input or each other");
+    return launch_glu_q8_1((int)kind, (int)layout, a, a_stride, b, b_stride, (int)T, (int)N, out, out_stride,
+                           static_cast<uint8_t *>(img), img_row_blocks, d_live_rows, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ weights
+size_t qk_weight_packed_bytes(qk_wtype wtype, int64_t N, int64_t K) {
+    if ((wtype != QK_W_Q4_0 && wtype != QK_W_Q8_0) || N < 0 || K < 0) return 0;
+    return (size_t)packed_bytes(wtype, N, K);
+}
+
+qk_status qk_weight_pack(qk_wtype wtype, const void *blocks, int64_t N, int64_t K, void *packed,
+                         size_t packed_bytes_, qk_stream stream) {
+    REQUIRE(wtype == QK_W_Q4_0 || wtype == QK_W_Q8_0, QK_ERR_ARG, "bad wtype %d", (int)wtype);
+    REQUIRE(N >= 1 && K >= 32 && N <= INT32_MAX && K <= INT32_MAX, QK_ERR_ARG, "N or K out of range");
+    REQUIRE(K % QB == 0, QK_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+    REQUIRE(blocks && packed, QK_ERR_ARG, "null pointer");
+    REQUIRE(aligned(packed, 16), QK_ERR_ARG, "packed must be 16-byte aligned");
+    const size_t need = (size_t)packed_bytes(wtype, N, K);
+    REQUIRE(packed_bytes_ >= need, QK_ERR_WORKSPACE, "packed_bytes=%zu < %zu", packed_bytes_, need);
+    const size_t src = (size_t)(N * (K / QB) * (wtype == QK_W_Q4_0 ? Q4_0_BYTES : Q8_0_BYTES));
+    REQUIRE(!overlap(span(blocks, src), span(packed, need)), QK_ERR_ALIAS, "packed overlaps blocks");
+    return launch_weight_pack(wtype, static_cast<const uint8_t *>(blocks), N, K, static_cast<uint8_t *>(packed),
+                              (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ projections
+static qk_status check_proj_common(int32_t wtype, const void *w, int64_t N, int64_t K, int64_t img_row_blocks) {
+    REQUIRE(wtype == QK_W_Q4_0 || wtype == QK_W_Q8_0, QK_ERR_ARG, "bad wtype %d", (int)wtype);
+    REQUIRE(w, QK_ERR_ARG, "null weight pointer");
+    REQUIRE(aligned(w, 16), QK_ERR_ARG, "packed weights must be 16-byte aligned");
+    REQUIRE(N >= 1 && N <= INT32_MAX && K >= 32 && K <= INT32_MAX, QK_ERR_ARG, "N or K out of range");
+    REQUIRE(K % QB == 0, QK_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+    REQUIRE(K / QB <= img_row_blocks, QK_ERR_SHAPE, "K=%lld reaches past the image row (%lld blocks)",
+            (long long)K, (long long)img_row_blocks);
+    return QK_OK;
+}
+
+qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_proj, const qk_proj *projs,
+                  const int32_t *d_live_rows, qk_stream stream) {
+    REQUIRE(img && projs, QK_ERR_ARG, "null pointer");
+    REQUIRE(aligned(img, 4), QK_ERR_ARG, "img not 4-byte aligned");
+    REQUIRE(T >= 1 && img_row_blocks >= 1, QK_ERR_ARG, "T or img_row_blocks < 1");
+    REQUIRE(T <= 8, QK_ERR_UNSUPPORTED, "T=%lld > 8 (use qk_mmq for larger batches)", (long long)T);
+    REQUIRE(n_proj >= 1 && n_proj <= 8, QK_ERR_UNSUPPORTED, "n_proj=%d not in 1..8", (int)n_proj);
+    Span si = span(img, (size_t)(T * img_row_blocks * Q8_1_BYTES));
+    for (int j = 0; j < n_proj; j++) {
+        const qk_proj &p = projs[j];
+        qk_status st = check_proj_common(p.wtype, p.w, p.N, p.K, img_row_blocks);
+        if (st != QK_OK) return st;
+        REQUIRE(p.y, QK_ERR_ARG, "projection %d: y is null", j);
+        REQUIRE(p.y_stride >= p.N, QK_ERR_SHAPE, "projection %d: y_stride < N", j);
+        Span sy = span(p.y, rows_span(T, p.y_stride * 4, p.N * 4));
+        Span sw = span(p.w, (size_t)packed_bytes(p.wtype, p.N, p.K));
+        REQUIRE(!overlap(sy, si) && !overlap(sy, sw), QK_ERR_ALIAS, "projection %d: y overlaps img or w", j);
+        for (int i = 0; i < j; i++) {
+            Span so = span(projs[i].y, rows_span(T, projs[i].y_stride * 4, projs[i].N * 4));
+            REQUIRE(!overlap(sy, so), QK_ERR_ALIAS, "outputs of projections %d and %d overlap", i, j);
+        }
+    }
+    // one launch per weight type present (a q/k/v or gate/up group is normally one type)
+    for (int wt = QK_W_Q4_0; wt <= QK_W_Q8_0; wt++) {
+        qk_proj group[8];
+        int n = 0;
+        for (int j = 0; j < n_proj; j++)
+            if (projs[j].wtype == wt) group[n++] = projs[j];
+        if (n == 0) continue;
+        qk_status st = launch_mmvq(static_cast<const uint8_t *>(img), img_row_blocks, (int)T, n, group,
+                                   d_live_rows, (cudaStream_t)stream);
+        if (st != QK_OK) return st;
+    }
+    return QK_OK;
+}
+
+qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k, int32_t n_proj,
+                     const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
+                     const int32_t *items, qk_stream stream) {
+    REQUIRE(img && projs && counts && offsets && items, QK_ERR_ARG, "null pointer");
+    REQUIRE(aligned(img, 4), QK_ERR_ARG, "img not 4-byte aligned");
+    REQUIRE(rows >= 1 && rows <= (1 << 24) && k >= 1 && k <= 64 && img_row_blocks >= 1, QK_ERR_ARG,
+            "rows, k or img_row_blocks out of range");
+    REQUIRE(n_proj >= 1 && n_proj <= 8, QK_ERR_UNSUPPORTED, "n_proj=%d not in 1..8", (int)n_proj);
+    Span si = span(img, (size_t)(rows * img_row_blocks * Q8_1_BYTES));
+    for (int j = 0; j < n_proj; j++) {
+        const qk_proj_id &p = projs[j];
+        qk_status st = check_proj_common(p.wtype, p.w, p.N, p.K, img_row_blocks);
+        if (st != QK_OK) return st;
+        REQUIRE(p.n_experts >= 1 && p.n_experts <= 1024, QK_ERR_UNSUPPORTED, "n_experts=%d", (int)p.n_experts);
+        REQUIRE(p.y, QK_ERR_ARG, "projection %d: y is null", j);
+        REQUIRE(projs[0].n_experts == p.n_experts, QK_ERR_ARG, "projections disagree on n_experts");
+        Span sy = span(p.y, (size_t)(rows * k * p.N * 4));
+        Span sw = span(p.w, (size_t)packed_bytes(p.wtype, p.N, p.K) * p.n_experts);
+        REQUIRE(!overlap(sy, si) && !overlap(sy, sw), QK_ERR_ALIAS, "projection %d: y overlaps img or w", j);
+        for (int i = 0; i < j; i++)
+            REQUIRE(!overlap(sy, span(projs[i].y, (size_t)(rows * k * projs[i].N * 4))), QK_ERR_ALIAS,
+                    "outputs of projections %d and %d overlap", i, j);
+    }
+    for (int wt = QK_W_Q4_0; wt <= QK_W_Q8_0; wt++) {
+        qk_proj_id group[8];
+        int n = 0;
+        for (int j = 0; j < n_proj; j++)
+            if (projs[j].wtype == wt) group[n++] = projs[j];
+        if (n == 0) continue;
+        qk_status st = launch_mmvq_id(static_cast<const uint8_t *>(img), img_row_blocks, (int)rows, k, n, group,
+                                      counts, offsets, items, (cudaStream_t)stream);
+        if (st != QK_OK) return st;
+    }
+    return QK_OK;
+}
+
+// ------------------------------------------------------------------ routing
+qk_status qk_topk_route(const float *logits, int64_t rows, int32_t E, int32_t k, int32_t *ids, float *wts,
+                        const int32_t *d_live_rows, qk_stream stream) {
+    REQUIRE(logits && ids && wts, QK_ERR_ARG, "null pointer");
+    REQUIRE(rows >= 0 && rows <= (1 << 24) && E >= 1 && k >= 1, QK_ERR_ARG, "rows, E or k out of range");
+    REQUIRE(E <= 256 && k <= 32 && k <= E, QK_ERR_UNSUPPORTED, "E=%d k=%d (need E <= 256, k <= min(32, E))", E, k);
+    Span sl = span(logits, (size_t)(rows * E * 4));
+    Span si = span(ids, (size_t)(rows * k * 4));
+    Span sw = span(wts, (size_t)(rows * k * 4));
+    REQUIRE(!overlap(si, sl) && !overlap(sw, sl) && !overlap(si, sw), QK_ERR_ALIAS, "ids/wts overlap logits or each other");
+    return launch_topk_route(logits, (int)rows, E, k, ids, wts, d_live_rows, (cudaStream_t)stream);
+}
+
+qk_status qk_moe_plan(const int32_t *ids, int64_t rows, int32_t k, int32_t E, int32_t *counts, int32_t *offsets,
+                      int32_t *items, const int32_t *d_live_rows, qk_stream stream) {
+    REQUIRE(ids && counts && offsets && items, QK_ERR_ARG, "null pointer");
+    REQUIRE(rows >= 0 && rows <= (1 << 24) && k >= 1 && k <= 64 && E >= 1, QK_ERR_ARG, "rows, k or E out of range");
+    REQUIRE(E <= 1024, QK_ERR_UNSUPPORTED, "E=%d > 1024", E);
+    Span s_ids = span(ids, (size_t)(rows * k * 4));
+    Span sc = span(counts, (size_t)E * 4), so = span(offsets, (size_t)(E + 1) * 4);
+    Span sit = span(items, (size_t)(rows * k * 4));
+    REQUIRE(!overlap(sc, s_ids) && !overlap(so, s_ids) && !overlap(sit, s_ids) && !overlap(sc, so) &&
+                !overlap(sc, sit) && !overlap(so, sit),
+            QK_ERR_ALIAS, "plan outputs overlap ids or each other");
+    return launch_moe_plan(ids, (int)rows, k, E, counts, offsets, items, d_live_rows, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ prefill
+qk_status qk_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int64_t T, int32_t n_proj,
+                 const qk_proj *projs, qk_stream stream) {
+    REQUIRE(qs && d && projs, QK_ERR_ARG, "null pointer");
+    REQUIRE(T >= 1 && T <= INT32_MAX && row_blocks >= 1, QK_ERR_ARG, "T or row_blocks out of range");
+    REQUIRE(n_proj >= 1 && n_proj <= 8, QK_ERR_UNSUPPORTED, "n_proj=%d not in 1..8", (int)n_proj);
+    REQUIRE(aligned(qs, 16) && aligned(d, 4), QK_ERR_ARG, "qs must be 16-byte and d 4-byte aligned");
+    Span sq = span(qs, (size_t)(T * row_blocks * QB)), sd = span(d, (size_t)(T * row_blocks * 2));
+    for (int j = 0; j < n_proj; j++) {
+        const qk_proj &p = projs[j];
+        qk_status st = check_proj_common(p.wtype, p.w, p.N, p.K, row_blocks);
+        if (st != QK_OK) return st;
+        REQUIRE(p.wtype == QK_W_Q4_0, QK_ERR_UNSUPPORTED, "qk_mmq takes Q4_0 weights");
+        REQUIRE(p.y && p.y_stride >= p.N, QK_ERR_SHAPE, "projection %d: y null or y_stride < N", j);
+        Span sy = span(p.y, rows_span(T, p.y_stride * 4, p.N * 4));
+        REQUIRE(!overlap(sy, sq) && !overlap(sy, sd) && !overlap(sy, span(p.w, (size_t)packed_bytes(p.wtype, p.N, p.K))),
+                QK_ERR_ALIAS, "projection %d: y overlaps an input", j);
+        for (int i = 0; i < j; i++)
+            REQUIRE(!overlap(sy, span(projs[i].y, rows_span(T, projs[i].y_stride * 4, projs[i].N * 4))), QK_ERR_ALIAS,
+                    "outputs of projections %d and %d overlap", i, j);
+    }
+    return launch_mmq(qs, d, row_blocks, (int)T, n_proj, projs, (cudaStream_t)stream);
+}
+
+}  // extern "C"

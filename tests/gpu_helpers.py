@@ -1,0 +1,47 @@
+"""Device-side helpers for the GPU parity tests (allocation and copies only)."""
+from __future__ import annotations
+
+import numpy as np
+
+from quantized_activation_q4_gb300 import binding as qk
+
+
+def dev(a: np.ndarray):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t) -> np.ndarray:
+    import torch
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def empty_u8(n: int, fill: int = 0xA5):
+    import torch
+    return torch.full((n,), fill, dtype=torch.uint8, device="cuda")
+
+
+def live_ptr(n: int):
+    import torch
+    return torch.tensor([n], dtype=torch.int32, device="cuda")
+
+
+def pack_weight(W: np.ndarray, wtype: str, N: int, K: int):
+    """Canonical blocks (host) -> packed device weights via qk_weight_pack."""
+    import torch
+    nbytes = qk.qk_weight_packed_bytes(wtype, N, K)
+    src = dev(W.reshape(-1))
+    packed = torch.full((nbytes,), 0x5A, dtype=torch.uint8, device="cuda")
+    qk.qk_weight_pack(wtype, src, N, K, packed, nbytes)
+    return packed
+
+
+def pack_experts(Ws: list[np.ndarray], wtype: str, N: int, K: int):
+    """E experts' canonical blocks -> one buffer, expert e at e * packed_bytes."""
+    import torch
+    per = qk.qk_weight_packed_bytes(wtype, N, K)
+    out = torch.empty((len(Ws) * per,), dtype=torch.uint8, device="cuda")
+    for e, W in enumerate(Ws):
+        qk.qk_weight_pack(wtype, dev(W.reshape(-1)), N, K, out[e * per:(e + 1) * per], per)
+    return out

@@ -1,0 +1,94 @@
+"""The C ABI library loads, exports every declared entry point, and rejects bad
+calls on the host before anything is launched (no GPU needed: the pointers
+below are never dereferenced)."""
+import ctypes as C
+
+import pytest
+
+from quantized_activation_q4_gb300 import binding as qk
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return qk.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = qk.declared_symbols()
+    assert len(names) >= 14
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert missing == []
+
+
+def test_status_strings(lib):
+    assert lib.qk_status_string(0) == b"QK_OK"
+    assert lib.qk_status_string(3) == b"QK_ERR_ALIAS"
+
+
+X = 0x10000000       # fake, never-dereferenced device addresses
+IMG = 0x20000000
+Y = 0x30000000
+W = 0x40000000
+S0 = 0               # null stream: never used by a call that fails validation
+
+
+def _st(fn, *args):
+    return fn(*args)
+
+
+def test_quantize_rejects_bad_shapes(lib):
+    P = C.c_void_p
+    assert lib.qk_quantize_q8_1(P(X), 2, 33, 32, P(IMG), 2, None, None) == 2       # x_stride < K
+    assert lib.qk_quantize_q8_1(P(X), 2, 33, 40, P(IMG), 1, None, None) == 2       # too few image blocks
+    assert lib.qk_quantize_q8_1(None, 2, 32, 32, P(IMG), 1, None, None) == 1       # null x
+    assert lib.qk_quantize_q8_1(P(X), 2, 0, 32, P(IMG), 1, None, None) == 1        # K < 1
+    assert lib.qk_quantize_q8_1(P(X + 2), 2, 32, 32, P(IMG), 1, None, None) == 1   # misaligned x
+    # image overlapping the input rows
+    assert lib.qk_quantize_q8_1(P(X), 4, 64, 64, P(X + 512), 2, None, None) == 3
+    assert b"overlaps" in lib.qk_last_error()
+
+
+def test_producers_reject_partial_blocks_and_aliases(lib):
+    P = C.c_void_p
+    # K not a whole number of 32-blocks
+    assert lib.qk_rmsnorm_q8_1(P(X), 1, 48, 48, 0, None, None, 1.0, 1e-6, P(Y), 48, P(IMG), 2, None, None) == 2
+    # MUL without w
+    assert lib.qk_rmsnorm_q8_1(P(X), 1, 64, 64, 1, None, None, 1.0, 1e-6, P(Y), 64, P(IMG), 2, None, None) == 1
+    # y written over x
+    assert lib.qk_rmsnorm_q8_1(P(X), 1, 64, 64, 0, None, None, 1.0, 1e-6, P(X), 64, P(IMG), 2, None, None) == 3
+    # GLU: N not whole blocks; bad layout; out over the packed input
+    assert lib.qk_glu_q8_1(0, 0, P(X), 40, P(W), 40, 1, 40, P(Y), 40, P(IMG), 2, None, None) == 2
+    assert lib.qk_glu_q8_1(0, 7, P(X), 64, P(W), 64, 1, 32, P(Y), 32, P(IMG), 1, None, None) == 1
+    assert lib.qk_glu_q8_1(0, 1, P(X), 128, None, 0, 1, 64, P(X + 64), 64, P(IMG), 2, None, None) == 3
+
+
+def test_projection_checks(lib):
+    P = C.c_void_p
+    good = qk.qk_proj(0, 0, W, 64, 256, Y, 64)
+    arr = (qk.qk_proj * 1)(good)
+    assert lib.qk_mmvq(P(IMG), 8, 9, 1, arr, None, None) == 5                  # T > 8
+    arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W, 64, 288, Y, 64))
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, None) == 2                  # K past the image row
+    arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W + 8, 64, 256, Y, 64))
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, None) == 1                  # misaligned packed weights
+    arr = (qk.qk_proj * 2)(good, qk.qk_proj(0, 0, W, 64, 256, Y + 128, 64))
+    assert lib.qk_mmvq(P(IMG), 8, 8, 2, arr, None, None) == 3                  # overlapping outputs
+    arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W, 64, 256, IMG + 4, 64))
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, None) == 3                  # output over the image
+
+
+def test_routing_checks(lib):
+    P = C.c_void_p
+    assert lib.qk_topk_route(P(X), 16, 512, 8, P(Y), P(W), None, None) == 5    # E > 256
+    assert lib.qk_topk_route(P(X), 16, 128, 8, P(X), P(W), None, None) == 3    # ids over logits
+    assert lib.qk_moe_plan(P(X), 16, 8, 2048, P(Y), P(W), P(IMG), None, None) == 5
+    assert lib.qk_moe_plan(P(X), 16, 8, 128, P(Y), P(Y + 16), P(IMG), None, None) == 3
+
+
+def test_weight_pack_checks(lib):
+    P = C.c_void_p
+    need = lib.qk_weight_packed_bytes(0, 100, 256)
+    assert need == 7 * 2 * 1152                                                  # 16-row x 128-col tiles
+    assert lib.qk_weight_pack(0, P(X), 100, 256, P(W), need - 1, None) == 4
+    assert lib.qk_weight_pack(0, P(X), 100, 250, P(W), need, None) == 2
+    assert lib.qk_weight_pack(0, P(X), 100, 256, P(X + 64), need, None) == 3
