@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(NW * 32) mmvq_kernel(const __grid_constant__ A
     constexpr uint32_t NEG_BIAS_HI = WT == QK_W_Q4_0 ? 0xD400D400u : 0xE480E480u;  //   -64 | -1152
 
     __shared__ float red[NW][RG * 4][32];
-    __shared__ int tok_img[8], tok_out[8], n_tok_s;
+    __shared__ int tok_img[8], tok_out[8];
 
     const int C = args.ksplit;
     const int rank = (int)(blockIdx.x % (unsigned)C);
@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(NW * 32) mmvq_kernel(const __grid_constant__ A
             const int s = threadIdx.x;
             if (ROUTED) {
                 const int idx = pass * 8 + s;
-                const int p = idx < n_items ? __ldg(args.items + item0 + idx) : -1;
+                int p = idx < n_items ? __ldg(args.items + item0 + idx) : -1;
+                if (p < 0 || p / args.k >= args.T) p = -1;     // not a pair of this bucket: skip
                 tok_img[s] = p >= 0 ? p / args.k : -1;
                 tok_out[s] = p;
             } else {

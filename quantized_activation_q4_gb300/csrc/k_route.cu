@@ -107,7 +107,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
     __syncthreads();
 
     // per expert: prefix over warps (seg becomes the warp's base), total count
-    int tot = 0;
     for (int e = tid; e < E; e += 1024) {
         int s = 0;
         for (int w = 0; w < 32; w++) {
@@ -117,7 +116,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
         }
         counts[e] = s;
         off[e] = s;
-        if (e == tid) tot = s;
     }
     __syncthreads();
     // exclusive scan of off[0..E) (E <= 1024: one value per thread)
@@ -161,7 +159,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
         if (ok && (m & lt) == 0) seg[warp * E + e] += __popc(m);
         __syncwarp();
     }
-    (void)tot;
 }
 
 }  // namespace
