@@ -163,16 +163,27 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                      "big": packed(300 + r, N_BIG, K_BIG)})
     torch.cuda.synchronize()
 
+    def qkv_projs(r):
+        return [qk.make_proj("q4_0", reps[r]["qkv"][i], N, D_ATTN, outs[name], N) for i, (name, N) in enumerate(QKV)]
+
+    def big_projs(r):
+        return [qk.make_proj("q4_0", reps[r]["big"], N_BIG, K_BIG, out_big, N_BIG)]
+
+    # zeroed once; every call leaves its workspace zeroed again
+    ws_a_n = qk.qk_mmvq_workspace_bytes(qkv_projs(0))
+    ws_m_n = qk.qk_mmvq_workspace_bytes(big_projs(0))
+    ws_a = torch.zeros((ws_a_n,), dtype=torch.uint8, device="cuda")
+    ws_m = torch.zeros((ws_m_n,), dtype=torch.uint8, device="cuda")
+
     def comp_a(r):
         qk.qk_rmsnorm_q8_1(x, T, D_ATTN, D_ATTN, "mul", w, None, 1.0, 1e-6, y, D_ATTN, img, D_ATTN // 32)
-        qk.qk_mmvq(img, D_ATTN // 32, T, [qk.make_proj("q4_0", reps[r]["qkv"][i], N, D_ATTN, outs[name], N)
-                                           for i, (name, N) in enumerate(QKV)])
+        qk.qk_mmvq(img, D_ATTN // 32, T, qkv_projs(r), ws_a, ws_a_n)
 
     def comp_q():
         qk.qk_quantize_q8_1(x2, T, K_BIG, K_BIG, img2, K_BIG // 32)
 
     def comp_m(r):
-        qk.qk_mmvq(img2, K_BIG // 32, T, [qk.make_proj("q4_0", reps[r]["big"], N_BIG, K_BIG, out_big, N_BIG)])
+        qk.qk_mmvq(img2, K_BIG // 32, T, big_projs(r), ws_m, ws_m_n)
 
     stream = torch.cuda.Stream()
     graphs = []
@@ -221,6 +232,9 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         time.sleep(0.2)
     if world > 1:
         torch.distributed.barrier()
+    faults = qk.qk_device_faults()
+    if faults:
+        raise RuntimeError(f"device fault word {faults:#x} after the timed region")
     t_a = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in range(K)]    # µs
     t_q = [evs[i][1].elapsed_time(evs[i][2]) * 1e3 for i in range(K)]
     t_m = [evs[i][2].elapsed_time(evs[i][3]) * 1e3 for i in range(K)]

@@ -102,6 +102,13 @@ QK_API const char *qk_last_error(void);
 /* Number of kernels this library has launched in this process (all threads). */
 QK_API uint64_t qk_launch_count(void);
 
+/*
+ * Device-side fault word of the current device, then cleared. Bit 0: a
+ * kernel's bounded wait on a shared-memory barrier gave up (the kernel then
+ * stopped early and its outputs are not valid). Synchronises the device.
+ */
+QK_API qk_status qk_device_faults(uint32_t *faults);
+
 /* ------------------------------------------------------------ the image */
 
 /*
@@ -222,12 +229,23 @@ typedef struct qk_proj {
  *   img  [T][img_row_blocks] Q8_1; every projection's K <= 32*img_row_blocks
  *   T    1..8 image rows (tokens); rows >= *d_live_rows are not written
  *   projs host array of n_proj (1..8) descriptors; outputs must not overlap
+ *   ws   device workspace of at least qk_mmvq_workspace_bytes(n_proj, projs)
+ *        bytes, 16-byte aligned, ZEROED ONCE before its first use (e.g. by
+ *        cudaMemset); every call leaves it zeroed again when its kernels
+ *        finish. Calls that may run concurrently need separate workspaces.
+ * The work is split by bytes over the device's SMs; partial sums of a row
+ * tile shared by several CTAs go through ws and are added in a fixed order,
+ * so outputs are deterministic on a given device.
  * Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED (T > 8 or n_proj > 8),
- * QK_ERR_SHAPE (K % 32, K beyond the image, y_stride < N), QK_ERR_ALIAS.
+ * QK_ERR_SHAPE (K % 32, K beyond the image, y_stride < N), QK_ERR_ALIAS,
+ * QK_ERR_WORKSPACE (ws null or too small).
  */
+QK_API size_t qk_mmvq_workspace_bytes(int32_t n_proj, const qk_proj *projs);
+
 QK_API qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T,
-                  int32_t n_proj, const qk_proj *projs,
-                  const int32_t *d_live_rows, qk_stream stream);
+                         int32_t n_proj, const qk_proj *projs,
+                         const int32_t *d_live_rows, void *ws, size_t ws_bytes,
+                         qk_stream stream);
 
 /* ---------------------------------------------------------- routing */
 

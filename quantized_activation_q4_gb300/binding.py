@@ -58,7 +58,9 @@ _SIGS = {
     "qk_glu_q8_1": ([C.c_int, C.c_int, P, I64, P, I64, I64, I64, P, I64, P, I64, P, P], C.c_int),
     "qk_weight_packed_bytes": ([C.c_int, I64, I64], SZ),
     "qk_weight_pack": ([C.c_int, P, I64, I64, P, SZ, P], C.c_int),
-    "qk_mmvq": ([P, I64, I64, I32, C.POINTER(qk_proj), P, P], C.c_int),
+    "qk_device_faults": ([C.POINTER(C.c_uint32)], C.c_int),
+    "qk_mmvq_workspace_bytes": ([I32, C.POINTER(qk_proj)], SZ),
+    "qk_mmvq": ([P, I64, I64, I32, C.POINTER(qk_proj), P, P, SZ, P], C.c_int),
     "qk_topk_route": ([P, I64, I32, I32, P, P, P, P], C.c_int),
     "qk_moe_plan": ([P, I64, I32, I32, P, P, P, P, P], C.c_int),
     "qk_mmvq_id": ([P, I64, I64, I32, I32, C.POINTER(qk_proj_id), P, P, P, P], C.c_int),
@@ -175,10 +177,21 @@ def make_proj_id(wtype, n_experts, w, N, K, y) -> qk_proj_id:
     return qk_proj_id(wtype, n_experts, _ptr(w), N, K, _ptr(y))
 
 
-def qk_mmvq(img, img_row_blocks, T, projs, d_live_rows=None, stream=None):
+def qk_mmvq_workspace_bytes(projs) -> int:
+    arr = (qk_proj * len(projs))(*projs)
+    return int(load().qk_mmvq_workspace_bytes(len(projs), arr))
+
+
+def qk_mmvq(img, img_row_blocks, T, projs, ws, ws_bytes, d_live_rows=None, stream=None):
     arr = (qk_proj * len(projs))(*projs)
     _check("qk_mmvq", load().qk_mmvq(_ptr(img), img_row_blocks, T, len(projs), arr, _ptr(d_live_rows),
-                                     _stream(stream)))
+                                     _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def qk_device_faults() -> int:
+    v = C.c_uint32(0)
+    _check("qk_device_faults", load().qk_device_faults(C.byref(v)))
+    return int(v.value)
 
 
 def qk_mmvq_id(img, img_row_blocks, rows, k, projs, counts, offsets, items, stream=None):

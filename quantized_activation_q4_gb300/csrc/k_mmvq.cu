@@ -10,105 +10,157 @@
 //   Q4_0: y += d_w * (d_a * D - 8 * s_a),   D = sum nibble_i * q_i
 //   Q8_0: y += d_w * (d_a * D),             D = sum w_i * q_i
 //
-// GB300 design. The exact integer block dot D runs on the f16 tensor path:
-// nibbles, int8 weights and int8 codes are all exact in binary16, products
-// are exact and every partial sum stays below 2^22, so the f32 accumulator
-// holds D exactly. (Blackwell Ultra's int8 MMA and dp4a rates are a quarter
-// of its f16 rate, too low to keep up with HBM at 8 tokens.) A nibble becomes
-// a half in one logic op by OR-ing it under a binary16 exponent (1024 + lo for
-// low nibbles, 64 + hi for high nibbles); the resulting bias sum_i bias * q_i
-// depends only on the token, so one pair of MMAs with a constant -bias A
-// operand per block yields it, and it seeds the accumulator of every row
-// group. Weights stream once from HBM with 128-bit no-L1-allocate loads in a
-// tile order written by qk_weight_pack; the small image is read through L1.
+// Block dot on the f16 tensor path. Nibbles, int8 weights and int8 codes are
+// exact in binary16, products are exact and every partial sum stays below
+// 2^22, so the f32 accumulator of mma.sync m16n8k16 holds the integer D
+// exactly. (Blackwell Ultra's int8 mma and dp4a run at about a quarter of its
+// f16 mma rate -- measured 150 vs 590 T/s -- too slow to keep up with HBM at
+// 8 tokens.) A nibble becomes a half with one logic op by OR-ing it under a
+// binary16 exponent (1024 + lo for low nibbles, 64 + hi for high ones); the
+// bias this adds, sum_i bias * q_i, depends only on the token, so a pair of
+// MMAs with a constant -bias A operand computes it once per block and it
+// seeds the accumulator of all 8 row groups.
 //
-// CTA: NW warps share RG 16-row groups and split their K chunks (128 columns
-// each); partial sums are reduced across warps in shared memory and across
-// the CTAs of a thread-block cluster (split K) through distributed shared
-// memory, always in the same order, so results are deterministic.
-
-#include <cooperative_groups.h>
+// Ordinary path: one persistent CTA per SM. A producer warp streams 128x128
+// weight units with TMA bulk copies (cp.async.bulk, L2 evict-first) into a
+// ring of shared-memory slots guarded by full/empty mbarriers; 15 consumer
+// warps take the units' 32-column blocks round-robin (block j of the CTA's
+// range goes to warp j mod 15), each computing all 128 rows x 8 tokens of its
+// block. Work is split by equal bytes over the CTAs (stream-K): a row tile
+// cut between CTAs leaves partial sums in a small caller workspace, and the
+// last CTA to finish it (atomic counter, reset after use) adds the parts in
+// CTA order. All sums run in a fixed order, so results do not depend on
+// timing or on the live-row count.
 
 #include "qk_internal.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace qk {
 namespace {
 
-constexpr int MAX_PROJ = 8;
-constexpr int NW = 8;   // warps per CTA
-constexpr int RG = 2;   // 16-row groups per CTA
+__device__ unsigned int g_qk_faults = 0;
 
-struct ProjDesc {
-    const uint8_t *w;        // packed tiles (expert 0 for routed)
-    float *y;
-    int64_t y_stride;        // elements between output rows of consecutive tokens / pairs
-    int64_t expert_bytes;    // routed: bytes per expert's packed matrix
-    int N, K;
-    int n_groups;            // ceil(N/16)
-    int chunks;              // ceil(K/128)
-    int row_tiles;           // ceil(n_groups / RG)
-    int experts;             // routed: E; ordinary: 1
-    int tiles_begin;         // first tile index of this projection
+constexpr int MAX_PROJ = 8;
+constexpr int CW = 15;                       // consumer warps (ordinary path); with the
+constexpr int THREADS = (CW + 1) * 32;       // producer, 16 warps = 4 per SM sub-partition
+constexpr int VALS = UNIT_GROUPS * 4 * 32;   // accumulators of one 128-row tile per warp
+constexpr int VPT = (VALS + CW * 32 - 1) / (CW * 32);   // reduced values per consumer thread
+constexpr uint32_t SPIN_LIMIT = 1u << 22;
+
+template <int WT> struct Layout;
+template <> struct Layout<QK_W_Q4_0> {
+    static constexpr int UNIT = Q4_UNIT_BYTES, BLOCK = Q4_BLOCK_STRIDE, SCALES = 8192, SLOTS = 16;
+};
+template <> struct Layout<QK_W_Q8_0> {
+    static constexpr int UNIT = Q8_UNIT_BYTES, BLOCK = Q8_BLOCK_STRIDE, SCALES = 16384, SLOTS = 8;
 };
 
-struct Args {
+struct SkProj {
+    const uint8_t *w;
+    float *y;
+    int64_t y_stride;
+    int64_t unit_base;   // first unit of this projection in the flat unit space
+    int N, K, chunks, row_tiles, rt_base;
+};
+
+struct SkArgs {
     const uint8_t *img;
     int64_t img_row_bytes;
-    int T;                   // image rows (tokens or bucket rows)
-    const int32_t *live;     // ordinary only
+    int T;
+    const int32_t *live;
     int n_proj;
-    int ksplit;              // cluster size along K
-    const int32_t *counts, *offsets, *items;  // routed plan
-    int k;                   // routed: slots per row
-    ProjDesc p[MAX_PROJ];
+    int64_t U;           // total units
+    float *ws_part;      // [G][2][VALS]
+    unsigned int *ws_cnt;
+    SkProj p[MAX_PROJ];
 };
 
-// ---------------------------------------------------------------- helpers
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg_stream16(const void *p) {
     uint4 v;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(p));
     return v;
 }
-__device__ __forceinline__ uint2 ld_stream8(const void *p) {
-    uint2 v;
-    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
 __device__ __forceinline__ uint32_t ld_img4(const uint8_t *p) {
     return __ldg(reinterpret_cast<const unsigned int *>(p));
 }
-
-// D = A * B + C for one m16n8k16 f16 MMA with f32 accumulators.
-__device__ __forceinline__ void mma_f16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ __half2 as_h2(uint32_t v) { return *reinterpret_cast<__half2 *>(&v); }
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
+    uint32_t ok;
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up after SPIN_LIMIT tries, records a fault and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+    for (uint32_t i = 0; i < SPIN_LIMIT; i++)
+        if (mbar_try_wait(a, parity)) return true;
+    atomicOr(&g_qk_faults, 1u);
+    return false;
+}
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory");
 }
 
-// Four int8 codes (bytes c0..c3 of w) -> two exact half2: (c0, c2) and (c1, c3).
-// XOR 0x80 makes u = c + 128 in 1..255; under the exponent of 1024 the half
-// 0x64uu is 1024 + u; subtracting 1152 leaves c exactly.
+// D = A * B + C (m16n8k16, f16 inputs, f32 accumulate); D and C may differ.
+__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1,
+                                        const float c[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+          "f"(c[2]), "f"(c[3]));
+}
+
+// Four int8 codes (bytes c0..c3) -> exact half2 (c0, c2) and (c1, c3):
+// XOR 0x80 gives u = c + 128; the half 0x64uu is 1024 + u; minus 1152 is c.
 __device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &h02, uint32_t &h13) {
     const uint32_t u = w ^ 0x80808080u;
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
     uint32_t a = __byte_perm(u, 0x64646464u, 0x4240);
     uint32_t b = __byte_perm(u, 0x64646464u, 0x4341);
-    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
-    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+    __half2 ha = __hsub2(as_h2(a), bias);
+    __half2 hb = __hsub2(as_h2(b), bias);
     h02 = *reinterpret_cast<uint32_t *>(&ha);
     h13 = *reinterpret_cast<uint32_t *>(&hb);
 }
 
-// Four Q4_0 nibble bytes (B0..B3) -> biased halves for the two MMAs of a block:
-//   lo02 = (1024+lo(B0), 1024+lo(B2)), lo13 = (1024+lo(B1), 1024+lo(B3))
-//   hi02 = (  64+hi(B0),   64+hi(B2)), hi13 = (  64+hi(B1),   64+hi(B3))
+// Q4_0 word (nibble bytes B0..B3) -> biased halves of one row for the two MMAs:
+//   lo02 = (1024+lo B0, 1024+lo B2), lo13 = (1024+lo B1, 1024+lo B3)
+//   hi02 = (  64+hi B0,   64+hi B2), hi13 = (  64+hi B1,   64+hi B3)
 __device__ __forceinline__ void nibbles_to_half2(uint32_t w, uint32_t &lo02, uint32_t &lo13,
                                                  uint32_t &hi02, uint32_t &hi13) {
     const uint32_t w8 = w >> 8;
@@ -118,273 +170,408 @@ __device__ __forceinline__ void nibbles_to_half2(uint32_t w, uint32_t &lo02, uin
     hi13 = (w8 & 0x00F000F0u) | 0x54005400u;
 }
 
-// Q8_0 weight codes keep the +1152 bias (removed by the correction MMAs).
+// Q8_0 weight codes keep their +1152 bias (removed by the correction MMAs).
 __device__ __forceinline__ void wcodes_to_half2(uint32_t w, uint32_t &h02, uint32_t &h13) {
     const uint32_t u = w ^ 0x80808080u;
     h02 = __byte_perm(u, 0x64646464u, 0x4240);
     h13 = __byte_perm(u, 0x64646464u, 0x4341);
 }
 
-__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu))); }
-__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+// ---------------------------------------------------------------- one block
+// Activation side of block b for this lane: B fragments of token g (elements
+// 4t..4t+3 and 16+4t..16+4t+3), scales of tokens 2t and 2t+1, and the bias
+// correction shared by every row group.
+struct BSide {
+    uint32_t lo02, lo13, hi02, hi13;
+    float da0, da1, ns0, ns1;
+    float corr[4];
+};
 
-// ---------------------------------------------------------------- the kernel
-//
-// Fragment map (m16n8k16, lane = 4g + t): A rows g and g+8, B column (token) g,
-// C rows g, g+8 and columns (tokens) 2t, 2t+1. Within a 32-block, MMA 0 takes
-// the elements 4t..4t+3 and MMA 1 the elements 16+4t..16+4t+3, in the order
-// (4t, 4t+2 | 4t+1, 4t+3) on both the A and the B side.
-template <int WT, bool ROUTED>
-__global__ void __launch_bounds__(NW * 32) mmvq_kernel(const __grid_constant__ Args args) {
-    constexpr int TILE = WT == QK_W_Q4_0 ? Q4_TILE_BYTES : Q8_TILE_BYTES;
-    constexpr int SCALE_OFF = WT == QK_W_Q4_0 ? 1024 : 2048;
-    constexpr int HALF_OFF = WT == QK_W_Q4_0 ? 512 : 1024;   // rows g+8
-    // constant A operand of the correction MMAs (-bias of each half)
-    constexpr uint32_t NEG_BIAS_LO = WT == QK_W_Q4_0 ? 0xE400E400u : 0xE480E480u;  // -1024 | -1152
-    constexpr uint32_t NEG_BIAS_HI = WT == QK_W_Q4_0 ? 0xD400D400u : 0xE480E480u;  //   -64 | -1152
-
-    __shared__ float red[NW][RG * 4][32];
-    __shared__ int tok_img[8], tok_out[8];
-
-    const int C = args.ksplit;
-    const int rank = (int)(blockIdx.x % (unsigned)C);
-    const int tile = (int)(blockIdx.x / (unsigned)C);
-    int j = 0;
-#pragma unroll 1
-    while (j + 1 < args.n_proj && tile >= args.p[j + 1].tiles_begin) j++;
-    const ProjDesc &P = args.p[j];
-    const int local = tile - P.tiles_begin;
-    const int e = ROUTED ? local / P.row_tiles : 0;
-    const int rt = ROUTED ? local % P.row_tiles : local;
-    const int g0 = rt * RG;
-
-    int n_items = 0, item0 = 0;
-    if (ROUTED) {
-        n_items = __ldg(args.counts + e);
-        if (n_items <= 0) return;          // uniform over the cluster: no weights read
-        item0 = __ldg(args.offsets + e);
+template <int WT>
+__device__ __forceinline__ void bside(const uint8_t *imgB, const uint8_t *imgS0, const uint8_t *imgS1,
+                                      int b, int t4, BSide &s) {
+    constexpr uint32_t NEG_LO = WT == QK_W_Q4_0 ? 0xE400E400u : 0xE480E480u;  // -1024 | -1152
+    constexpr uint32_t NEG_HI = WT == QK_W_Q4_0 ? 0xD400D400u : 0xE480E480u;  //   -64 | -1152
+    s.lo02 = s.lo13 = s.hi02 = s.hi13 = 0u;
+    if (imgB) {
+        const uint8_t *blk = imgB + (int64_t)b * Q8_1_BYTES;
+        codes_to_half2(ld_img4(blk + 4 + 4 * t4), s.lo02, s.lo13);
+        codes_to_half2(ld_img4(blk + 20 + 4 * t4), s.hi02, s.hi13);
     }
-    const uint8_t *wbase = P.w + (ROUTED ? (int64_t)e * P.expert_bytes : 0);
+    s.da0 = s.da1 = s.ns0 = s.ns1 = 0.0f;
+    if (imgS0) {
+        const float2 ds = __half22float2(as_h2(ld_img4(imgS0 + (int64_t)b * Q8_1_BYTES)));
+        s.da0 = ds.x;
+        if (WT == QK_W_Q4_0) s.ns0 = -8.0f * ds.y;
+    }
+    if (imgS1) {
+        const float2 ds = __half22float2(as_h2(ld_img4(imgS1 + (int64_t)b * Q8_1_BYTES)));
+        s.da1 = ds.x;
+        if (WT == QK_W_Q4_0) s.ns1 = -8.0f * ds.y;
+    }
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t alo[4] = {NEG_LO, NEG_LO, NEG_LO, NEG_LO};
+    const uint32_t ahi[4] = {NEG_HI, NEG_HI, NEG_HI, NEG_HI};
+    float c1[4];
+    mma_f16(c1, alo, s.lo02, s.lo13, zero);
+    mma_f16(s.corr, ahi, s.hi02, s.hi13, c1);
+}
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int Kb = P.K / QB;
-    const int per = (P.chunks + C - 1) / C;
-    const int c_begin = rank * per;
-    const int c_end = min(P.chunks, c_begin + per);
-    const int n_passes = ROUTED ? (n_items + 7) / 8 : 1;
+// Row group: two MMAs seeded with the correction, then the scale epilogue.
+__device__ __forceinline__ void row_group(const uint32_t a_lo[4], const uint32_t a_hi[4], uint32_t dw2,
+                                          const BSide &s, float acc[4]) {
+    float d1[4], dv[4];
+    mma_f16(d1, a_lo, s.lo02, s.lo13, s.corr);
+    mma_f16(dv, a_hi, s.hi02, s.hi13, d1);
+    const float2 dw = __half22float2(as_h2(dw2));   // (row g, row g+8)
+    acc[0] = fmaf(dw.x, fmaf(s.da0, dv[0], s.ns0), acc[0]);
+    acc[1] = fmaf(dw.x, fmaf(s.da1, dv[1], s.ns1), acc[1]);
+    acc[2] = fmaf(dw.y, fmaf(s.da0, dv[2], s.ns0), acc[2]);
+    acc[3] = fmaf(dw.y, fmaf(s.da1, dv[3], s.ns1), acc[3]);
+}
 
-    for (int pass = 0; pass < n_passes; pass++) {
-        if (threadIdx.x < 8) {
-            const int s = threadIdx.x;
-            if (ROUTED) {
-                const int idx = pass * 8 + s;
-                int p = idx < n_items ? __ldg(args.items + item0 + idx) : -1;
-                if (p < 0 || p / args.k >= args.T) p = -1;     // not a pair of this bucket: skip
-                tok_img[s] = p >= 0 ? p / args.k : -1;
-                tok_out[s] = p;
-            } else {
-                const int tl = live_rows(args.live, args.T);
-                tok_img[s] = s < tl ? s : -1;
-                tok_out[s] = s < tl ? s : -1;
+// All 8 row groups of one block, from shared memory (SMEM, 32-bit shared
+// addresses) or with streaming global loads.
+template <int WT, bool SMEM>
+__device__ __forceinline__ void block_rows(const uint8_t *gblk, uint32_t sblk, const uint8_t *gsc, uint32_t ssc,
+                                           int lane, const BSide &s, float acc[UNIT_GROUPS][4]) {
+    const int g = lane >> 2;
+    uint4 sc0, sc1;
+    if (SMEM) {
+        sc0 = lds128(ssc + g * 32);
+        sc1 = lds128(ssc + g * 32 + 16);
+    } else {
+        sc0 = ldg_stream16(gsc + g * 32);
+        sc1 = ldg_stream16(gsc + g * 32 + 16);
+    }
+    const uint32_t scw[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
+    if (WT == QK_W_Q4_0) {
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint4 v = SMEM ? lds128(sblk + k * 512 + lane * 16) : ldg_stream16(gblk + k * 512 + lane * 16);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const uint32_t wg = h ? v.z : v.x, wg8 = h ? v.w : v.y;
+                uint32_t a_lo[4], a_hi[4];
+                nibbles_to_half2(wg, a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
+                nibbles_to_half2(wg8, a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
+                row_group(a_lo, a_hi, scw[2 * k + h], s, acc[2 * k + h]);
             }
         }
-        __syncthreads();
-        const int rowB = tok_img[g];
-        const int rowS0 = tok_img[2 * t4], rowS1 = tok_img[2 * t4 + 1];
-        const uint8_t *imgB = rowB >= 0 ? args.img + (int64_t)rowB * args.img_row_bytes : nullptr;
-        const uint8_t *imgS0 = rowS0 >= 0 ? args.img + (int64_t)rowS0 * args.img_row_bytes : nullptr;
-        const uint8_t *imgS1 = rowS1 >= 0 ? args.img + (int64_t)rowS1 * args.img_row_bytes : nullptr;
-
-        float acc[RG][4];
+    } else {
 #pragma unroll
-        for (int r = 0; r < RG; r++)
+        for (int k = 0; k < 8; k++) {
+            const uint4 v = SMEM ? lds128(sblk + k * 512 + lane * 16) : ldg_stream16(gblk + k * 512 + lane * 16);
+            uint32_t a_lo[4], a_hi[4];
+            wcodes_to_half2(v.x, a_lo[0], a_lo[2]);
+            wcodes_to_half2(v.y, a_hi[0], a_hi[2]);
+            wcodes_to_half2(v.z, a_lo[1], a_lo[3]);
+            wcodes_to_half2(v.w, a_hi[1], a_hi[3]);
+            row_group(a_lo, a_hi, scw[k], s, acc[k]);
+        }
+    }
+}
+
+// Output position of accumulator value v (0..VALS-1) of a 128-row tile.
+__device__ __forceinline__ void val_pos(int v, int &row, int &slot) {
+    const int l = v & 31, i = (v >> 5) & 3, r = v >> 7;
+    row = 16 * r + (l >> 2) + ((i & 2) ? 8 : 0);
+    slot = 2 * (l & 3) + (i & 1);
+}
+
+__device__ __forceinline__ int64_t cta_start(int c, int64_t U, int G) { return ((int64_t)c * U) / G; }
+__device__ __forceinline__ int cta_of(int64_t u, int64_t U, int G) {
+    int c = (int)((u * G) / U);
+    while (c + 1 < G && cta_start(c + 1, U, G) <= u) c++;
+    while (c > 0 && cta_start(c, U, G) > u) c--;
+    return c;
+}
+
+// ---------------------------------------------------------------- ordinary path
+template <int WT>
+__global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_constant__ SkArgs a) {
+    using L = Layout<WT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ring = smem;
+    float *red = reinterpret_cast<float *>(smem + L::SLOTS * L::UNIT);
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + CW * VALS);
+    uint64_t *empty = full + L::SLOTS;
+    __shared__ int s_last;
+
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int64_t u0 = cta_start(cta, a.U, G), u1 = cta_start(cta + 1, a.U, G);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::SLOTS; s++) {
+            mbar_init(smem_addr(full + s), 1);
+            mbar_init(smem_addr(empty + s), 4);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto decode = [&](int64_t u, int &j, int &rt, int &c) {
+        j = 0;
+        while (j + 1 < a.n_proj && u >= a.p[j + 1].unit_base) j++;
+        const int64_t local = u - a.p[j].unit_base;
+        rt = (int)(local / a.p[j].chunks);
+        c = (int)(local % a.p[j].chunks);
+    };
+
+    if (warp == CW) {   // ---------------- producer
+        if (lane == 0) {
+            const uint64_t pol = evict_first_policy();
+            for (int64_t i = 0; u0 + i < u1; i++) {
+                const int slot = (int)(i % L::SLOTS);
+                const uint32_t n = (uint32_t)(i / L::SLOTS);
+                if (n > 0 && !mbar_wait(smem_addr(empty + slot), (n - 1) & 1u)) break;
+                int j, rt, c;
+                decode(u0 + i, j, rt, c);
+                const uint8_t *src = a.p[j].w + ((int64_t)rt * a.p[j].chunks + c) * L::UNIT;
+                mbar_expect_tx(smem_addr(full + slot), L::UNIT);
+                bulk_g2s(smem_addr(ring + (size_t)slot * L::UNIT), src, L::UNIT, smem_addr(full + slot), pol);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int g = lane >> 2, t4 = lane & 3, tid = threadIdx.x;
+    const int tl = live_rows(a.live, a.T);
+    const uint8_t *imgB = g < tl ? a.img + (int64_t)g * a.img_row_bytes : nullptr;
+    const uint8_t *imgS0 = 2 * t4 < tl ? a.img + (int64_t)(2 * t4) * a.img_row_bytes : nullptr;
+    const uint8_t *imgS1 = 2 * t4 + 1 < tl ? a.img + (int64_t)(2 * t4 + 1) * a.img_row_bytes : nullptr;
+    bool ok = true;
+
+    for (int64_t u = u0; u < u1;) {
+        int j, rt, c0;
+        decode(u, j, rt, c0);
+        const SkProj &P = a.p[j];
+        const int64_t rt_start = P.unit_base + (int64_t)rt * P.chunks, rt_end = rt_start + P.chunks;
+        const int64_t s1 = u1 < rt_end ? u1 : rt_end;
+        const int nblk = (int)(4 * (s1 - u));
+        const int Kb = P.K / QB;
+        float acc[UNIT_GROUPS][4];
+#pragma unroll
+        for (int r = 0; r < UNIT_GROUPS; r++)
 #pragma unroll
             for (int i = 0; i < 4; i++) acc[r][i] = 0.0f;
 
-        for (int c = c_begin + warp; c < c_end; c += NW) {
-            // weights of this chunk for every row group (issued first: HBM latency)
-            uint4 wv[RG][WT == QK_W_Q4_0 ? 2 : 4];
-            uint2 sv[RG][2];
-#pragma unroll
-            for (int r = 0; r < RG; r++) {
-                if (g0 + r < P.n_groups) {
-                    const uint8_t *tp = wbase + ((int64_t)(g0 + r) * P.chunks + c) * TILE;
-                    if (WT == QK_W_Q4_0) {
-                        wv[r][0] = ld_stream16(tp + lane * 16);
-                        wv[r][1] = ld_stream16(tp + HALF_OFF + lane * 16);
-                    } else {
-                        wv[r][0] = ld_stream16(tp + lane * 32);
-                        wv[r][1] = ld_stream16(tp + lane * 32 + 16);
-                        wv[r][2] = ld_stream16(tp + HALF_OFF + lane * 32);
-                        wv[r][3] = ld_stream16(tp + HALF_OFF + lane * 32 + 16);
-                    }
-                    sv[r][0] = ld_stream8(tp + SCALE_OFF + g * 8);
-                    sv[r][1] = ld_stream8(tp + SCALE_OFF + (g + 8) * 8);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < (WT == QK_W_Q4_0 ? 2 : 4); i++) wv[r][i] = make_uint4(0, 0, 0, 0);
-                    sv[r][0] = sv[r][1] = make_uint2(0, 0);
-                }
+        for (int jj = warp; jj < nblk; jj += CW) {
+            const int64_t i = (u - u0) + (jj >> 2);
+            const int slot = (int)(i % L::SLOTS);
+            if (ok) ok = mbar_wait(smem_addr(full + slot), (uint32_t)(i / L::SLOTS) & 1u);
+            const int jb = jj & 3;
+            const int b = 4 * (c0 + (jj >> 2)) + jb;
+            if (ok && b < Kb) {
+                BSide s;
+                bside<WT>(imgB, imgS0, imgS1, b, t4, s);
+                const uint32_t ub = smem_addr(ring + (size_t)slot * L::UNIT);
+                block_rows<WT, true>(nullptr, ub + jb * L::BLOCK, nullptr, ub + L::SCALES + jb * 256, lane, s, acc);
             }
-#pragma unroll
-            for (int jb = 0; jb < 4; jb++) {
-                const int b = 4 * c + jb;
-                if (b >= Kb) break;
-                // B side: this lane's token g, elements 4t..4t+3 and 16+4t..16+4t+3
-                uint32_t blo02 = 0, blo13 = 0, bhi02 = 0, bhi13 = 0;
-                if (imgB) {
-                    const uint8_t *blk = imgB + (int64_t)b * Q8_1_BYTES;
-                    codes_to_half2(ld_img4(blk + 4 + 4 * t4), blo02, blo13);
-                    codes_to_half2(ld_img4(blk + 20 + 4 * t4), bhi02, bhi13);
-                }
-                // activation scales of tokens 2t and 2t+1
-                float da0 = 0.f, da1 = 0.f, ns0 = 0.f, ns1 = 0.f;
-                if (imgS0) {
-                    const uint32_t ds = ld_img4(imgS0 + (int64_t)b * Q8_1_BYTES);
-                    da0 = half_lo(ds);
-                    if (WT == QK_W_Q4_0) ns0 = -8.0f * half_hi(ds);
-                }
-                if (imgS1) {
-                    const uint32_t ds = ld_img4(imgS1 + (int64_t)b * Q8_1_BYTES);
-                    da1 = half_lo(ds);
-                    if (WT == QK_W_Q4_0) ns1 = -8.0f * half_hi(ds);
-                }
-                // bias correction: -sum(bias_i * q_i) per token, same for every row
-                float corr[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_f16(corr, NEG_BIAS_LO, NEG_BIAS_LO, NEG_BIAS_LO, NEG_BIAS_LO, blo02, blo13);
-                mma_f16(corr, NEG_BIAS_HI, NEG_BIAS_HI, NEG_BIAS_HI, NEG_BIAS_HI, bhi02, bhi13);
-#pragma unroll
-                for (int r = 0; r < RG; r++) {
-                    uint32_t a_lo[4], a_hi[4];  // {row g k0, row g+8 k0, row g k8, row g+8 k8}
-                    if (WT == QK_W_Q4_0) {
-                        const uint32_t wg = (&wv[r][0].x)[jb];
-                        const uint32_t wg8 = (&wv[r][1].x)[jb];
-                        nibbles_to_half2(wg, a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
-                        nibbles_to_half2(wg8, a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
-                    } else {
-                        const uint32_t *vg = &wv[r][jb >> 1].x + 2 * (jb & 1);
-                        const uint32_t *vg8 = &wv[r][2 + (jb >> 1)].x + 2 * (jb & 1);
-                        wcodes_to_half2(vg[0], a_lo[0], a_lo[2]);
-                        wcodes_to_half2(vg[1], a_hi[0], a_hi[2]);
-                        wcodes_to_half2(vg8[0], a_lo[1], a_lo[3]);
-                        wcodes_to_half2(vg8[1], a_hi[1], a_hi[3]);
-                    }
-                    float dv[4] = {corr[0], corr[1], corr[2], corr[3]};
-                    mma_f16(dv, a_lo[0], a_lo[1], a_lo[2], a_lo[3], blo02, blo13);
-                    mma_f16(dv, a_hi[0], a_hi[1], a_hi[2], a_hi[3], bhi02, bhi13);
-                    const uint32_t sg = (jb < 2) ? sv[r][0].x : sv[r][0].y;
-                    const uint32_t sg8 = (jb < 2) ? sv[r][1].x : sv[r][1].y;
-                    const float dwg = (jb & 1) ? half_hi(sg) : half_lo(sg);
-                    const float dwg8 = (jb & 1) ? half_hi(sg8) : half_lo(sg8);
-                    acc[r][0] = fmaf(dwg, fmaf(da0, dv[0], ns0), acc[r][0]);
-                    acc[r][1] = fmaf(dwg, fmaf(da1, dv[1], ns1), acc[r][1]);
-                    acc[r][2] = fmaf(dwg8, fmaf(da0, dv[2], ns0), acc[r][2]);
-                    acc[r][3] = fmaf(dwg8, fmaf(da1, dv[3], ns1), acc[r][3]);
-                }
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(empty + slot));
         }
 
-        // reduce: warps (fixed order), then cluster ranks (fixed order)
+        // CTA reduction over the consumer warps, fixed order
 #pragma unroll
-        for (int r = 0; r < RG; r++)
+        for (int r = 0; r < UNIT_GROUPS; r++)
 #pragma unroll
-            for (int i = 0; i < 4; i++) red[warp][r * 4 + i][lane] = acc[r][i];
-        __syncthreads();
-        float *part = &red[0][0][0];
-        for (int v = threadIdx.x; v < RG * 4 * 32; v += NW * 32) {
-            float s = 0.0f;
+            for (int i = 0; i < 4; i++) red[warp * VALS + (r * 4 + i) * 32 + lane] = acc[r][i];
+        consumer_sync();
+        float v[VPT];
 #pragma unroll
-            for (int w = 0; w < NW; w++) s += (&red[w][0][0])[v];
-            part[v] = s;   // each v is read and written by one thread only
-        }
-        if (C > 1) {
-            cg::cluster_group cluster = cg::this_cluster();
-            cluster.sync();
-            if (rank == 0) {
-                for (int v = threadIdx.x; v < RG * 4 * 32; v += NW * 32) {
-                    float s = part[v];
-                    for (int q = 1; q < C; q++) s += cluster.map_shared_rank(part, q)[v];
-                    part[v] = s;
-                }
+        for (int q = 0; q < VPT; q++) {
+            const int t = tid + q * CW * 32;
+            float sum = 0.0f;
+            if (t < VALS) {
+#pragma unroll
+                for (int w = 0; w < CW; w++) sum += red[w * VALS + t];
             }
-            cluster.sync();
+            v[q] = sum;
+        }
+        const int row0 = rt * UNIT_ROWS;
+        if (u == rt_start && s1 == rt_end) {
+#pragma unroll
+            for (int q = 0; q < VPT; q++) {
+                const int t = tid + q * CW * 32;
+                if (t >= VALS) break;
+                int row, slot;
+                val_pos(t, row, slot);
+                row += row0;
+                if (row < P.N && slot < tl) P.y[(int64_t)slot * P.y_stride + row] = v[q];
+            }
         } else {
-            __syncthreads();
-        }
-        if (rank == 0) {
-            for (int v = threadIdx.x; v < RG * 4 * 32; v += NW * 32) {
-                const int l = v & 31, ri = v >> 5, r = ri >> 2, i = ri & 3;
-                const int row = (g0 + r) * 16 + (l >> 2) + ((i & 2) ? 8 : 0);
-                const int slot = 2 * (l & 3) + (i & 1);
-                const int orow = tok_out[slot];
-                if (row < P.N && orow >= 0) P.y[(int64_t)orow * P.y_stride + row] = part[v];
+            // partial row tile: publish it; the last contributor finishes the tile
+            const int R = P.rt_base + rt;
+            const int part_slot = u0 >= rt_start ? 0 : 1;
+            float *mine = a.ws_part + ((int64_t)cta * 2 + part_slot) * VALS;
+#pragma unroll
+            for (int q = 0; q < VPT; q++)
+                if (tid + q * CW * 32 < VALS) mine[tid + q * CW * 32] = v[q];
+            __threadfence();
+            consumer_sync();
+            const int c_first = cta_of(rt_start, a.U, G), c_last = cta_of(rt_end - 1, a.U, G);
+            if (tid == 0) {
+                const unsigned old = atomicAdd(a.ws_cnt + R, 1u);
+                s_last = old == (unsigned)(c_last - c_first);
+            }
+            consumer_sync();
+            if (s_last) {
+                __threadfence();
+#pragma unroll
+                for (int q = 0; q < VPT; q++) {
+                    const int t = tid + q * CW * 32;
+                    if (t >= VALS) break;
+                    float sum = 0.0f;
+                    for (int cc = c_first; cc <= c_last; cc++) {
+                        const int ps = cta_start(cc, a.U, G) >= rt_start ? 0 : 1;
+                        sum += __ldcg(a.ws_part + ((int64_t)cc * 2 + ps) * VALS + t);
+                    }
+                    int row, slot;
+                    val_pos(t, row, slot);
+                    row += row0;
+                    if (row < P.N && slot < tl) P.y[(int64_t)slot * P.y_stride + row] = sum;
+                }
+                if (tid == 0) a.ws_cnt[R] = 0u;
             }
         }
-        __syncthreads();   // tok_* and red reused by the next pass
+        consumer_sync();   // red is rewritten by the next row tile
+        u = s1;
+    }
+}
+
+// ---------------------------------------------------------------- routed path
+// One CTA of 8 warps per (projection, expert, 128-row tile). Experts with no
+// planned pair return at once. Warps take the K blocks round-robin, reading
+// the expert's packed units from global memory, and reduce in shared memory
+// in fixed warp order. Up to 8 planned pairs per pass; more pairs re-run the
+// pass (the weights then come from L2).
+constexpr int RW = 8;
+
+struct IdProj {
+    const uint8_t *w;
+    float *y;
+    int64_t expert_bytes;
+    int N, K, chunks, row_tiles, tiles_begin;
+};
+struct IdArgs {
+    const uint8_t *img;
+    int64_t img_row_bytes;
+    int rows, k, n_proj;
+    const int32_t *counts, *offsets, *items;
+    IdProj p[MAX_PROJ];
+};
+
+template <int WT>
+__global__ void __launch_bounds__(RW * 32) mmvq_id_kernel(const __grid_constant__ IdArgs a) {
+    using L = Layout<WT>;
+    extern __shared__ __align__(16) float red_id[];   // [RW][VALS]
+    __shared__ int tok_img[8], tok_out[8];
+    const int tile = blockIdx.x;
+    int j = 0;
+    while (j + 1 < a.n_proj && tile >= a.p[j + 1].tiles_begin) j++;
+    const IdProj &P = a.p[j];
+    const int local = tile - P.tiles_begin;
+    const int e = local / P.row_tiles, rt = local % P.row_tiles;
+    const int n_items = __ldg(a.counts + e);
+    if (n_items <= 0) return;   // no planned pair: no weights read
+    const int item0 = __ldg(a.offsets + e);
+    const uint8_t *wbase = P.w + (int64_t)e * P.expert_bytes + (int64_t)rt * P.chunks * L::UNIT;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t4 = lane & 3, g = lane >> 2;
+    const int Kb = P.K / QB;
+
+    for (int pass = 0; pass * 8 < n_items; pass++) {
+        if (threadIdx.x < 8) {
+            const int idx = pass * 8 + threadIdx.x;
+            int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
+            if (p < 0 || p / a.k >= a.rows) p = -1;   // not a pair of this bucket: skip
+            tok_img[threadIdx.x] = p >= 0 ? p / a.k : -1;
+            tok_out[threadIdx.x] = p;
+        }
+        __syncthreads();
+        const int rB = tok_img[g], rS0 = tok_img[2 * t4], rS1 = tok_img[2 * t4 + 1];
+        const uint8_t *imgB = rB >= 0 ? a.img + (int64_t)rB * a.img_row_bytes : nullptr;
+        const uint8_t *imgS0 = rS0 >= 0 ? a.img + (int64_t)rS0 * a.img_row_bytes : nullptr;
+        const uint8_t *imgS1 = rS1 >= 0 ? a.img + (int64_t)rS1 * a.img_row_bytes : nullptr;
+        float acc[UNIT_GROUPS][4];
+#pragma unroll
+        for (int r = 0; r < UNIT_GROUPS; r++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) acc[r][i] = 0.0f;
+        for (int b = warp; b < Kb; b += RW) {
+            const uint8_t *unit = wbase + (int64_t)(b >> 2) * L::UNIT;
+            BSide s;
+            bside<WT>(imgB, imgS0, imgS1, b, t4, s);
+            block_rows<WT, false>(unit + (b & 3) * L::BLOCK, 0, unit + L::SCALES + (b & 3) * 256, 0, lane, s, acc);
+        }
+#pragma unroll
+        for (int r = 0; r < UNIT_GROUPS; r++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) red_id[warp * VALS + (r * 4 + i) * 32 + lane] = acc[r][i];
+        __syncthreads();
+        for (int t = threadIdx.x; t < VALS; t += RW * 32) {
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < RW; w++) sum += red_id[w * VALS + t];
+            int row, slot;
+            val_pos(t, row, slot);
+            row += rt * UNIT_ROWS;
+            const int orow = tok_out[slot];
+            if (row < P.N && orow >= 0) P.y[(int64_t)orow * P.N + row] = sum;
+        }
+        __syncthreads();   // tok_* and red_id are reused by the next pass
     }
 }
 
 // ---------------------------------------------------------------- weight pack
-// One CTA of 128 threads per 16x128 tile. Canonical source blocks are read
-// byte by byte (18- and 34-byte blocks are only 2-byte aligned).
+// One CTA of 256 threads per 128x128 unit. Canonical blocks are only 2-byte
+// aligned, so they are read byte by byte.
 template <int WT>
-__global__ void __launch_bounds__(128) pack_kernel(const uint8_t *__restrict__ src, int N, int K,
-                                                   int chunks, uint8_t *__restrict__ dst) {
-    constexpr int TILE = WT == QK_W_Q4_0 ? Q4_TILE_BYTES : Q8_TILE_BYTES;
+__global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ src, int N, int K, int chunks,
+                                                   uint8_t *__restrict__ dst) {
+    using L = Layout<WT>;
     constexpr int SB = WT == QK_W_Q4_0 ? Q4_0_BYTES : Q8_0_BYTES;
-    constexpr int SCALE_OFF = WT == QK_W_Q4_0 ? 1024 : 2048;
-    const int64_t tile = blockIdx.x;
-    const int grp = (int)(tile / chunks), c = (int)(tile % chunks);
+    constexpr int REGIONS = WT == QK_W_Q4_0 ? 4 : 8;
+    const int64_t unit = blockIdx.x;
+    const int rt = (int)(unit / chunks), c = (int)(unit % chunks);
     const int Kb = K / QB;
-    uint8_t *out = dst + tile * TILE;
-    const int tid = threadIdx.x;
+    uint8_t *out = dst + unit * L::UNIT;
     auto byte_at = [&](int n, int b, int off) -> uint32_t {
         if (n >= N || b >= Kb) return 0u;
         return src[((int64_t)n * Kb + b) * SB + off];
     };
-    if (tid < 64) {
-        const int half = tid >> 5, l = tid & 31, gg = l >> 2, t = l & 3;
-        const int n = grp * 16 + gg + 8 * half;
+    auto word_at = [&](int n, int b, int off) -> uint32_t {
+        return byte_at(n, b, off) | (byte_at(n, b, off + 1) << 8) | (byte_at(n, b, off + 2) << 16) |
+               (byte_at(n, b, off + 3) << 24);
+    };
+    const int n0 = rt * UNIT_ROWS;
+    for (int idx = threadIdx.x; idx < 4 * REGIONS * 32; idx += 256) {
+        const int jb = idx / (REGIONS * 32), k = (idx / 32) % REGIONS, l = idx % 32, g = l >> 2, t = l & 3;
+        const int b = 4 * c + jb;
+        uint4 v;
         if (WT == QK_W_Q4_0) {
-            uint32_t v[4];
-            for (int jb = 0; jb < 4; jb++) {
-                const int b = 4 * c + jb;
-                v[jb] = byte_at(n, b, 2 + 4 * t) | (byte_at(n, b, 3 + 4 * t) << 8) |
-                        (byte_at(n, b, 4 + 4 * t) << 16) | (byte_at(n, b, 5 + 4 * t) << 24);
-            }
-            *reinterpret_cast<uint4 *>(out + half * 512 + l * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+            const int off = 2 + 4 * t;
+            v.x = word_at(n0 + 32 * k + g, b, off);
+            v.y = word_at(n0 + 32 * k + g + 8, b, off);
+            v.z = word_at(n0 + 32 * k + 16 + g, b, off);
+            v.w = word_at(n0 + 32 * k + 24 + g, b, off);
         } else {
-            uint32_t v[8];
-            for (int jb = 0; jb < 4; jb++) {
-                const int b = 4 * c + jb;
-                for (int h = 0; h < 2; h++) {
-                    const int o = 2 + 16 * h + 4 * t;
-                    v[2 * jb + h] = byte_at(n, b, o) | (byte_at(n, b, o + 1) << 8) |
-                                    (byte_at(n, b, o + 2) << 16) | (byte_at(n, b, o + 3) << 24);
-                }
-            }
-            uint4 *o4 = reinterpret_cast<uint4 *>(out + half * 1024 + l * 32);
-            o4[0] = make_uint4(v[0], v[1], v[2], v[3]);
-            o4[1] = make_uint4(v[4], v[5], v[6], v[7]);
+            v.x = word_at(n0 + 16 * k + g, b, 2 + 4 * t);
+            v.y = word_at(n0 + 16 * k + g, b, 18 + 4 * t);
+            v.z = word_at(n0 + 16 * k + g + 8, b, 2 + 4 * t);
+            v.w = word_at(n0 + 16 * k + g + 8, b, 18 + 4 * t);
         }
-    } else if (tid < 80) {
-        const int r = tid - 64, n = grp * 16 + r;
-        uint16_t h[4];
-        for (int jb = 0; jb < 4; jb++) {
-            const int b = 4 * c + jb;
-            h[jb] = (uint16_t)(byte_at(n, b, 0) | (byte_at(n, b, 1) << 8));
-        }
-        *reinterpret_cast<uint2 *>(out + SCALE_OFF + r * 8) =
-            make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+        *reinterpret_cast<uint4 *>(out + jb * L::BLOCK + k * 512 + l * 16) = v;
     }
-}
-
-// Split K over a cluster so that the grid holds at least ~4 CTAs per SM.
-int pick_ksplit(int64_t tiles, int chunks, int n_sm) {
-    int C = 1;
-    while (C < 8 && tiles * C < 4LL * n_sm && chunks >= 2 * C * NW) C *= 2;
-    return C;
+    // scales: block jb, lane group g, row group r -> half2 (row 16r+g, row 16r+g+8)
+    for (int idx = threadIdx.x; idx < 4 * 8 * 8; idx += 256) {
+        const int jb = idx / 64, g = (idx / 8) % 8, r = idx % 8;
+        const int b = 4 * c + jb, n = n0 + 16 * r + g;
+        const uint32_t lo = byte_at(n, b, 0) | (byte_at(n, b, 1) << 8);
+        const uint32_t hi = byte_at(n + 8, b, 0) | (byte_at(n + 8, b, 1) << 8);
+        *reinterpret_cast<uint32_t *>(out + L::SCALES + jb * 256 + g * 32 + r * 4) = lo | (hi << 16);
+    }
 }
 
 int sm_count() {
@@ -398,105 +585,129 @@ int sm_count() {
     return n;
 }
 
-template <int WT, bool ROUTED>
-qk_status launch(const Args &a, int64_t tiles, cudaStream_t s) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3((unsigned)(tiles * a.ksplit));
-    cfg.blockDim = dim3(NW * 32);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cfg.numAttrs = 0;
-    if (a.ksplit > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)a.ksplit;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    cudaError_t err = cudaLaunchKernelEx(&cfg, mmvq_kernel<WT, ROUTED>, a);
-    count_launch();
-    if (err != cudaSuccess) return fail(QK_ERR_CUDA, "%s: %s", ROUTED ? "mmvq_id" : "mmvq", cudaGetErrorString(err));
-    return check_launch(ROUTED ? "mmvq_id" : "mmvq");
+template <int WT>
+size_t sk_smem() {
+    using L = Layout<WT>;
+    return (size_t)L::SLOTS * L::UNIT + (size_t)CW * VALS * sizeof(float) + 2 * L::SLOTS * sizeof(uint64_t);
 }
 
 }  // namespace
 
-qk_status launch_weight_pack(int wtype, const uint8_t *blocks, int64_t N, int64_t K,
-                             uint8_t *packed, cudaStream_t s) {
-    const int64_t chunks = ceil_div(K, TILE_COLS);
-    const int64_t tiles = ceil_div(N, TILE_ROWS) * chunks;
-    if (tiles == 0) return QK_OK;
+// Workspace of the ordinary path: [G][2][VALS] partial sums, then one counter
+// per 128-row tile; G = min(units, SMs) CTAs.
+int64_t mmvq_workspace_bytes(int n_proj, const qk_proj *projs) {
+    int64_t U = 0, R = 0;
+    for (int j = 0; j < n_proj; j++) {
+        const int64_t rts = ceil_div(projs[j].N, UNIT_ROWS);
+        U += rts * ceil_div(projs[j].K, UNIT_COLS);
+        R += rts;
+    }
+    const int64_t G = U < sm_count() ? U : sm_count();
+    return G * 2 * VALS * (int64_t)sizeof(float) + R * (int64_t)sizeof(unsigned int);
+}
+
+qk_status read_device_faults(uint32_t *faults) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_qk_faults, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_qk_faults, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(QK_ERR_CUDA, "qk_device_faults: %s", cudaGetErrorString(e));
+    *faults = v;
+    return QK_OK;
+}
+
+qk_status launch_weight_pack(int wtype, const uint8_t *blocks, int64_t N, int64_t K, uint8_t *packed,
+                             cudaStream_t s) {
+    const int64_t chunks = ceil_div(K, UNIT_COLS);
+    const int64_t units = ceil_div(N, UNIT_ROWS) * chunks;
+    if (units == 0) return QK_OK;
     if (wtype == QK_W_Q4_0)
-        pack_kernel<QK_W_Q4_0><<<(unsigned)tiles, 128, 0, s>>>(blocks, (int)N, (int)K, (int)chunks, packed);
+        pack_kernel<QK_W_Q4_0><<<(unsigned)units, 256, 0, s>>>(blocks, (int)N, (int)K, (int)chunks, packed);
     else
-        pack_kernel<QK_W_Q8_0><<<(unsigned)tiles, 128, 0, s>>>(blocks, (int)N, (int)K, (int)chunks, packed);
+        pack_kernel<QK_W_Q8_0><<<(unsigned)units, 256, 0, s>>>(blocks, (int)N, (int)K, (int)chunks, packed);
     count_launch();
     return check_launch("weight_pack");
 }
 
-static void fill_desc(ProjDesc &d, int wtype, const void *w, float *y, int64_t y_stride, int64_t N,
-                      int64_t K, int experts, int tiles_begin) {
-    d.w = static_cast<const uint8_t *>(w);
-    d.y = y;
-    d.y_stride = y_stride;
-    d.expert_bytes = packed_bytes(wtype, N, K);
-    d.N = (int)N;
-    d.K = (int)K;
-    d.n_groups = (int)ceil_div(N, TILE_ROWS);
-    d.chunks = (int)ceil_div(K, TILE_COLS);
-    d.row_tiles = (int)ceil_div(d.n_groups, RG);
-    d.experts = experts;
-    d.tiles_begin = tiles_begin;
+template <int WT>
+static qk_status launch_sk(const SkArgs &a, int G, cudaStream_t s) {
+    static bool configured = false;
+    const size_t smem = sk_smem<WT>();
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(mmvq_sk_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq: shared memory attribute: %s", cudaGetErrorString(e));
+        configured = true;
+    }
+    mmvq_sk_kernel<WT><<<G, THREADS, smem, s>>>(a);
+    count_launch();
+    return check_launch("mmvq");
 }
 
-qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj,
-                      const qk_proj *projs, const int32_t *live, cudaStream_t s) {
-    Args a = {};
+qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj, const qk_proj *projs,
+                      const int32_t *live, void *ws, size_t ws_bytes, cudaStream_t s) {
+    SkArgs a = {};
     a.img = img;
     a.img_row_bytes = row_blocks * Q8_1_BYTES;
     a.T = T;
     a.live = live;
     a.n_proj = n_proj;
-    a.k = 1;
-    int64_t tiles = 0;
-    int min_chunks = 1 << 30;
+    int64_t U = 0;
+    int R = 0;
     for (int j = 0; j < n_proj; j++) {
-        fill_desc(a.p[j], projs[j].wtype, projs[j].w, projs[j].y, projs[j].y_stride, projs[j].N,
-                  projs[j].K, 1, (int)tiles);
-        tiles += a.p[j].row_tiles;
-        min_chunks = min(min_chunks, a.p[j].chunks);
+        SkProj &d = a.p[j];
+        d.w = static_cast<const uint8_t *>(projs[j].w);
+        d.y = projs[j].y;
+        d.y_stride = projs[j].y_stride;
+        d.N = (int)projs[j].N;
+        d.K = (int)projs[j].K;
+        d.chunks = (int)ceil_div(d.K, UNIT_COLS);
+        d.row_tiles = (int)ceil_div(d.N, UNIT_ROWS);
+        d.unit_base = U;
+        d.rt_base = R;
+        U += (int64_t)d.row_tiles * d.chunks;
+        R += d.row_tiles;
     }
-    a.ksplit = pick_ksplit(tiles, min_chunks, sm_count());
-    // one weight type per launch: mixed groups are split by the caller side below
-    const int wt = projs[0].wtype;
-    return wt == QK_W_Q4_0 ? launch<QK_W_Q4_0, false>(a, tiles, s) : launch<QK_W_Q8_0, false>(a, tiles, s);
+    a.U = U;
+    const int G = (int)(U < sm_count() ? U : sm_count());
+    const int64_t need = mmvq_workspace_bytes(n_proj, projs);
+    if (!ws || ws_bytes < (size_t)need)
+        return fail(QK_ERR_WORKSPACE, "mmvq: workspace %zu < %lld bytes", ws_bytes, (long long)need);
+    a.ws_part = static_cast<float *>(ws);
+    a.ws_cnt = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(ws) + (int64_t)G * 2 * VALS * sizeof(float));
+    return projs[0].wtype == QK_W_Q4_0 ? launch_sk<QK_W_Q4_0>(a, G, s) : launch_sk<QK_W_Q8_0>(a, G, s);
 }
 
 qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k, int n_proj,
                          const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
                          const int32_t *items, cudaStream_t s) {
-    Args a = {};
+    IdArgs a = {};
     a.img = img;
     a.img_row_bytes = row_blocks * Q8_1_BYTES;
-    a.T = rows;
+    a.rows = rows;
+    a.k = k;
     a.n_proj = n_proj;
     a.counts = counts;
     a.offsets = offsets;
     a.items = items;
-    a.k = k;
-    int64_t tiles = 0;
-    int min_chunks = 1 << 30;
+    int tiles = 0;
     for (int j = 0; j < n_proj; j++) {
-        fill_desc(a.p[j], projs[j].wtype, projs[j].w, projs[j].y, projs[j].N, projs[j].N, projs[j].K,
-                  projs[j].n_experts, (int)tiles);
-        tiles += (int64_t)a.p[j].row_tiles * projs[j].n_experts;
-        min_chunks = min(min_chunks, a.p[j].chunks);
+        IdProj &d = a.p[j];
+        d.w = static_cast<const uint8_t *>(projs[j].w);
+        d.y = projs[j].y;
+        d.expert_bytes = packed_bytes(projs[j].wtype, projs[j].N, projs[j].K);
+        d.N = (int)projs[j].N;
+        d.K = (int)projs[j].K;
+        d.chunks = (int)ceil_div(d.K, UNIT_COLS);
+        d.row_tiles = (int)ceil_div(d.N, UNIT_ROWS);
+        d.tiles_begin = tiles;
+        tiles += d.row_tiles * projs[j].n_experts;
     }
-    a.ksplit = pick_ksplit(tiles, min_chunks, sm_count());
-    const int wt = projs[0].wtype;
-    return wt == QK_W_Q4_0 ? launch<QK_W_Q4_0, true>(a, tiles, s) : launch<QK_W_Q8_0, true>(a, tiles, s);
+    const size_t smem = (size_t)RW * VALS * sizeof(float);
+    if (projs[0].wtype == QK_W_Q4_0)
+        mmvq_id_kernel<QK_W_Q4_0><<<tiles, RW * 32, smem, s>>>(a);
+    else
+        mmvq_id_kernel<QK_W_Q8_0><<<tiles, RW * 32, smem, s>>>(a);
+    count_launch();
+    return check_launch("mmvq_id");
 }
 
 }  // namespace qk

@@ -189,8 +189,28 @@ static qk_status check_proj_common(int32_t wtype, const void *w, int64_t N, int6
     return QK_OK;
 }
 
+size_t qk_mmvq_workspace_bytes(int32_t n_proj, const qk_proj *projs) {
+    if (n_proj < 1 || n_proj > 8 || !projs) return 0;
+    size_t need = 0;
+    for (int wt = QK_W_Q4_0; wt <= QK_W_Q8_0; wt++) {
+        qk_proj group[8];
+        int n = 0;
+        for (int j = 0; j < n_proj; j++)
+            if (projs[j].wtype == wt) group[n++] = projs[j];
+        if (n == 0) continue;
+        const size_t g = (size_t)mmvq_workspace_bytes(n, group);
+        need = g > need ? g : need;
+    }
+    return need;
+}
+
+qk_status qk_device_faults(uint32_t *faults) {
+    REQUIRE(faults, QK_ERR_ARG, "faults is null");
+    return read_device_faults(faults);
+}
+
 qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_proj, const qk_proj *projs,
-                  const int32_t *d_live_rows, qk_stream stream) {
+                  const int32_t *d_live_rows, void *ws, size_t ws_bytes, qk_stream stream) {
     REQUIRE(img && projs, QK_ERR_ARG, "null pointer");
     REQUIRE(aligned(img, 4), QK_ERR_ARG, "img not 4-byte aligned");
     REQUIRE(T >= 1 && img_row_blocks >= 1, QK_ERR_ARG, "T or img_row_blocks < 1");
@@ -211,7 +231,23 @@ qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_
             REQUIRE(!overlap(sy, so), QK_ERR_ALIAS, "outputs of projections %d and %d overlap", i, j);
         }
     }
-    // one launch per weight type present (a q/k/v or gate/up group is normally one type)
+    REQUIRE(ws && aligned(ws, 16), QK_ERR_WORKSPACE, "workspace null or not 16-byte aligned");
+    // one launch per weight type present, in order on the stream; they share ws
+    for (int wt = QK_W_Q4_0; wt <= QK_W_Q8_0; wt++) {
+        qk_proj group[8];
+        int n = 0;
+        for (int j = 0; j < n_proj; j++)
+            if (projs[j].wtype == wt) group[n++] = projs[j];
+        if (n == 0) continue;
+        const size_t need = (size_t)mmvq_workspace_bytes(n, group);
+        REQUIRE(ws_bytes >= need, QK_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+        Span sws = span(ws, need);
+        REQUIRE(!overlap(sws, si), QK_ERR_ALIAS, "workspace overlaps img");
+        for (int j = 0; j < n_proj; j++)
+            REQUIRE(!overlap(sws, span(projs[j].y, rows_span(T, projs[j].y_stride * 4, projs[j].N * 4))) &&
+                        !overlap(sws, span(projs[j].w, (size_t)packed_bytes(projs[j].wtype, projs[j].N, projs[j].K))),
+                    QK_ERR_ALIAS, "workspace overlaps projection %d", j);
+    }
     for (int wt = QK_W_Q4_0; wt <= QK_W_Q8_0; wt++) {
         qk_proj group[8];
         int n = 0;
@@ -219,7 +255,7 @@ qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_
             if (projs[j].wtype == wt) group[n++] = projs[j];
         if (n == 0) continue;
         qk_status st = launch_mmvq(static_cast<const uint8_t *>(img), img_row_blocks, (int)T, n, group,
-                                   d_live_rows, (cudaStream_t)stream);
+                                   d_live_rows, ws, ws_bytes, (cudaStream_t)stream);
         if (st != QK_OK) return st;
     }
     return QK_OK;

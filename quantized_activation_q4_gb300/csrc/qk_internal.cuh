@@ -42,26 +42,36 @@ __device__ __forceinline__ int live_rows(const int32_t *live, int rows) {
     return n < 0 ? 0 : (n > rows ? rows : n);
 }
 
-// Packed Q4_0 weights: 16-row groups x 128-column chunks, 1152-byte tiles.
-//   bytes    0..511 : lane l = 4g+t holds 16 B = for blocks j=0..3 of the chunk,
-//                     nibble bytes 4t..4t+3 of row g of the group
-//   bytes  512..1023: the same for row g+8
-//   bytes 1024..1151: scales, row r (0..15) at 1024 + 8r, block j half at +2j
-// Packed Q8_0 weights: same tiling, 2176-byte tiles.
-//   bytes    0..1023: lane l holds 32 B = for blocks j=0..3: codes 4t..4t+3 and
-//                     16+4t..16+4t+3 of row g (8 B per block)
-//   bytes 1024..2047: the same for row g+8
-//   bytes 2048..2175: scales as for Q4_0
-constexpr int TILE_ROWS = 16;
-constexpr int TILE_COLS = 128;
-constexpr int Q4_TILE_BYTES = 1152;
-constexpr int Q8_TILE_BYTES = 2176;
+// Packed weights: units of 128 rows x 128 columns (8 row groups of 16 rows x
+// 4 quant blocks), ordered (row tile, column chunk) and block-major inside a
+// unit, so one warp reads everything it needs for one 32-column block of all
+// 8 row groups with conflict-free 128-bit loads. Lane l = 4g + t; "word t" of
+// a row's block = its bytes 4t..4t+3 (Q4_0: nibble bytes; Q8_0: codes 4t..4t+3
+// "lo" and codes 16+4t..16+4t+3 "hi").
+//   Q4_0 unit, 9216 B: block jb at jb*2048, four 512-B regions; region k,
+//     lane l: 16 B = word t of rows 32k+g, 32k+g+8, 32k+16+g, 32k+24+g.
+//     Scales at 8192 + jb*256 + g*32: eight half2 (row 16r+g, row 16r+g+8),
+//     r = 0..7.
+//   Q8_0 unit, 17408 B: block jb at jb*4096, eight 512-B regions; region k,
+//     lane l: 16 B = [row 16k+g lo, hi][row 16k+g+8 lo, hi]. Scales at
+//     16384 + jb*256 as for Q4_0.
+constexpr int UNIT_ROWS = 128;
+constexpr int UNIT_GROUPS = 8;
+constexpr int UNIT_COLS = 128;
+constexpr int Q4_UNIT_BYTES = 9216;
+constexpr int Q8_UNIT_BYTES = 17408;
+constexpr int Q4_BLOCK_STRIDE = 2048;
+constexpr int Q8_BLOCK_STRIDE = 4096;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-inline int64_t tile_bytes(int wtype) { return wtype == QK_W_Q4_0 ? Q4_TILE_BYTES : Q8_TILE_BYTES; }
+inline int64_t unit_bytes(int wtype) { return wtype == QK_W_Q4_0 ? Q4_UNIT_BYTES : Q8_UNIT_BYTES; }
 inline int64_t packed_bytes(int wtype, int64_t N, int64_t K) {
-    return ceil_div(N, TILE_ROWS) * ceil_div(K, TILE_COLS) * tile_bytes(wtype);
+    return ceil_div(N, UNIT_ROWS) * ceil_div(K, UNIT_COLS) * unit_bytes(wtype);
 }
+
+// Reads and clears the device-side fault word (bit 0: a bounded mbarrier
+// wait gave up). Synchronous.
+qk_status read_device_faults(uint32_t *faults);
 
 // ------------------------------------------------------- kernel launchers
 // Defined in the kernel translation units; arguments already validated.
@@ -78,8 +88,10 @@ qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride
                           uint8_t *img, int64_t row_blocks, const int32_t *live, cudaStream_t s);
 qk_status launch_weight_pack(int wtype, const uint8_t *blocks, int64_t N, int64_t K,
                              uint8_t *packed, cudaStream_t s);
+int64_t mmvq_workspace_bytes(int n_proj, const qk_proj *projs);
 qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj,
-                      const qk_proj *projs, const int32_t *live, cudaStream_t s);
+                      const qk_proj *projs, const int32_t *live, void *ws, size_t ws_bytes,
+                      cudaStream_t s);
 qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k, int n_proj,
                          const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
                          const int32_t *items, cudaStream_t s);

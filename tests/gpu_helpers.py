@@ -45,3 +45,16 @@ def pack_experts(Ws: list[np.ndarray], wtype: str, N: int, K: int):
     for e, W in enumerate(Ws):
         qk.qk_weight_pack(wtype, dev(W.reshape(-1)), N, K, out[e * per:(e + 1) * per], per)
     return out
+
+
+def workspace(projs):
+    """Zeroed device workspace for qk_mmvq (the library leaves it zeroed after each call)."""
+    import torch
+    n = max(16, qk.qk_mmvq_workspace_bytes(projs))
+    return torch.zeros((n,), dtype=torch.uint8, device="cuda"), n
+
+
+def mmvq(img, rb, T, projs, live=None):
+    ws, n = workspace(projs)
+    qk.qk_mmvq(img, rb, T, projs, ws, n, live)
+    return ws

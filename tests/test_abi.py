@@ -64,17 +64,22 @@ def test_producers_reject_partial_blocks_and_aliases(lib):
 
 def test_projection_checks(lib):
     P = C.c_void_p
+    WS = 0x50000000
     good = qk.qk_proj(0, 0, W, 64, 256, Y, 64)
     arr = (qk.qk_proj * 1)(good)
-    assert lib.qk_mmvq(P(IMG), 8, 9, 1, arr, None, None) == 5                  # T > 8
+    assert lib.qk_mmvq(P(IMG), 8, 9, 1, arr, None, P(WS), 1 << 20, None) == 5       # T > 8
     arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W, 64, 288, Y, 64))
-    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, None) == 2                  # K past the image row
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, P(WS), 1 << 20, None) == 2       # K past the image row
     arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W + 8, 64, 256, Y, 64))
-    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, None) == 1                  # misaligned packed weights
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, P(WS), 1 << 20, None) == 1       # misaligned weights
     arr = (qk.qk_proj * 2)(good, qk.qk_proj(0, 0, W, 64, 256, Y + 128, 64))
-    assert lib.qk_mmvq(P(IMG), 8, 8, 2, arr, None, None) == 3                  # overlapping outputs
+    assert lib.qk_mmvq(P(IMG), 8, 8, 2, arr, None, P(WS), 1 << 20, None) == 3       # overlapping outputs
     arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W, 64, 256, IMG + 4, 64))
-    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, None) == 3                  # output over the image
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, P(WS), 1 << 20, None) == 3       # output over the image
+    arr = (qk.qk_proj * 1)(good)
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, None, 0, None) == 4              # no workspace
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, P(WS), 16, None) == 4            # workspace too small
+    assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, P(Y), 1 << 20, None) == 3        # workspace over y
 
 
 def test_routing_checks(lib):
@@ -88,7 +93,8 @@ def test_routing_checks(lib):
 def test_weight_pack_checks(lib):
     P = C.c_void_p
     need = lib.qk_weight_packed_bytes(0, 100, 256)
-    assert need == 7 * 2 * 1152                                                  # 16-row x 128-col tiles
+    assert need == 1 * 2 * 9216                                                  # 128-row x 128-col units
+    assert lib.qk_weight_packed_bytes(1, 300, 300) == 3 * 3 * 17408
     assert lib.qk_weight_pack(0, P(X), 100, 256, P(W), need - 1, None) == 4
     assert lib.qk_weight_pack(0, P(X), 100, 250, P(W), need, None) == 2
     assert lib.qk_weight_pack(0, P(X), 100, 256, P(X + 64), need, None) == 3

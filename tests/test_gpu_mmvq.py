@@ -12,7 +12,7 @@ import pytest
 from oracle import oracle as O
 from quantized_activation_q4_gb300 import binding as qk
 from quantized_activation_q4_gb300 import synth
-from tests.gpu_helpers import dev, empty_u8, host, live_ptr, pack_weight
+from tests.gpu_helpers import dev, empty_u8, host, live_ptr, mmvq, pack_weight, workspace
 
 pytestmark = pytest.mark.gpu
 
@@ -39,8 +39,11 @@ def run_mmvq(img, rb, T, projs_spec, live=None, y_fill=np.nan):
         y = torch.full((T, N), float(y_fill), dtype=torch.float32, device="cuda")
         outs.append(y)
         projs.append(qk.make_proj(wtype, packed, N, K, y, N))
-    qk.qk_mmvq(img, rb, T, projs, live_ptr(live) if live is not None else None)
-    return [host(y) for y in outs]
+    ws = mmvq(img, rb, T, projs, live_ptr(live) if live is not None else None)
+    outs = [host(y) for y in outs]
+    assert not host(ws).any(), "workspace not left zeroed"
+    assert qk.qk_device_faults() == 0
+    return outs
 
 
 def check(yg, wtype, W, N, K, x, img_host, rb, rows_plain=None):

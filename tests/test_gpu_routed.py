@@ -109,6 +109,8 @@ def _poison(bufs, x_d, logits_d, rows, live, seed):
     bufs["yg"].fill_(float(SENTINEL))
     bufs["yu"].fill_(float(SENTINEL))
     bufs["items"].fill_(-3)
+    bufs["y"].fill_(float("nan"))
+    bufs["img"].fill_(0xA5)
     return x_h, l_h
 
 
