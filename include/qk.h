@@ -231,8 +231,11 @@ typedef struct qk_proj {
  *   projs host array of n_proj (1..8) descriptors; outputs must not overlap
  *   ws   device workspace of at least qk_mmvq_workspace_bytes(n_proj, projs)
  *        bytes, 16-byte aligned, ZEROED ONCE before its first use (e.g. by
- *        cudaMemset); every call leaves it zeroed again when its kernels
- *        finish. Calls that may run concurrently need separate workspaces.
+ *        cudaMemset). It holds completion counters, which every call returns
+ *        to zero before its kernels finish, and scratch partial sums; so it
+ *        can be reused by later calls (and graph replays) on the same stream
+ *        without zeroing again. Calls that may run concurrently need
+ *        separate workspaces.
  * The work is split by bytes over the device's SMs; partial sums of a row
  * tile shared by several CTAs go through ws and are added in a fixed order,
  * so outputs are deterministic on a given device.

@@ -27,9 +27,10 @@
 // warps take the units' 32-column blocks round-robin (block j of the CTA's
 // range goes to warp j mod 15), each computing all 128 rows x 8 tokens of its
 // block. Work is split by equal bytes over the CTAs (stream-K): a row tile
-// cut between CTAs leaves partial sums in a small caller workspace, and the
-// last CTA to finish it (atomic counter, reset after use) adds the parts in
-// CTA order. All sums run in a fixed order, so results do not depend on
+// cut between CTAs leaves partial sums in a small caller workspace (written
+// when the CTA has finished its whole range, so no consumer waits on global
+// memory mid-stream), and the last CTA to publish its part (atomic counter,
+// reset after use) adds the parts in CTA order. All sums run in a fixed order, so results do not depend on
 // timing or on the live-row count.
 
 #include "qk_internal.cuh"
@@ -43,7 +44,8 @@ constexpr int MAX_PROJ = 8;
 constexpr int CW = 15;                       // consumer warps (ordinary path); with the
 constexpr int THREADS = (CW + 1) * 32;       // producer, 16 warps = 4 per SM sub-partition
 constexpr int VALS = UNIT_GROUPS * 4 * 32;   // accumulators of one 128-row tile per warp
-constexpr int VPT = (VALS + CW * 32 - 1) / (CW * 32);   // reduced values per consumer thread
+constexpr int HALF_VALS = VALS / 2;          // reduced in two passes of 4 row groups
+constexpr int MAXP = 8;                      // partial sums loaded per batch
 constexpr uint32_t SPIN_LIMIT = 1u << 22;
 
 template <int WT> struct Layout;
@@ -130,6 +132,22 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar), "l"(pol)
         : "memory");
 }
+// Atomic add with acquire-release semantics at GPU scope (returns the old value).
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// A row tile this CTA shares with others (stream-K): where its parts live.
+struct SharedTile {
+    float *y;
+    int64_t y_stride;
+    int N, rt, R;            // rows, row tile in its projection, global row-tile index
+    int c_first, c_last;     // contributing CTAs
+    int first_slot;          // part slot used by c_first (later CTAs use slot 0)
+};
+
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory");
 }
@@ -180,35 +198,41 @@ __device__ __forceinline__ void wcodes_to_half2(uint32_t w, uint32_t &h02, uint3
 // ---------------------------------------------------------------- one block
 // Activation side of block b for this lane: B fragments of token g (elements
 // 4t..4t+3 and 16+4t..16+4t+3), scales of tokens 2t and 2t+1, and the bias
-// correction shared by every row group.
+// correction shared by every row group. The four image words are loaded one
+// block ahead (Raw) so their latency overlaps the previous block's MMAs.
+struct Raw {
+    uint32_t lo, hi, ds0, ds1;
+};
 struct BSide {
     uint32_t lo02, lo13, hi02, hi13;
     float da0, da1, ns0, ns1;
     float corr[4];
 };
 
+__device__ __forceinline__ Raw load_raw(const uint8_t *imgB, const uint8_t *imgS0, const uint8_t *imgS1, int b,
+                                        int t4) {
+    Raw r = {0u, 0u, 0u, 0u};
+    const int64_t off = (int64_t)b * Q8_1_BYTES;
+    if (imgB) {
+        r.lo = ld_img4(imgB + off + 4 + 4 * t4);
+        r.hi = ld_img4(imgB + off + 20 + 4 * t4);
+    }
+    if (imgS0) r.ds0 = ld_img4(imgS0 + off);
+    if (imgS1) r.ds1 = ld_img4(imgS1 + off);
+    return r;
+}
+
 template <int WT>
-__device__ __forceinline__ void bside(const uint8_t *imgB, const uint8_t *imgS0, const uint8_t *imgS1,
-                                      int b, int t4, BSide &s) {
+__device__ __forceinline__ void bside(const Raw &r, BSide &s) {
     constexpr uint32_t NEG_LO = WT == QK_W_Q4_0 ? 0xE400E400u : 0xE480E480u;  // -1024 | -1152
     constexpr uint32_t NEG_HI = WT == QK_W_Q4_0 ? 0xD400D400u : 0xE480E480u;  //   -64 | -1152
-    s.lo02 = s.lo13 = s.hi02 = s.hi13 = 0u;
-    if (imgB) {
-        const uint8_t *blk = imgB + (int64_t)b * Q8_1_BYTES;
-        codes_to_half2(ld_img4(blk + 4 + 4 * t4), s.lo02, s.lo13);
-        codes_to_half2(ld_img4(blk + 20 + 4 * t4), s.hi02, s.hi13);
-    }
-    s.da0 = s.da1 = s.ns0 = s.ns1 = 0.0f;
-    if (imgS0) {
-        const float2 ds = __half22float2(as_h2(ld_img4(imgS0 + (int64_t)b * Q8_1_BYTES)));
-        s.da0 = ds.x;
-        if (WT == QK_W_Q4_0) s.ns0 = -8.0f * ds.y;
-    }
-    if (imgS1) {
-        const float2 ds = __half22float2(as_h2(ld_img4(imgS1 + (int64_t)b * Q8_1_BYTES)));
-        s.da1 = ds.x;
-        if (WT == QK_W_Q4_0) s.ns1 = -8.0f * ds.y;
-    }
+    codes_to_half2(r.lo, s.lo02, s.lo13);   // an absent token has zero words: exact zeros
+    codes_to_half2(r.hi, s.hi02, s.hi13);
+    const float2 d0 = __half22float2(as_h2(r.ds0)), d1 = __half22float2(as_h2(r.ds1));
+    s.da0 = d0.x;
+    s.da1 = d1.x;
+    s.ns0 = WT == QK_W_Q4_0 ? -8.0f * d0.y : 0.0f;
+    s.ns1 = WT == QK_W_Q4_0 ? -8.0f * d1.y : 0.0f;
     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t alo[4] = {NEG_LO, NEG_LO, NEG_LO, NEG_LO};
     const uint32_t ahi[4] = {NEG_HI, NEG_HI, NEG_HI, NEG_HI};
@@ -279,7 +303,9 @@ __device__ __forceinline__ void val_pos(int v, int &row, int &slot) {
     slot = 2 * (l & 3) + (i & 1);
 }
 
-__device__ __forceinline__ int64_t cta_start(int c, int64_t U, int G) { return ((int64_t)c * U) / G; }
+__device__ __forceinline__ int64_t cta_start(int c, int64_t U, int G) {
+    return (int64_t)(((uint64_t)c * (uint64_t)U) / (uint32_t)G);
+}
 __device__ __forceinline__ int cta_of(int64_t u, int64_t U, int G) {
     int c = (int)((u * G) / U);
     while (c + 1 < G && cta_start(c + 1, U, G) <= u) c++;
@@ -294,9 +320,11 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     float *red = reinterpret_cast<float *>(smem + L::SLOTS * L::UNIT);
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + CW * VALS);
+    float *keep = red + CW * HALF_VALS;   // [2][VALS]
+    uint64_t *full = reinterpret_cast<uint64_t *>(keep + 2 * VALS);
     uint64_t *empty = full + L::SLOTS;
-    __shared__ int s_last;
+    __shared__ int s_last[2];
+    __shared__ SharedTile s_tile[2];
 
     const int G = gridDim.x, cta = blockIdx.x;
     const int64_t u0 = cta_start(cta, a.U, G), u1 = cta_start(cta + 1, a.U, G);
@@ -319,17 +347,26 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
     };
 
     if (warp == CW) {   // ---------------- producer
-        if (lane == 0) {
+        if (lane == 0 && u0 < u1) {
             const uint64_t pol = evict_first_policy();
-            for (int64_t i = 0; u0 + i < u1; i++) {
-                const int slot = (int)(i % L::SLOTS);
-                const uint32_t n = (uint32_t)(i / L::SLOTS);
+            int j, rt, c;
+            decode(u0, j, rt, c);
+            // units of one projection are contiguous in its packed buffer
+            const uint8_t *src = a.p[j].w + ((int64_t)rt * a.p[j].chunks + c) * L::UNIT;
+            int64_t left_in_proj = a.p[j].unit_base + (int64_t)a.p[j].row_tiles * a.p[j].chunks - u0;
+            for (int i = 0; u0 + i < u1; i++) {
+                const int slot = i % L::SLOTS;
+                const uint32_t n = (uint32_t)i / L::SLOTS;
                 if (n > 0 && !mbar_wait(smem_addr(empty + slot), (n - 1) & 1u)) break;
-                int j, rt, c;
-                decode(u0 + i, j, rt, c);
-                const uint8_t *src = a.p[j].w + ((int64_t)rt * a.p[j].chunks + c) * L::UNIT;
+                if (left_in_proj == 0) {   // next projection
+                    j++;
+                    src = a.p[j].w;
+                    left_in_proj = (int64_t)a.p[j].row_tiles * a.p[j].chunks;
+                }
                 mbar_expect_tx(smem_addr(full + slot), L::UNIT);
                 bulk_g2s(smem_addr(ring + (size_t)slot * L::UNIT), src, L::UNIT, smem_addr(full + slot), pol);
+                src += L::UNIT;
+                left_in_proj--;
             }
         }
         return;
@@ -343,9 +380,34 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
     const uint8_t *imgS1 = 2 * t4 + 1 < tl ? a.img + (int64_t)(2 * t4 + 1) * a.img_row_bytes : nullptr;
     bool ok = true;
 
+    // Row tiles this CTA shares (at most its first, slot 0, and its last, slot
+    // 1), planned now so that the tail only stores, counts and adds.
+    if (tid < 2) {
+        SharedTile st = {};
+        st.R = -1;
+        if (u0 < u1) {
+            int jj, rr, cc;
+            decode(tid == 0 ? u0 : u1 - 1, jj, rr, cc);
+            const SkProj &P = a.p[jj];
+            const int64_t rs = P.unit_base + (int64_t)rr * P.chunks, re = rs + P.chunks;
+            const bool first_tile_too = tid == 1 && rs <= u0;   // last tile == first tile
+            if (!first_tile_too && (rs < u0 || re > u1)) {
+                st.y = P.y;
+                st.y_stride = P.y_stride;
+                st.N = P.N;
+                st.rt = rr;
+                st.R = P.rt_base + rr;
+                st.c_first = cta_of(rs, a.U, G);
+                st.c_last = cta_of(re - 1, a.U, G);
+                st.first_slot = cta_start(st.c_first, a.U, G) < rs ? 1 : 0;
+            }
+        }
+        s_tile[tid] = st;
+    }
+
+    int j = 0, rt = 0, c0 = 0;
+    if (u0 < u1) decode(u0, j, rt, c0);
     for (int64_t u = u0; u < u1;) {
-        int j, rt, c0;
-        decode(u, j, rt, c0);
         const SkProj &P = a.p[j];
         const int64_t rt_start = P.unit_base + (int64_t)rt * P.chunks, rt_end = rt_start + P.chunks;
         const int64_t s1 = u1 < rt_end ? u1 : rt_end;
@@ -357,15 +419,20 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
 #pragma unroll
             for (int i = 0; i < 4; i++) acc[r][i] = 0.0f;
 
+        auto blk_of = [&](int jj) { return 4 * (c0 + (jj >> 2)) + (jj & 3); };
+        Raw next = {0u, 0u, 0u, 0u};
+        if (warp < nblk && blk_of(warp) < Kb) next = load_raw(imgB, imgS0, imgS1, blk_of(warp), t4);
         for (int jj = warp; jj < nblk; jj += CW) {
-            const int64_t i = (u - u0) + (jj >> 2);
-            const int slot = (int)(i % L::SLOTS);
-            if (ok) ok = mbar_wait(smem_addr(full + slot), (uint32_t)(i / L::SLOTS) & 1u);
+            const Raw cur = next;
+            const int jn = jj + CW;
+            if (jn < nblk && blk_of(jn) < Kb) next = load_raw(imgB, imgS0, imgS1, blk_of(jn), t4);
+            const int i = (int)(u - u0) + (jj >> 2);
+            const int slot = i % L::SLOTS;
+            if (ok) ok = mbar_wait(smem_addr(full + slot), ((uint32_t)i / L::SLOTS) & 1u);
             const int jb = jj & 3;
-            const int b = 4 * (c0 + (jj >> 2)) + jb;
-            if (ok && b < Kb) {
+            if (ok && blk_of(jj) < Kb) {
                 BSide s;
-                bside<WT>(imgB, imgS0, imgS1, b, t4, s);
+                bside<WT>(cur, s);
                 const uint32_t ub = smem_addr(ring + (size_t)slot * L::UNIT);
                 block_rows<WT, true>(nullptr, ub + jb * L::BLOCK, nullptr, ub + L::SCALES + jb * 256, lane, s, acc);
             }
@@ -373,71 +440,102 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
             if (lane == 0) mbar_arrive(smem_addr(empty + slot));
         }
 
-        // CTA reduction over the consumer warps, fixed order
+        // CTA reduction over the consumer warps in fixed order, in two passes
+        // of 4 row groups (value v of pass h is accumulator index h*512 + v)
+        const bool whole = u == rt_start && s1 == rt_end;
+        const int part_slot = u0 >= rt_start ? 0 : 1;
 #pragma unroll
-        for (int r = 0; r < UNIT_GROUPS; r++)
+        for (int h = 0; h < 2; h++) {
 #pragma unroll
-            for (int i = 0; i < 4; i++) red[warp * VALS + (r * 4 + i) * 32 + lane] = acc[r][i];
-        consumer_sync();
-        float v[VPT];
+            for (int r = 0; r < UNIT_GROUPS / 2; r++)
 #pragma unroll
-        for (int q = 0; q < VPT; q++) {
-            const int t = tid + q * CW * 32;
-            float sum = 0.0f;
-            if (t < VALS) {
+                for (int i = 0; i < 4; i++) red[warp * HALF_VALS + (r * 4 + i) * 32 + lane] = acc[h * 4 + r][i];
+            consumer_sync();
+            for (int t = tid; t < HALF_VALS; t += CW * 32) {
+                float sum = 0.0f;
 #pragma unroll
-                for (int w = 0; w < CW; w++) sum += red[w * VALS + t];
+                for (int w = 0; w < CW; w++) sum += red[w * HALF_VALS + t];
+                const int tv = h * HALF_VALS + t;
+                if (whole) {
+                    int row, slot;
+                    val_pos(tv, row, slot);
+                    row += rt * UNIT_ROWS;
+                    if (row < P.N && slot < tl) P.y[(int64_t)slot * P.y_stride + row] = sum;
+                } else {
+                    keep[part_slot * VALS + tv] = sum;
+                }
             }
-            v[q] = sum;
+            consumer_sync();   // red is rewritten by the next pass / row tile
         }
-        const int row0 = rt * UNIT_ROWS;
-        if (u == rt_start && s1 == rt_end) {
+        u = s1;
+        // next segment starts at chunk 0 of the next row tile (or projection)
+        c0 = 0;
+        if (++rt == P.row_tiles) {
+            rt = 0;
+            j++;
+        }
+    }
+
+    // Publish this CTA's parts of shared row tiles; the last contributor of a
+    // tile adds every part in CTA order and writes the output. Thread 0/1's
+    // acquire-release atomic after the barrier covers the whole CTA's stores.
+    const SharedTile t0 = s_tile[0], t1 = s_tile[1];
+    if (t0.R < 0 && t1.R < 0) return;
+    for (int ps = 0; ps < 2; ps++) {
+        if ((ps ? t1.R : t0.R) < 0) continue;
+        float *mine = a.ws_part + ((int64_t)cta * 2 + ps) * VALS;
+        for (int t = tid; t < VALS; t += CW * 32) mine[t] = keep[ps * VALS + t];
+    }
+    consumer_sync();
+    if (tid < 2) {
+        const SharedTile &st = tid ? t1 : t0;
+        int last = 0;
+        if (st.R >= 0) {
+            const unsigned old = atom_add_acq_rel(a.ws_cnt + st.R, 1u);
+            last = old == (unsigned)(st.c_last - st.c_first);
+        }
+        s_last[tid] = last;
+    }
+    consumer_sync();
+    for (int ps = 0; ps < 2; ps++) {
+        if (!s_last[ps]) continue;
+        const SharedTile &st = ps ? t1 : t0;
+        constexpr int PER = (VALS + CW * 32 - 1) / (CW * 32);
+        float sums[PER];
 #pragma unroll
-            for (int q = 0; q < VPT; q++) {
-                const int t = tid + q * CW * 32;
-                if (t >= VALS) break;
+        for (int k = 0; k < PER; k++) sums[k] = 0.0f;
+        for (int cb = st.c_first; cb <= st.c_last; cb += MAXP) {   // MAXP parts in flight at once
+            const float *src[MAXP];
+#pragma unroll
+            for (int q = 0; q < MAXP; q++) {
+                const int cc = cb + q <= st.c_last ? cb + q : st.c_last;
+                const int pslot = cc == st.c_first ? st.first_slot : 0;
+                src[q] = a.ws_part + ((int64_t)cc * 2 + pslot) * VALS;
+            }
+#pragma unroll
+            for (int k = 0; k < PER; k++) {
+                const int t = tid + k * CW * 32;
+                if (t < VALS) {
+                    float part[MAXP];
+#pragma unroll
+                    for (int q = 0; q < MAXP; q++) part[q] = __ldcg(src[q] + t);
+#pragma unroll
+                    for (int q = 0; q < MAXP; q++)
+                        if (cb + q <= st.c_last) sums[k] += part[q];
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PER; k++) {
+            const int t = tid + k * CW * 32;
+            if (t < VALS) {
                 int row, slot;
                 val_pos(t, row, slot);
-                row += row0;
-                if (row < P.N && slot < tl) P.y[(int64_t)slot * P.y_stride + row] = v[q];
-            }
-        } else {
-            // partial row tile: publish it; the last contributor finishes the tile
-            const int R = P.rt_base + rt;
-            const int part_slot = u0 >= rt_start ? 0 : 1;
-            float *mine = a.ws_part + ((int64_t)cta * 2 + part_slot) * VALS;
-#pragma unroll
-            for (int q = 0; q < VPT; q++)
-                if (tid + q * CW * 32 < VALS) mine[tid + q * CW * 32] = v[q];
-            __threadfence();
-            consumer_sync();
-            const int c_first = cta_of(rt_start, a.U, G), c_last = cta_of(rt_end - 1, a.U, G);
-            if (tid == 0) {
-                const unsigned old = atomicAdd(a.ws_cnt + R, 1u);
-                s_last = old == (unsigned)(c_last - c_first);
-            }
-            consumer_sync();
-            if (s_last) {
-                __threadfence();
-#pragma unroll
-                for (int q = 0; q < VPT; q++) {
-                    const int t = tid + q * CW * 32;
-                    if (t >= VALS) break;
-                    float sum = 0.0f;
-                    for (int cc = c_first; cc <= c_last; cc++) {
-                        const int ps = cta_start(cc, a.U, G) >= rt_start ? 0 : 1;
-                        sum += __ldcg(a.ws_part + ((int64_t)cc * 2 + ps) * VALS + t);
-                    }
-                    int row, slot;
-                    val_pos(t, row, slot);
-                    row += row0;
-                    if (row < P.N && slot < tl) P.y[(int64_t)slot * P.y_stride + row] = sum;
-                }
-                if (tid == 0) a.ws_cnt[R] = 0u;
+                row += st.rt * UNIT_ROWS;
+                if (row < st.N && slot < tl) st.y[(int64_t)slot * st.y_stride + row] = sums[k];
             }
         }
-        consumer_sync();   // red is rewritten by the next row tile
-        u = s1;
+        if (tid == 0) a.ws_cnt[st.R] = 0u;
     }
 }
 
@@ -502,7 +600,7 @@ __global__ void __launch_bounds__(RW * 32) mmvq_id_kernel(const __grid_constant_
         for (int b = warp; b < Kb; b += RW) {
             const uint8_t *unit = wbase + (int64_t)(b >> 2) * L::UNIT;
             BSide s;
-            bside<WT>(imgB, imgS0, imgS1, b, t4, s);
+            bside<WT>(load_raw(imgB, imgS0, imgS1, b, t4), s);
             block_rows<WT, false>(unit + (b & 3) * L::BLOCK, 0, unit + L::SCALES + (b & 3) * 256, 0, lane, s, acc);
         }
 #pragma unroll
@@ -588,7 +686,8 @@ int sm_count() {
 template <int WT>
 size_t sk_smem() {
     using L = Layout<WT>;
-    return (size_t)L::SLOTS * L::UNIT + (size_t)CW * VALS * sizeof(float) + 2 * L::SLOTS * sizeof(uint64_t);
+    return (size_t)L::SLOTS * L::UNIT + ((size_t)CW * HALF_VALS + 2 * VALS) * sizeof(float) +
+           2 * L::SLOTS * sizeof(uint64_t);
 }
 
 }  // namespace

@@ -47,11 +47,17 @@ def pack_experts(Ws: list[np.ndarray], wtype: str, N: int, K: int):
     return out
 
 
+_WS = {}
+
+
 def workspace(projs):
-    """Zeroed device workspace for qk_mmvq (the library leaves it zeroed after each call)."""
+    """A qk_mmvq workspace, zeroed once when first made and then reused by every
+    later call of the same size (the library keeps its counters at zero)."""
     import torch
     n = max(16, qk.qk_mmvq_workspace_bytes(projs))
-    return torch.zeros((n,), dtype=torch.uint8, device="cuda"), n
+    if n not in _WS:
+        _WS[n] = torch.zeros((n,), dtype=torch.uint8, device="cuda")
+    return _WS[n], n
 
 
 def mmvq(img, rb, T, projs, live=None):
