@@ -61,6 +61,7 @@ _SIGS = {
     "qk_device_faults": ([C.POINTER(C.c_uint32)], C.c_int),
     "qk_mmvq_workspace_bytes": ([I32, C.POINTER(qk_proj)], SZ),
     "qk_mmvq": ([P, I64, I64, I32, C.POINTER(qk_proj), P, P, SZ, P], C.c_int),
+    "qk_mmvq_static_ws": ([P, I64, I64, I32, C.POINTER(qk_proj), P, P], C.c_int),
     "qk_topk_route": ([P, I64, I32, I32, P, P, P, P], C.c_int),
     "qk_moe_plan": ([P, I64, I32, I32, P, P, P, P, P], C.c_int),
     "qk_mmvq_id": ([P, I64, I64, I32, I32, C.POINTER(qk_proj_id), P, P, P, P], C.c_int),
@@ -186,6 +187,13 @@ def qk_mmvq(img, img_row_blocks, T, projs, ws, ws_bytes, d_live_rows=None, strea
     arr = (qk_proj * len(projs))(*projs)
     _check("qk_mmvq", load().qk_mmvq(_ptr(img), img_row_blocks, T, len(projs), arr, _ptr(d_live_rows),
                                      _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def qk_mmvq_static_ws(img, img_row_blocks, T, projs, d_live_rows=None, stream=None):
+    """qk_mmvq with the library's own static scratch array (no workspace argument)."""
+    arr = (qk_proj * len(projs))(*projs)
+    _check("qk_mmvq_static_ws", load().qk_mmvq_static_ws(_ptr(img), img_row_blocks, T, len(projs), arr,
+                                                         _ptr(d_live_rows), _stream(stream)))
 
 
 def qk_device_faults() -> int:

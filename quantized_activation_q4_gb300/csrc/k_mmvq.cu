@@ -33,6 +33,8 @@
 // reset after use) adds the parts in CTA order. All sums run in a fixed order, so results do not depend on
 // timing or on the live-row count.
 
+#include <mutex>
+
 #include "qk_internal.cuh"
 
 namespace qk {
@@ -810,3 +812,47 @@ qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k
 }
 
 }  // namespace qk
+
+// ------------------------------------------------------------------ no-allocation variant
+// qk_mmvq_static_ws: the workspace is this file-scope device array instead of
+// caller memory. In host code the array's name is only a host-side stand-in,
+// so its device address is looked up once per device (with that device
+// current) and cached.
+static __device__ __align__(256) unsigned char g_mmvq_static_ws[QK_MMVQ_STATIC_WS_BYTES];
+
+namespace {
+constexpr int MAX_DEVICES = 64;
+std::mutex g_static_ws_mu;
+void *g_static_ws_ptr[MAX_DEVICES] = {};
+}  // namespace
+
+extern "C" QK_API qk_status qk_mmvq_static_ws(const void *img, int64_t img_row_blocks, int64_t T,
+                                              int32_t n_proj, const qk_proj *projs,
+                                              const int32_t *d_live_rows, qk_stream stream) {
+    if (!projs || n_proj < 1 || n_proj > 8)
+        return qk::fail(QK_ERR_ARG, "qk_mmvq_static_ws: projs null or n_proj=%d not in 1..8", (int)n_proj);
+    const size_t need = qk_mmvq_workspace_bytes(n_proj, projs);
+    if (need > QK_MMVQ_STATIC_WS_BYTES)
+        return qk::fail(QK_ERR_UNSUPPORTED, "qk_mmvq_static_ws: needs %zu bytes of scratch, the static array holds %u",
+                    need, (unsigned)QK_MMVQ_STATIC_WS_BYTES);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return qk::fail(QK_ERR_CUDA, "qk_mmvq_static_ws: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= MAX_DEVICES) return qk::fail(QK_ERR_UNSUPPORTED, "qk_mmvq_static_ws: device %d", dev);
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_ws_mu);
+        if (!g_static_ws_ptr[dev]) {
+            e = cudaGetSymbolAddress(&g_static_ws_ptr[dev], g_mmvq_static_ws);
+            if (e != cudaSuccess) {
+                g_static_ws_ptr[dev] = nullptr;
+                return qk::fail(QK_ERR_CUDA, "qk_mmvq_static_ws: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+            }
+        }
+        ws = g_static_ws_ptr[dev];
+    }
+    // the counters (and, simply, all scratch this call uses) must start at zero
+    e = cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream);
+    if (e != cudaSuccess) return qk::fail(QK_ERR_CUDA, "qk_mmvq_static_ws: clearing scratch: %s", cudaGetErrorString(e));
+    return qk_mmvq(img, img_row_blocks, T, n_proj, projs, d_live_rows, ws, QK_MMVQ_STATIC_WS_BYTES, stream);
+}
