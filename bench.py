@@ -63,6 +63,24 @@ RMS_BYTES = T * D_ATTN * 4 * 2 + D_ATTN * 4 + IMG_ATTN          # x in, w in, y 
 QUANT_BIG_BYTES = T * K_BIG * 4 + IMG_BIG
 
 
+def recorded_traffic():
+    """DRAM bytes per launch of the roofline kernel from the committed ncu summary,
+    or None when the kernel sources changed since that capture."""
+    import glob
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "mmvq_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    csrc = os.path.join(ROOT, "quantized_activation_q4_gb300", "csrc")
+    h = hashlib.sha256()
+    for q in sorted(glob.glob(os.path.join(csrc, "*.cu"))) + sorted(glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(q, "rb") as f:
+            h.update(os.path.basename(q).encode() + f.read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec.get("csrc_sha256") else None
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -191,43 +209,60 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         for r in range(R):                       # eager warm-up of every path
             comp_a(r); comp_q(); comp_m(r)
     torch.cuda.synchronize()
+    # Graphs: one per replica holding the whole step (for ms_per_step), and
+    # per-component graphs of R back-to-back replicas (for component times and
+    # the dominant kernel's launch duration), so that graph-launch gaps are
+    # amortised and consecutive kernels overlap as they do inside a step.
     n0 = qk.launch_count()
+    step_graphs = []
     for r in range(R):
-        ga, gq, gm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga, stream=stream):
-            comp_a(r)
-        with torch.cuda.graph(gq, stream=stream):
-            comp_q()
-        with torch.cuda.graph(gm, stream=stream):
-            comp_m(r)
-        graphs.append((ga, gq, gm))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            comp_a(r); comp_q(); comp_m(r)
+        step_graphs.append(g)
     kernels_per_step = (qk.launch_count() - n0) // R
+    comp_graphs = {}
+    for name, fn in (("a", lambda r: comp_a(r)), ("b", lambda r: (comp_q(), comp_m(r))), ("m", lambda r: comp_m(r))):
+        n1 = qk.launch_count()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(R):
+                fn(r)
+        comp_graphs[name] = (g, qk.launch_count() - n1)
 
-    def enqueue_steps(n, evs=None, start=0):
+    def enqueue_steps(n, start=0):
         for i in range(n):
-            ga, gq, gm = graphs[(start + i) % R]
-            if evs: evs[i][0].record(stream)
-            ga.replay()
-            if evs: evs[i][1].record(stream)
-            gq.replay()
-            if evs: evs[i][2].record(stream)
-            gm.replay()
-            if evs: evs[i][3].record(stream)
+            step_graphs[(start + i) % R].replay()
 
     with torch.cuda.stream(stream):
         enqueue_steps(args.warmup)
+        for g, _ in comp_graphs.values():
+            g.replay()
     torch.cuda.synchronize()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    KC = max(3, K // R)                    # replays of each component graph (R components each)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    e_s0, e_s1 = ev(), ev()
+    e_c = {name: (ev(), ev()) for name in comp_graphs}
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    launches = 0
     with ClockSampler(dev_index) as clk:
         time.sleep(0.3)
         with torch.cuda.stream(stream):
-            torch.cuda._sleep(int(4e6 + 250_000 * K))  # hold the stream while the host enqueues (bounded)
-            enqueue_steps(K, evs, start=args.warmup)
+            torch.cuda._sleep(int(4e6 + 250_000 * (K + 3 * KC)))  # hold the stream while the host enqueues
+            e_s0.record(stream)
+            enqueue_steps(K, start=args.warmup)
+            e_s1.record(stream)
+            launches += kernels_per_step * K
+            for name, (g, nk) in comp_graphs.items():
+                e_c[name][0].record(stream)
+                for _ in range(KC):
+                    g.replay()
+                e_c[name][1].record(stream)
+                launches += nk * KC
         torch.cuda.synchronize()
         time.sleep(0.2)
     if world > 1:
@@ -235,11 +270,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     faults = qk.qk_device_faults()
     if faults:
         raise RuntimeError(f"device fault word {faults:#x} after the timed region")
-    t_a = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in range(K)]    # µs
-    t_q = [evs[i][1].elapsed_time(evs[i][2]) * 1e3 for i in range(K)]
-    t_m = [evs[i][2].elapsed_time(evs[i][3]) * 1e3 for i in range(K)]
-    total_ms = evs[0][0].elapsed_time(evs[K - 1][3])
-    ms_per_step = total_ms / K
+    ms_per_step = e_s0.elapsed_time(e_s1) / K
+    comp_us = {name: e_c[name][0].elapsed_time(e_c[name][1]) * 1e3 / (KC * R) for name in comp_graphs}
     if world > 1:
         t = torch.tensor([ms_per_step], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -259,8 +291,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         r = i % R
         x.copy_(xh, non_blocking=True)
         x2.copy_(x2h, non_blocking=True)
-        ga, gq, gm = graphs[r]
-        ga.replay(); gq.replay(); gm.replay()
+        step_graphs[r].replay()
         for name, _ in QKV:
             outh[name].copy_(outs[name], non_blocking=True)
         bigh.copy_(out_big, non_blocking=True)
@@ -280,25 +311,25 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
 
     peaks = measured_peaks()
     hbm = peaks["hbm_gbs"]
-    med = statistics.median
-    us_a, us_q, us_m = med(t_a), med(t_q), med(t_m)
-    avg_m = sum(t_m) / K
-    achieved = MMVQ_BIG_BYTES / (avg_m * 1e-6) / 1e9
+    us_a, us_b, us_m = comp_us["a"], comp_us["b"], comp_us["m"]
+    achieved = MMVQ_BIG_BYTES / (us_m * 1e-6) / 1e9
     value = world * W_STEP / (ms_per_step * 1e-3) / 1e9
     clocks = clk.summary()
     if rank != 0:
         return None
     comp = {
-        "rms_image_qkv": {"us_median": us_a, "weight_bytes": W_QKV,
-                          "weight_gbs": W_QKV / (us_a * 1e-6) / 1e9,
-                          "hbm_frac_weights": W_QKV / (us_a * 1e-6) / 1e9 / hbm,
+        "rms_image_qkv": {"us": round(us_a, 3), "weight_bytes": W_QKV,
+                          "weight_gbs": round(W_QKV / (us_a * 1e-6) / 1e9, 1),
+                          "hbm_frac_weights": round(W_QKV / (us_a * 1e-6) / 1e9 / hbm, 4),
                           "kernels": ["rmsnorm_q8_1", "mmvq(q,k,v)"]},
-        "quantize_q8_1_8192": {"us_median": us_q, "bytes": QUANT_BIG_BYTES},
-        "mmvq_8192x8192": {"us_median": us_m, "us_mean": avg_m, "weight_bytes": W_BIG,
-                           "weight_gbs": W_BIG / (us_m * 1e-6) / 1e9,
-                           "hbm_frac_weights": W_BIG / (us_m * 1e-6) / 1e9 / hbm},
-        "ordinary_k8192_component": {"us_median": us_q + us_m,
-                                     "weight_gbs": W_BIG / ((us_q + us_m) * 1e-6) / 1e9},
+        "quantize_mmvq_k8192": {"us": round(us_b, 3), "weight_bytes": W_BIG,
+                                "weight_gbs": round(W_BIG / (us_b * 1e-6) / 1e9, 1),
+                                "hbm_frac_weights": round(W_BIG / (us_b * 1e-6) / 1e9 / hbm, 4),
+                                "kernels": ["quantize_q8_1", "mmvq(8192x8192)"]},
+        "mmvq_8192x8192": {"us": round(us_m, 3), "weight_bytes": W_BIG,
+                           "weight_gbs": round(W_BIG / (us_m * 1e-6) / 1e9, 1),
+                           "hbm_frac_weights": round(W_BIG / (us_m * 1e-6) / 1e9 / hbm, 4)},
+        "timing": f"each component graph holds {R} back-to-back replicas (rotating weights), replayed {KC} times",
     }
     return {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -311,16 +342,18 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                    "weight_replicas": R, "weight_bytes_in_rotation": R * W_STEP,
                    "l2_policy": f"weights rotate over {R} replicas ({R * W_STEP / 1e6:.0f} MB > 3x L2 "
                                 f"{l2 / 1e6:.0f} MB); activations and images are small and stay resident",
-                   "graphs": "each component captured as a CUDA graph, replayed",
+                   "graphs": "one CUDA graph per step (4 kernels, programmatic dependent launch between them)",
                    "parallelism": "replicas only" if world > 1 else "single GPU"},
         "components": comp,
         "roofline": {"kernel": "mmvq (Q4_0, K=N=8192, T=8)", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy burst)",
-                     "algorithmic_bytes_per_launch": MMVQ_BIG_BYTES, "traffic": None},
+                     "algorithmic_bytes_per_launch": MMVQ_BIG_BYTES, "traffic": recorded_traffic(),
+                     "traffic_source": "profiles/mmvq_q4_0_8192x8192_t8.md (ncu, one launch; null if the "
+                                       "kernel sources changed since)"},
         "e2e": {"value": round(W_STEP / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": kernels_per_step * K,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
 

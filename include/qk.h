@@ -24,6 +24,13 @@
  *   - The library allocates no memory and never synchronises; each call
  *     validates its arguments on the host, then enqueues its kernel(s) on
  *     `stream` (NULL = the legacy default stream) and returns.
+ *   - Kernels are launched with programmatic stream serialization: a kernel
+ *     of this library may start while the library kernel before it on the
+ *     stream is finishing, and waits for it before reading anything it may
+ *     have written. The projection kernels may begin streaming their packed
+ *     weights early, so packed weights must not be written by the library
+ *     kernel enqueued immediately before a projection that reads them
+ *     (qk_weight_pack itself always completes first).
  *   - On an invalid argument nothing is launched and a status other than
  *     QK_OK is returned; qk_last_error() gives a one-line reason (per host
  *     thread).
@@ -165,8 +172,8 @@ QK_API qk_status qk_quantize_q8_0(const float *x, int64_t T, int64_t K, int64_t 
  *       qk_quantize_q8_1 applied to y)
  *   w, b: [K] F32, required by MUL / MUL_ADD (b only by MUL_ADD), else ignored
  * Errors: QK_ERR_ARG, QK_ERR_SHAPE (K % 32 != 0: the producer's width must be
- * whole Q8_1 blocks; strides too small), QK_ERR_ALIAS (y or img overlapping
- * x, w, b or each other).
+ * whole Q8_1 blocks; strides too small), QK_ERR_UNSUPPORTED (K > 32768),
+ * QK_ERR_ALIAS (y or img overlapping x, w, b or each other).
  */
 QK_API qk_status qk_rmsnorm_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride,
                           qk_norm_kind kind, const float *w, const float *b,

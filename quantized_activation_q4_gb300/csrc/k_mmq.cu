@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(MW * 32) mmq_kernel(const __grid_constant__ Mm
     extern __shared__ __align__(16) uint8_t smem[];
     Stage *st = reinterpret_cast<Stage *>(smem);                       // [2]
     Frags *fr = reinterpret_cast<Frags *>(smem + 2 * sizeof(Stage));
+    pdl_trigger();
+    pdl_wait();
 
     const int tile = blockIdx.x;
     int j = 0;
@@ -257,9 +259,7 @@ qk_status launch_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, in
         configured = true;
     }
     dim3 grid((unsigned)tiles, (unsigned)ceil_div(T, TT));
-    mmq_kernel<<<grid, MW * 32, smem, s>>>(a);
-    count_launch();
-    return check_launch("mmq");
+    return launch_pdl("mmq", mmq_kernel, grid, dim3(MW * 32), smem, s, a);
 }
 
 }  // namespace qk

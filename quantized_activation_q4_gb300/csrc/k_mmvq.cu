@@ -328,6 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
     __shared__ int s_last[2];
     __shared__ SharedTile s_tile[2];
 
+    pdl_trigger();
     const int G = gridDim.x, cta = blockIdx.x;
     const int64_t u0 = cta_start(cta, a.U, G), u1 = cta_start(cta + 1, a.U, G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -375,6 +376,11 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
     }
 
     // ---------------- consumers
+    // The producer above streams weights without waiting for the previous
+    // kernel (no library kernel that may run just before writes packed
+    // weights); the consumers wait before reading the image, the live count or
+    // the workspace, or writing outputs.
+    pdl_wait();
     const int g = lane >> 2, t4 = lane & 3, tid = threadIdx.x;
     const int tl = live_rows(a.live, a.T);
     const uint8_t *imgB = g < tl ? a.img + (int64_t)g * a.img_row_bytes : nullptr;
@@ -568,6 +574,8 @@ __global__ void __launch_bounds__(RW * 32) mmvq_id_kernel(const __grid_constant_
     using L = Layout<WT>;
     extern __shared__ __align__(16) float red_id[];   // [RW][VALS]
     __shared__ int tok_img[8], tok_out[8];
+    pdl_trigger();
+    pdl_wait();
     const int tile = blockIdx.x;
     int j = 0;
     while (j + 1 < a.n_proj && tile >= a.p[j + 1].tiles_begin) j++;
@@ -738,9 +746,7 @@ static qk_status launch_sk(const SkArgs &a, int G, cudaStream_t s) {
         if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq: shared memory attribute: %s", cudaGetErrorString(e));
         configured = true;
     }
-    mmvq_sk_kernel<WT><<<G, THREADS, smem, s>>>(a);
-    count_launch();
-    return check_launch("mmvq");
+    return launch_pdl("mmvq", mmvq_sk_kernel<WT>, dim3(G), dim3(THREADS), smem, s, a);
 }
 
 qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj, const qk_proj *projs,
@@ -804,11 +810,8 @@ qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k
     }
     const size_t smem = (size_t)RW * VALS * sizeof(float);
     if (projs[0].wtype == QK_W_Q4_0)
-        mmvq_id_kernel<QK_W_Q4_0><<<tiles, RW * 32, smem, s>>>(a);
-    else
-        mmvq_id_kernel<QK_W_Q8_0><<<tiles, RW * 32, smem, s>>>(a);
-    count_launch();
-    return check_launch("mmvq_id");
+        return launch_pdl("mmvq_id", mmvq_id_kernel<QK_W_Q4_0>, dim3(tiles), dim3(RW * 32), smem, s, a);
+    return launch_pdl("mmvq_id", mmvq_id_kernel<QK_W_Q8_0>, dim3(tiles), dim3(RW * 32), smem, s, a);
 }
 
 }  // namespace qk

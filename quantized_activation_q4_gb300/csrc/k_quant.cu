@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
                                                        int64_t x_stride, uint8_t *__restrict__ out,
                                                        int8_t *__restrict__ qs, uint16_t *__restrict__ dh,
                                                        int64_t row_blocks, int T, const int32_t *live) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.y;
     if (t >= live_rows(live, T)) return;
     const int lane = threadIdx.x & 31, j8 = lane & 7;
@@ -106,66 +108,77 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
 }
 
 // ---------------------------------------------------------------- RMS producer
-// One CTA of 256 threads per row. Thread i handles columns 4i + 1024*it.
-__global__ void __launch_bounds__(256) rmsnorm_q8_1_kernel(
+// One CTA of 1024 threads per row; the row stays in registers between the
+// sum of squares and the output (thread i holds columns 4i + 4096*it, up to
+// RMS_ITEMS float4, so K <= 32768).
+constexpr int RMS_THREADS = 1024;
+constexpr int RMS_ITEMS = 8;
+
+__global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
     const float *__restrict__ x, int K, int64_t x_stride, int kind, const float *__restrict__ w,
     const float *__restrict__ bias, float scale, float eps, float *__restrict__ y, int64_t y_stride,
     uint8_t *__restrict__ img, int64_t row_blocks, int T, const int32_t *live) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     if (t >= live_rows(live, T)) return;
     const float *xr = x + t * x_stride;
     const int tid = threadIdx.x, lane = tid & 31, j8 = lane & 7;
 
+    float v[RMS_ITEMS][4];
     float ss = 0.0f;
-    for (int c = 4 * tid; c < K; c += 1024) {
-        float v[4];
-        load4(xr + c, K - c, v);
-        ss += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+    for (int it = 0; it < RMS_ITEMS; it++) {
+        const int c = 4 * tid + 4 * RMS_THREADS * it;
+        v[it][0] = v[it][1] = v[it][2] = v[it][3] = 0.0f;
+        if (c < K) {
+            load4(xr + c, 4, v[it]);
+            ss += v[it][0] * v[it][0] + v[it][1] * v[it][1] + v[it][2] * v[it][2] + v[it][3] * v[it][3];
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
-    __shared__ float red[8];
-    __shared__ float rs;
+    __shared__ float red[RMS_THREADS / 32];
     if (lane == 0) red[tid >> 5] = ss;
     __syncthreads();
-    if (tid == 0) {
-        float tot = 0.0f;
-        for (int i = 0; i < 8; i++) tot += red[i];
-        rs = 1.0f / sqrtf(tot / (float)K + eps);
+    if (tid < 32) {
+        float tot = red[tid];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+        if (tid == 0) red[0] = 1.0f / sqrtf(tot / (float)K + eps);
     }
     __syncthreads();
-    const float r = rs;
+    const float r = red[0];
 
     float *yr = y + t * y_stride;
     uint8_t *ir = img + t * row_blocks * Q8_1_BYTES;
-    const int iters = (int)((K + 1023) / 1024);
-    for (int it = 0; it < iters; it++) {           // uniform trip count: shuffles stay full-warp
-        const int c = 4 * tid + 1024 * it;
-        const bool ok = c < K;                     // K % 32 == 0: whole 8-lane groups agree
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int it = 0; it < RMS_ITEMS; it++) {
+        if (4 * RMS_THREADS * it >= K) break;               // uniform: no warp has columns left
+        const int c = 4 * tid + 4 * RMS_THREADS * it;
+        const bool ok = c < K;                               // K % 32 == 0: whole 8-lane groups agree
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
         if (ok) {
-            load4(xr + c, 4, v);
             float wv[4], bv[4];
             if (kind == QK_NORM_MUL || kind == QK_NORM_MUL_ADD) load4(w + c, 4, wv);
             if (kind == QK_NORM_MUL_ADD) load4(bias + c, 4, bv);
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-                float o = v[i] * r;
-                if (kind == QK_NORM_MUL) o = o * wv[i];
-                else if (kind == QK_NORM_MUL_ADD) o = o * wv[i] + bv[i];
-                else if (kind == QK_NORM_SCALE) o = o * scale;
-                v[i] = o;
+                float q = v[it][i] * r;
+                if (kind == QK_NORM_MUL) q = q * wv[i];
+                else if (kind == QK_NORM_MUL_ADD) q = q * wv[i] + bv[i];
+                else if (kind == QK_NORM_SCALE) q = q * scale;
+                o[i] = q;
             }
-            store4(yr + c, v);
+            store4(yr + c, o);
         }
         uint32_t codes;
         int sum;
-        const float d = q8_block(v, &codes, &sum);
+        const float d = q8_block(o, &codes, &sum);   // all lanes of the warp take part
         if (ok) put_q8_1(ir + (int64_t)(c / QB) * Q8_1_BYTES, j8, d, codes, sum);
     }
     // zero blocks of the row padding
-    const int kb = K / QB;
-    for (int64_t bb = kb + tid; bb < row_blocks; bb += 256) {
+    for (int64_t bb = K / QB + tid; bb < row_blocks; bb += RMS_THREADS) {
         uint32_t *p = reinterpret_cast<uint32_t *>(ir + bb * Q8_1_BYTES);
 #pragma unroll
         for (int i = 0; i < 9; i++) p[i] = 0u;
@@ -187,6 +200,8 @@ __global__ void __launch_bounds__(256) glu_q8_1_kernel(
     int kind, int layout, const float *__restrict__ a, int64_t a_stride, const float *__restrict__ b,
     int64_t b_stride, int N, float *__restrict__ out, int64_t out_stride, uint8_t *__restrict__ img,
     int64_t row_blocks, int T, const int32_t *live) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.y;
     if (t >= live_rows(live, T)) return;
     const int tid = threadIdx.x, j8 = tid & 7;
@@ -232,18 +247,16 @@ qk_status launch_quantize_q8_1(const float *x, int T, int K, int64_t x_stride, u
                                int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
     dim3 grid((unsigned)ceil_div(row_blocks, 32), (unsigned)T);
-    quantize_kernel<true><<<grid, 256, 0, s>>>(x, K, x_stride, img, nullptr, nullptr, row_blocks, T, live);
-    count_launch();
-    return check_launch("quantize_q8_1");
+    return launch_pdl("quantize_q8_1", quantize_kernel<true>, grid, dim3(256), 0, s, x, K, x_stride, img,
+                      (int8_t *)nullptr, (uint16_t *)nullptr, row_blocks, T, live);
 }
 
 qk_status launch_quantize_q8_0(const float *x, int T, int K, int64_t x_stride, int8_t *qs,
                                uint16_t *d, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
     dim3 grid((unsigned)ceil_div(row_blocks, 32), (unsigned)T);
-    quantize_kernel<false><<<grid, 256, 0, s>>>(x, K, x_stride, nullptr, qs, d, row_blocks, T, live);
-    count_launch();
-    return check_launch("quantize_q8_0");
+    return launch_pdl("quantize_q8_0", quantize_kernel<false>, grid, dim3(256), 0, s, x, K, x_stride,
+                      (uint8_t *)nullptr, qs, d, row_blocks, T, live);
 }
 
 qk_status launch_rmsnorm_q8_1(const float *x, int T, int K, int64_t x_stride, int kind,
@@ -251,10 +264,8 @@ qk_status launch_rmsnorm_q8_1(const float *x, int T, int K, int64_t x_stride, in
                               int64_t y_stride, uint8_t *img, int64_t row_blocks,
                               const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
-    rmsnorm_q8_1_kernel<<<T, 256, 0, s>>>(x, K, x_stride, kind, w, b, scale, eps, y, y_stride, img,
-                                          row_blocks, T, live);
-    count_launch();
-    return check_launch("rmsnorm_q8_1");
+    return launch_pdl("rmsnorm_q8_1", rmsnorm_q8_1_kernel, dim3((unsigned)T), dim3(RMS_THREADS), 0, s, x, K,
+                      x_stride, kind, w, b, scale, eps, y, y_stride, img, row_blocks, T, live);
 }
 
 qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride, const float *b,
@@ -262,10 +273,8 @@ qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride
                           uint8_t *img, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
     dim3 grid((unsigned)ceil_div(N, 1024), (unsigned)T);
-    glu_q8_1_kernel<<<grid, 256, 0, s>>>(kind, layout, a, a_stride, b, b_stride, N, out, out_stride,
-                                         img, row_blocks, T, live);
-    count_launch();
-    return check_launch("glu_q8_1");
+    return launch_pdl("glu_q8_1", glu_q8_1_kernel, grid, dim3(256), 0, s, kind, layout, a, a_stride, b, b_stride,
+                      N, out, out_stride, img, row_blocks, T, live);
 }
 
 }  // namespace qk

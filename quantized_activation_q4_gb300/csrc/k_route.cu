@@ -19,6 +19,8 @@ constexpr int MAX_E_PER_LANE = 8;   // E <= 256
 __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int rows, int E,
                                                    int k, int32_t *__restrict__ ids,
                                                    float *__restrict__ wts, const int32_t *live) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= live_rows(live, rows)) return;   // warp-uniform
@@ -87,6 +89,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
     int32_t *seg = sm;                 // [32][E] per-warp counts, then per-warp bases
     int32_t *off = sm + 32 * E;        // [E + 1]
     __shared__ int32_t wsum[32];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int npairs = live_rows(live, rows) * k;
     const int per = (npairs + 31) / 32;
@@ -166,9 +170,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
 qk_status launch_topk_route(const float *logits, int rows, int E, int k, int32_t *ids, float *wts,
                             const int32_t *live, cudaStream_t s) {
     if (rows == 0) return QK_OK;
-    topk_kernel<<<(unsigned)ceil_div(rows, 8), 256, 0, s>>>(logits, rows, E, k, ids, wts, live);
-    count_launch();
-    return check_launch("topk_route");
+    return launch_pdl("topk_route", topk_kernel, dim3((unsigned)ceil_div(rows, 8)), dim3(256), 0, s, logits, rows,
+                      E, k, ids, wts, live);
 }
 
 qk_status launch_moe_plan(const int32_t *ids, int rows, int k, int E, int32_t *counts,
@@ -179,9 +182,8 @@ qk_status launch_moe_plan(const int32_t *ids, int rows, int k, int E, int32_t *c
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         configured = (int)smem;
     }
-    plan_kernel<<<1, 1024, smem, s>>>(ids, rows, k, E, counts, offsets, items, live);
-    count_launch();
-    return check_launch("moe_plan");
+    return launch_pdl("moe_plan", plan_kernel, dim3(1), dim3(1024), smem, s, ids, rows, k, E, counts, offsets,
+                      items, live);
 }
 
 }  // namespace qk

@@ -112,6 +112,7 @@ qk_status qk_rmsnorm_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride
     if (st != QK_OK) return st;
     REQUIRE(kind >= QK_NORM_PLAIN && kind <= QK_NORM_SCALE, QK_ERR_ARG, "bad norm kind %d", (int)kind);
     REQUIRE(K % QB == 0, QK_ERR_SHAPE, "K=%lld is not a whole number of 32-blocks", (long long)K);
+    REQUIRE(K <= 32768, QK_ERR_UNSUPPORTED, "K=%lld > 32768 (a row is kept in registers)", (long long)K);
     REQUIRE((y && img) || T == 0, QK_ERR_ARG, "y or img is null");
     const bool need_w = kind == QK_NORM_MUL || kind == QK_NORM_MUL_ADD;
     REQUIRE(!need_w || w, QK_ERR_ARG, "w is null for a MUL kind");

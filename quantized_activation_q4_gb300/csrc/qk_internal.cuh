@@ -35,6 +35,14 @@ constexpr int Q8_1_BYTES = 36;   // half d, half s, 32 codes
 constexpr int Q4_0_BYTES = 18;
 constexpr int Q8_0_BYTES = 34;
 
+// Programmatic dependent launch. Every compute kernel of the library lets the
+// next kernel on the stream start launching as soon as all of its own CTAs are
+// resident (trigger), and waits for the previous kernel's completion and
+// memory before it reads anything that kernel may have written (wait). Both
+// are no-ops when the launch has no programmatic dependency.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Live rows: min(rows, max(0, *live)), or rows when no pointer is given.
 __device__ __forceinline__ int live_rows(const int32_t *live, int rows) {
     if (!live) return rows;
@@ -72,6 +80,26 @@ inline int64_t packed_bytes(int wtype, int64_t N, int64_t K) {
 // Reads and clears the device-side fault word (bit 0: a bounded mbarrier
 // wait gave up). Synchronous.
 qk_status read_device_faults(uint32_t *faults);
+
+// Launch with programmatic stream serialization (see pdl_trigger/pdl_wait).
+template <typename... KArgs, typename... Args>
+qk_status launch_pdl(const char *name, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    count_launch();
+    if (e != cudaSuccess) return fail(QK_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
+    return check_launch(name);
+}
 
 // ------------------------------------------------------- kernel launchers
 // Defined in the kernel translation units; arguments already validated.
