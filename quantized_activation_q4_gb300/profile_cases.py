@@ -5,7 +5,10 @@
 Each case builds its seeded inputs, runs the case's kernel `reps` times
 through the C ABI (the first launches warm up) and synchronises, so that an
 ncu capture of the last launch (`-k regex:<kernel> -s <reps-1> -c 1`) sees
-one steady-state launch. Cases:
+one steady-state launch. With `--time N` it then times N more launches, one
+by one with CUDA events on the current stream, each after a 512 MB write that
+flushes the 129 MB L2 (so weights come from HBM), and prints the median
+duration with the case's algorithmic bytes (or flops) per launch. Cases:
 
   mmvq_8192     qk_mmvq, Q4_0 8192x8192, T=8        (kernel mmvq_sk)
   mmvq_qkv      qk_mmvq, q/k/v 3584->3584/512/512   (kernel mmvq_sk)
@@ -13,13 +16,14 @@ one steady-state launch. Cases:
   rmsnorm       qk_rmsnorm_q8_1, [8, 3584] x w      (kernel rmsnorm_q8_1)
   quantize      qk_quantize_q8_1, [8, 8192]         (kernel quantize)
   glu           qk_glu_q8_1 SwiGLU packed [8, 18944] (kernel glu_q8_1)
-  mmvq_id       qk_mmvq_id, 128 experts, top-8, live 128 rows (kernel mmvq_id)
+  mmvq_id_<R>   qk_mmvq_id, gate+up 2560->768 over 128 experts, top-8 of R rows (kernel mmvq_id)
   mmq_qkv       qk_mmq, 3325 tokens, q/k/v          (kernel mmq)
   quantize_q8_0 qk_quantize_q8_0, [3325, 3584]      (kernel quantize)
 """
 from __future__ import annotations
 
 import argparse
+import json
 import os
 import sys
 
@@ -52,9 +56,14 @@ def _image(T, K, seed=2):
     return img
 
 
+Q4_ROW_BYTES = 18          # one Q4_0 block of 32 weights
+Q8_1_BLOCK = 36
+
+
 def _mmvq_case(shapes, K, T=8):
     import torch
     keep, projs = [], []
+    nbytes = sum(N * (K // 32) * Q4_ROW_BYTES + T * N * 4 for N in shapes) + T * (K // 32) * Q8_1_BLOCK
     for i, N in enumerate(shapes):
         w = _packed(10 + i, N, K)
         y = torch.empty((T, N), dtype=torch.float32, device="cuda")
@@ -64,7 +73,7 @@ def _mmvq_case(shapes, K, T=8):
     n = qk.qk_mmvq_workspace_bytes(projs)
     ws = torch.zeros((n,), dtype=torch.uint8, device="cuda")
     keep += [img, ws]
-    return lambda: qk.qk_mmvq(img, K // 32, T, projs, ws, n), keep
+    return lambda: qk.qk_mmvq(img, K // 32, T, projs, ws, n), keep, {"bytes": nbytes}
 
 
 def build_case(name):
@@ -80,20 +89,25 @@ def build_case(name):
         x, w = _dev(synth.activations(1, T, K)), _dev(synth.norm_weight(2, K))
         y = torch.empty((T, K), dtype=torch.float32, device="cuda")
         img = torch.empty((T * K // 32 * 36,), dtype=torch.uint8, device="cuda")
-        return lambda: qk.qk_rmsnorm_q8_1(x, T, K, K, "mul", w, None, 1.0, 1e-6, y, K, img, K // 32), [x, w, y, img]
+        nbytes = 2 * T * K * 4 + K * 4 + T * (K // 32) * Q8_1_BLOCK
+        return (lambda: qk.qk_rmsnorm_q8_1(x, T, K, K, "mul", w, None, 1.0, 1e-6, y, K, img, K // 32),
+                [x, w, y, img], {"bytes": nbytes})
     if name == "quantize":
         T, K = 8, 8192
         x = _dev(synth.activations(1, T, K))
         img = torch.empty((T * K // 32 * 36,), dtype=torch.uint8, device="cuda")
-        return lambda: qk.qk_quantize_q8_1(x, T, K, K, img, K // 32), [x, img]
+        return (lambda: qk.qk_quantize_q8_1(x, T, K, K, img, K // 32), [x, img],
+                {"bytes": T * K * 4 + T * (K // 32) * Q8_1_BLOCK})
     if name == "glu":
         T, N = 8, 18944
         a = _dev(np.concatenate([synth.activations(1, T, N), synth.activations(2, T, N)], axis=1))
         out = torch.empty((T, N), dtype=torch.float32, device="cuda")
         img = torch.empty((T * N // 32 * 36,), dtype=torch.uint8, device="cuda")
-        return lambda: qk.qk_glu_q8_1("swiglu", "packed", a, 2 * N, None, 0, T, N, out, N, img, N // 32), [a, out, img]
-    if name == "mmvq_id":
-        E, k, K, NF, rows = 128, 8, 2560, 768, 128
+        nbytes = 3 * T * N * 4 + T * (N // 32) * Q8_1_BLOCK
+        return (lambda: qk.qk_glu_q8_1("swiglu", "packed", a, 2 * N, None, 0, T, N, out, N, img, N // 32),
+                [a, out, img], {"bytes": nbytes})
+    if name.startswith("mmvq_id_"):
+        E, k, K, NF, rows = 128, 8, 2560, 768, int(name.rsplit("_", 1)[1])
         per = qk.qk_weight_packed_bytes("q4_0", NF, K)
         ws = []
         for p in range(2):
@@ -113,7 +127,10 @@ def build_case(name):
         ys = [torch.empty((rows * k, NF), dtype=torch.float32, device="cuda") for _ in range(2)]
         projs = [qk.make_proj_id("q4_0", E, ws[p], NF, K, ys[p]) for p in range(2)]
         keep = ws + ys + [img, ids, wts, counts, offsets, items]
-        return lambda: qk.qk_mmvq_id(img, K // 32, rows, k, projs, counts, offsets, items), keep
+        live = int((counts > 0).sum().item())
+        nbytes = 2 * live * NF * (K // 32) * Q4_ROW_BYTES + 2 * rows * k * NF * 4 + rows * (K // 32) * Q8_1_BLOCK
+        return (lambda: qk.qk_mmvq_id(img, K // 32, rows, k, projs, counts, offsets, items), keep,
+                {"bytes": nbytes, "live_experts": live})
     if name in ("mmq_qkv", "quantize_q8_0"):
         T, K = 3325, 3584
         x = _dev(synth.activations(4, T, K))
@@ -121,7 +138,7 @@ def build_case(name):
         d = torch.empty((T * 112,), dtype=torch.int16, device="cuda")
         quant = lambda: qk.qk_quantize_q8_0(x, T, K, K, qs, d, 112)
         if name == "quantize_q8_0":
-            return quant, [x, qs, d]
+            return quant, [x, qs, d], {"bytes": T * K * 4 + T * K + T * (K // 32) * 2}
         quant()
         keep, projs = [x, qs, d], []
         for i, N in enumerate((3584, 512, 512)):
@@ -129,7 +146,7 @@ def build_case(name):
             y = torch.empty((T, N), dtype=torch.float32, device="cuda")
             keep += [w, y]
             projs.append(qk.make_proj("q4_0", w, N, K, y, N))
-        return lambda: qk.qk_mmq(qs, d, 112, T, projs), keep
+        return lambda: qk.qk_mmq(qs, d, 112, T, projs), keep, {"flops": 2 * T * K * (3584 + 512 + 512)}
     raise SystemExit(f"unknown case {name!r}")
 
 
@@ -137,10 +154,11 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case")
     ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--time", type=int, default=0, metavar="N")
     args = ap.parse_args()
     import torch
     qk.load(build_if_missing=True)
-    run, keep = build_case(args.case)
+    run, keep, info = build_case(args.case)
     torch.cuda.synchronize()
     for _ in range(args.reps):
         run()
@@ -149,6 +167,22 @@ def main():
     if faults:
         raise SystemExit(f"device fault word {faults:#x}")
     print(f"{args.case}: {args.reps} launches ok")
+    if args.time:
+        flush = torch.empty((512 << 20,), dtype=torch.uint8, device="cuda")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.time)]
+        for e0, e1 in ev:
+            flush.fill_(1)
+            e0.record()
+            run()
+            e1.record()
+        torch.cuda.synchronize()
+        us = float(np.median([e0.elapsed_time(e1) * 1e3 for e0, e1 in ev]))
+        line = {"case": args.case, "median_us": round(us, 3), "launches": args.time, **info}
+        if "bytes" in info:
+            line["GB_per_s"] = round(info["bytes"] / us / 1e3, 1)
+        if "flops" in info:
+            line["TFLOP_per_s"] = round(info["flops"] / us / 1e6, 2)
+        print(json.dumps(line))
 
 
 if __name__ == "__main__":
