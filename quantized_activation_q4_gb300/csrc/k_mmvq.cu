@@ -43,12 +43,12 @@ namespace {
 __device__ unsigned int g_qk_faults = 0;
 
 constexpr int MAX_PROJ = 8;
-constexpr int CW = 15;                       // consumer warps (ordinary path); with the
-constexpr int THREADS = (CW + 1) * 32;       // producer, 16 warps = 4 per SM sub-partition
-constexpr int VALS = UNIT_GROUPS * 4 * 32;   // accumulators of one 128-row tile per warp
-constexpr int HALF_VALS = VALS / 2;          // reduced in two passes of 4 row groups
+constexpr int VALS = UNIT_GROUPS * 4 * 32;   // accumulator values of one 128-row tile
 constexpr int MAXP = 8;                      // partial sums loaded per batch
-constexpr uint32_t SPIN_LIMIT = 1u << 22;
+// A wait suspends the thread until the phase completes or SUSPEND_NS passes,
+// and gives up after SPIN_LIMIT tries (at most about a second).
+constexpr uint32_t SUSPEND_NS = 20000;
+constexpr uint32_t SPIN_LIMIT = 1u << 16;
 
 template <int WT> struct Layout;
 template <> struct Layout<QK_W_Q4_0> {
@@ -110,9 +110,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
 __device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(a), "r"(parity)
+        : "r"(a), "r"(parity), "r"(SUSPEND_NS)
         : "memory");
     return ok != 0;
 }
@@ -150,10 +150,6 @@ struct SharedTile {
     int first_slot;          // part slot used by c_first (later CTAs use slot 0)
 };
 
-__device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory");
-}
-
 // D = A * B + C (m16n8k16, f16 inputs, f32 accumulate); D and C may differ.
 __device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1,
                                         const float c[4]) {
@@ -178,25 +174,6 @@ __device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &h02, uint32
     h13 = *reinterpret_cast<uint32_t *>(&hb);
 }
 
-// Q4_0 word (nibble bytes B0..B3) -> biased halves of one row for the two MMAs:
-//   lo02 = (1024+lo B0, 1024+lo B2), lo13 = (1024+lo B1, 1024+lo B3)
-//   hi02 = (  64+hi B0,   64+hi B2), hi13 = (  64+hi B1,   64+hi B3)
-__device__ __forceinline__ void nibbles_to_half2(uint32_t w, uint32_t &lo02, uint32_t &lo13,
-                                                 uint32_t &hi02, uint32_t &hi13) {
-    const uint32_t w8 = w >> 8;
-    lo02 = (w & 0x000F000Fu) | 0x64006400u;
-    hi02 = (w & 0x00F000F0u) | 0x54005400u;
-    lo13 = (w8 & 0x000F000Fu) | 0x64006400u;
-    hi13 = (w8 & 0x00F000F0u) | 0x54005400u;
-}
-
-// Q8_0 weight codes keep their +1152 bias (removed by the correction MMAs).
-__device__ __forceinline__ void wcodes_to_half2(uint32_t w, uint32_t &h02, uint32_t &h13) {
-    const uint32_t u = w ^ 0x80808080u;
-    h02 = __byte_perm(u, 0x64646464u, 0x4240);
-    h13 = __byte_perm(u, 0x64646464u, 0x4341);
-}
-
 // ---------------------------------------------------------------- one block
 // Activation side of block b for this lane: B fragments of token g (elements
 // 4t..4t+3 and 16+4t..16+4t+3), scales of tokens 2t and 2t+1, and the bias
@@ -214,7 +191,7 @@ struct BSide {
 __device__ __forceinline__ Raw load_raw(const uint8_t *imgB, const uint8_t *imgS0, const uint8_t *imgS1, int b,
                                         int t4) {
     Raw r = {0u, 0u, 0u, 0u};
-    const int64_t off = (int64_t)b * Q8_1_BYTES;
+    const uint32_t off = (uint32_t)b * Q8_1_BYTES;   // b < 2^26 (K < 2^31)
     if (imgB) {
         r.lo = ld_img4(imgB + off + 4 + 4 * t4);
         r.hi = ld_img4(imgB + off + 20 + 4 * t4);
@@ -243,12 +220,63 @@ __device__ __forceinline__ void bside(const Raw &r, BSide &s) {
     mma_f16(s.corr, ahi, s.hi02, s.hi13, c1);
 }
 
-// Row group: two MMAs seeded with the correction, then the scale epilogue.
-__device__ __forceinline__ void row_group(const uint32_t a_lo[4], const uint32_t a_hi[4], uint32_t dw2,
-                                          const BSide &s, float acc[4]) {
-    float d1[4], dv[4];
-    mma_f16(d1, a_lo, s.lo02, s.lo13, s.corr);
-    mma_f16(dv, a_hi, s.hi02, s.hi13, d1);
+// Block dot of one row group in a single asm block, so that the weight
+// conversions write the MMA operand registers directly (built in C++, the
+// operand arrays cost extra register moves):
+//   D = A_lo * (lo02, lo13) + A_hi * (hi02, hi13) + C.
+// Q4_0: w, w8 = nibble words of rows g and g+8 (see nibbles_to_half2).
+__device__ __forceinline__ void dot_q4(uint32_t w, uint32_t w8, const BSide &s, float d[4]) {
+    asm("{\n"
+        ".reg .b32 s0, s1, l0, l1, l2, l3, h0, h1, h2, h3;\n"
+        ".reg .f32 e0, e1, e2, e3;\n"
+        "shr.b32 s0, %4, 8;\n"
+        "shr.b32 s1, %5, 8;\n"
+        "lop3.b32 l0, %4, 0x000F000F, 0x64006400, 0xEA;\n"
+        "lop3.b32 l1, %5, 0x000F000F, 0x64006400, 0xEA;\n"
+        "lop3.b32 l2, s0, 0x000F000F, 0x64006400, 0xEA;\n"
+        "lop3.b32 l3, s1, 0x000F000F, 0x64006400, 0xEA;\n"
+        "lop3.b32 h0, %4, 0x00F000F0, 0x54005400, 0xEA;\n"
+        "lop3.b32 h1, %5, 0x00F000F0, 0x54005400, 0xEA;\n"
+        "lop3.b32 h2, s0, 0x00F000F0, 0x54005400, 0xEA;\n"
+        "lop3.b32 h3, s1, 0x00F000F0, 0x54005400, 0xEA;\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {e0,e1,e2,e3}, {l0,l1,l2,l3}, {%6,%7}, "
+        "{%10,%11,%12,%13};\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {h0,h1,h2,h3}, {%8,%9}, "
+        "{e0,e1,e2,e3};\n"
+        "}\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(w), "r"(w8), "r"(s.lo02), "r"(s.lo13), "r"(s.hi02), "r"(s.hi13), "f"(s.corr[0]), "f"(s.corr[1]),
+          "f"(s.corr[2]), "f"(s.corr[3]));
+}
+// Q8_0: v = one row group's 16 bytes (see the weight pack): codes of row g
+// (elements 4t.. and 16+4t..) and of row g+8.
+__device__ __forceinline__ void dot_q8(uint4 v, const BSide &s, float d[4]) {
+    asm("{\n"
+        ".reg .b32 u0, u1, u2, u3, l0, l1, l2, l3, h0, h1, h2, h3;\n"
+        ".reg .f32 e0, e1, e2, e3;\n"
+        "xor.b32 u0, %4, 0x80808080;\n"
+        "xor.b32 u1, %5, 0x80808080;\n"
+        "xor.b32 u2, %6, 0x80808080;\n"
+        "xor.b32 u3, %7, 0x80808080;\n"
+        "prmt.b32 l0, u0, 0x64646464, 0x4240;\n"
+        "prmt.b32 l2, u0, 0x64646464, 0x4341;\n"
+        "prmt.b32 h0, u1, 0x64646464, 0x4240;\n"
+        "prmt.b32 h2, u1, 0x64646464, 0x4341;\n"
+        "prmt.b32 l1, u2, 0x64646464, 0x4240;\n"
+        "prmt.b32 l3, u2, 0x64646464, 0x4341;\n"
+        "prmt.b32 h1, u3, 0x64646464, 0x4240;\n"
+        "prmt.b32 h3, u3, 0x64646464, 0x4341;\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {e0,e1,e2,e3}, {l0,l1,l2,l3}, {%8,%9}, "
+        "{%12,%13,%14,%15};\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {h0,h1,h2,h3}, {%10,%11}, "
+        "{e0,e1,e2,e3};\n"
+        "}\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(s.lo02), "r"(s.lo13), "r"(s.hi02), "r"(s.hi13),
+          "f"(s.corr[0]), "f"(s.corr[1]), "f"(s.corr[2]), "f"(s.corr[3]));
+}
+
+__device__ __forceinline__ void scale_epilogue(const float dv[4], uint32_t dw2, const BSide &s, float acc[4]) {
     const float2 dw = __half22float2(as_h2(dw2));   // (row g, row g+8)
     acc[0] = fmaf(dw.x, fmaf(s.da0, dv[0], s.ns0), acc[0]);
     acc[1] = fmaf(dw.x, fmaf(s.da1, dv[1], s.ns1), acc[1]);
@@ -275,26 +303,126 @@ __device__ __forceinline__ void block_rows(const uint8_t *gblk, uint32_t sblk, c
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             const uint4 v = SMEM ? lds128(sblk + k * 512 + lane * 16) : ldg_stream16(gblk + k * 512 + lane * 16);
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const uint32_t wg = h ? v.z : v.x, wg8 = h ? v.w : v.y;
-                uint32_t a_lo[4], a_hi[4];
-                nibbles_to_half2(wg, a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
-                nibbles_to_half2(wg8, a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
-                row_group(a_lo, a_hi, scw[2 * k + h], s, acc[2 * k + h]);
-            }
+            float d0[4], d1[4];
+            dot_q4(v.x, v.y, s, d0);
+            dot_q4(v.z, v.w, s, d1);
+            scale_epilogue(d0, scw[2 * k], s, acc[2 * k]);
+            scale_epilogue(d1, scw[2 * k + 1], s, acc[2 * k + 1]);
         }
     } else {
 #pragma unroll
         for (int k = 0; k < 8; k++) {
             const uint4 v = SMEM ? lds128(sblk + k * 512 + lane * 16) : ldg_stream16(gblk + k * 512 + lane * 16);
-            uint32_t a_lo[4], a_hi[4];
-            wcodes_to_half2(v.x, a_lo[0], a_lo[2]);
-            wcodes_to_half2(v.y, a_hi[0], a_hi[2]);
-            wcodes_to_half2(v.z, a_lo[1], a_lo[3]);
-            wcodes_to_half2(v.w, a_hi[1], a_hi[3]);
-            row_group(a_lo, a_hi, scw[k], s, acc[k]);
+            float d[4];
+            dot_q8(v, s, d);
+            scale_epilogue(d, scw[k], s, acc[k]);
         }
+    }
+}
+
+// ---------------------------------------------------------------- ordinary path
+// One persistent CTA per SM: a producer warp streams the CTA's units with TMA
+// bulk copies into a ring of shared-memory slots (full/empty mbarriers), and
+// 16 consumer warps work on four units at once. Warp w belongs to unit phase
+// q = w >> 2 (the CTA's units with index = q mod 4) and owns row-group pair
+// p = w & 3 (rows 32p..32p+31 of the 128-row tile), over all four blocks of
+// each of its units, so it keeps only 2 x 4 accumulators. The activation side
+// of a unit is shared through shared memory: warp (p, q) turns the image words
+// of block p into an activation record (the B fragments of every lane, the
+// bias-correction C operand and (d_a, -8 s_a) per pair of tokens), and the
+// four warps of the phase meet at a named barrier before reading all four
+// records. A slot is empty again when the phase's 128 threads have loaded
+// their operands from it (each thread arrives after its own loads). At the end
+// of a segment (the CTA's units of one row tile) the four phases' partial sums
+// are added in fixed order.
+constexpr int SK_CONS = 16;
+constexpr int SK_PRODUCER = SK_CONS;
+constexpr int SK_THREADS = (SK_CONS + 1) * 32;
+constexpr int BREC = 640;       // [0,512) fragments (16 B per lane), [512,576) C quads, [576,640) scales (per t4)
+constexpr int IMG_AHEAD = 3;    // units of image words a consumer warp has in flight
+
+template <int WT>
+struct SkLayout {
+    static constexpr int UNIT = Layout<WT>::UNIT, SLOTS = Layout<WT>::SLOTS;
+    static constexpr int SLOT = UNIT;
+    static constexpr int RECS = SLOTS * SLOT;                     // [4 phases][2][4 blocks][BREC]
+    static constexpr int RED = RECS + 4 * 2 * 4 * BREC;           // [SK_CONS][256] floats
+    static constexpr int KEEP = RED + SK_CONS * 256 * 4;          // [2][VALS] floats
+    static constexpr int BARS = KEEP + 2 * VALS * 4;              // full[SLOTS], empty[SLOTS]
+    static constexpr int BYTES = BARS + 2 * SLOTS * 8;
+};
+
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void all_consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(SK_CONS * 32) : "memory");
+}
+// The four warps of unit phase q (barriers 2..5). A warp writes its record of
+// unit k into buffer k & 1 and reads all four after this barrier; it can only
+// write buffer k & 1 again (unit k+2) after the barrier of unit k+1, which the
+// other three warps pass only once they have read unit k's records.
+__device__ __forceinline__ void phase_sync(int q) {
+    asm volatile("bar.sync %0, 128;" ::"r"(2 + q) : "memory");
+}
+
+// Activation record of one block from its image words (zero words: zero record).
+template <int WT>
+__device__ __forceinline__ void write_record(uint32_t rec, const Raw &r, int lane) {
+    BSide s;
+    bside<WT>(r, s);
+    sts128(rec + lane * 16, make_uint4(s.lo02, s.lo13, s.hi02, s.hi13));
+    if (lane < 4) {   // lanes 0..3: g = 0, t4 = lane; the records depend on t4 only
+        sts128(rec + 512 + lane * 16, make_uint4(__float_as_uint(s.corr[0]), __float_as_uint(s.corr[1]),
+                                                 __float_as_uint(s.corr[2]), __float_as_uint(s.corr[3])));
+        sts128(rec + 576 + lane * 16, make_uint4(__float_as_uint(s.da0), __float_as_uint(s.da1),
+                                                 __float_as_uint(s.ns0), __float_as_uint(s.ns1)));
+    }
+}
+
+// Row groups 2p and 2p+1 (rows 32p..32p+31) of all four blocks of the unit in
+// ring slot sb: weights and scales from the unit, B operands, correction and
+// token scales from the unit's four activation records at recs.
+template <int WT>
+__device__ __forceinline__ void unit_rows(uint32_t sb, uint32_t recs, int p, int lane, float acc[2][4]) {
+    using L = Layout<WT>;
+    const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int jb = 0; jb < 4; jb++) {
+        const uint32_t rec = recs + jb * BREC;
+        const uint4 bf = lds128(rec + lane * 16);
+        const uint4 cq = lds128(rec + 512 + t4 * 16);
+        const uint4 dq = lds128(rec + 576 + t4 * 16);
+        const uint2 sc = lds64(sb + L::SCALES + jb * 256 + g * 32 + p * 8);
+        BSide s;
+        s.lo02 = bf.x;
+        s.lo13 = bf.y;
+        s.hi02 = bf.z;
+        s.hi13 = bf.w;
+        s.corr[0] = __uint_as_float(cq.x);
+        s.corr[1] = __uint_as_float(cq.y);
+        s.corr[2] = __uint_as_float(cq.z);
+        s.corr[3] = __uint_as_float(cq.w);
+        s.da0 = __uint_as_float(dq.x);
+        s.da1 = __uint_as_float(dq.y);
+        s.ns0 = __uint_as_float(dq.z);
+        s.ns1 = __uint_as_float(dq.w);
+        float d0[4], d1[4];
+        if (WT == QK_W_Q4_0) {
+            const uint4 w = lds128(sb + jb * L::BLOCK + p * 512 + lane * 16);
+            dot_q4(w.x, w.y, s, d0);
+            dot_q4(w.z, w.w, s, d1);
+        } else {
+            dot_q8(lds128(sb + jb * L::BLOCK + (2 * p) * 512 + lane * 16), s, d0);
+            dot_q8(lds128(sb + jb * L::BLOCK + (2 * p + 1) * 512 + lane * 16), s, d1);
+        }
+        scale_epilogue(d0, sc.x, s, acc[0]);
+        scale_epilogue(d1, sc.y, s, acc[1]);
     }
 }
 
@@ -315,15 +443,23 @@ __device__ __forceinline__ int cta_of(int64_t u, int64_t U, int G) {
     return c;
 }
 
-// ---------------------------------------------------------------- ordinary path
+// Unit u of the flat unit space -> projection j, row tile rt, column chunk c.
+__device__ __forceinline__ void decode_unit(const SkArgs &a, int64_t u, int &j, int &rt, int &c) {
+    j = 0;
+    while (j + 1 < a.n_proj && u >= a.p[j + 1].unit_base) j++;
+    const uint32_t local = (uint32_t)(u - a.p[j].unit_base);   // < 2^31 units per projection
+    rt = (int)(local / (uint32_t)a.p[j].chunks);
+    c = (int)(local % (uint32_t)a.p[j].chunks);
+}
+
 template <int WT>
-__global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_constant__ SkArgs a) {
+__global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_constant__ SkArgs a) {
     using L = Layout<WT>;
+    using S = SkLayout<WT>;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *ring = smem;
-    float *red = reinterpret_cast<float *>(smem + L::SLOTS * L::UNIT);
-    float *keep = red + CW * HALF_VALS;   // [2][VALS]
-    uint64_t *full = reinterpret_cast<uint64_t *>(keep + 2 * VALS);
+    float *red = reinterpret_cast<float *>(smem + S::RED);
+    float *keep = reinterpret_cast<float *>(smem + S::KEEP);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::BARS);
     uint64_t *empty = full + L::SLOTS;
     __shared__ int s_last[2];
     __shared__ SharedTile s_tile[2];
@@ -331,33 +467,27 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
     pdl_trigger();
     const int G = gridDim.x, cta = blockIdx.x;
     const int64_t u0 = cta_start(cta, a.U, G), u1 = cta_start(cta + 1, a.U, G);
+    const int n_units = (int)(u1 - u0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ring = smem_addr(smem);
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::SLOTS; s++) {
-            mbar_init(smem_addr(full + s), 1);
-            mbar_init(smem_addr(empty + s), 4);
+            mbar_init(smem_addr(full + s), 1);                 // the producer, with the unit's bytes
+            mbar_init(smem_addr(empty + s), 4 * 32);          // the four warps of one unit phase
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    auto decode = [&](int64_t u, int &j, int &rt, int &c) {
-        j = 0;
-        while (j + 1 < a.n_proj && u >= a.p[j + 1].unit_base) j++;
-        const int64_t local = u - a.p[j].unit_base;
-        rt = (int)(local / a.p[j].chunks);
-        c = (int)(local % a.p[j].chunks);
-    };
-
-    if (warp == CW) {   // ---------------- producer
-        if (lane == 0 && u0 < u1) {
+    if (warp == SK_PRODUCER) {   // ---------------- producer: weights only, no wait on the previous kernel
+        if (lane == 0 && n_units > 0) {
             const uint64_t pol = evict_first_policy();
             int j, rt, c;
-            decode(u0, j, rt, c);
+            decode_unit(a, u0, j, rt, c);
             // units of one projection are contiguous in its packed buffer
             const uint8_t *src = a.p[j].w + ((int64_t)rt * a.p[j].chunks + c) * L::UNIT;
             int64_t left_in_proj = a.p[j].unit_base + (int64_t)a.p[j].row_tiles * a.p[j].chunks - u0;
-            for (int i = 0; u0 + i < u1; i++) {
+            for (int i = 0; i < n_units; i++) {
                 const int slot = i % L::SLOTS;
                 const uint32_t n = (uint32_t)i / L::SLOTS;
                 if (n > 0 && !mbar_wait(smem_addr(empty + slot), (n - 1) & 1u)) break;
@@ -367,7 +497,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
                     left_in_proj = (int64_t)a.p[j].row_tiles * a.p[j].chunks;
                 }
                 mbar_expect_tx(smem_addr(full + slot), L::UNIT);
-                bulk_g2s(smem_addr(ring + (size_t)slot * L::UNIT), src, L::UNIT, smem_addr(full + slot), pol);
+                bulk_g2s(ring + (uint32_t)slot * S::SLOT, src, L::UNIT, smem_addr(full + slot), pol);
                 src += L::UNIT;
                 left_in_proj--;
             }
@@ -375,17 +505,13 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
         return;
     }
 
-    // ---------------- consumers
-    // The producer above streams weights without waiting for the previous
-    // kernel (no library kernel that may run just before writes packed
-    // weights); the consumers wait before reading the image, the live count or
-    // the workspace, or writing outputs.
+    // Everything below reads what the previous kernel wrote (image, live count,
+    // workspace) or writes outputs, so it waits for that kernel first.
     pdl_wait();
-    const int g = lane >> 2, t4 = lane & 3, tid = threadIdx.x;
     const int tl = live_rows(a.live, a.T);
-    const uint8_t *imgB = g < tl ? a.img + (int64_t)g * a.img_row_bytes : nullptr;
-    const uint8_t *imgS0 = 2 * t4 < tl ? a.img + (int64_t)(2 * t4) * a.img_row_bytes : nullptr;
-    const uint8_t *imgS1 = 2 * t4 + 1 < tl ? a.img + (int64_t)(2 * t4 + 1) * a.img_row_bytes : nullptr;
+
+    // ---------------- consumers
+    const int tid = threadIdx.x, p = warp & 3;
     bool ok = true;
 
     // Row tiles this CTA shares (at most its first, slot 0, and its last, slot
@@ -393,9 +519,9 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
     if (tid < 2) {
         SharedTile st = {};
         st.R = -1;
-        if (u0 < u1) {
+        if (n_units > 0) {
             int jj, rr, cc;
-            decode(tid == 0 ? u0 : u1 - 1, jj, rr, cc);
+            decode_unit(a, tid == 0 ? u0 : u1 - 1, jj, rr, cc);
             const SkProj &P = a.p[jj];
             const int64_t rs = P.unit_base + (int64_t)rr * P.chunks, re = rs + P.chunks;
             const bool first_tile_too = tid == 1 && rs <= u0;   // last tile == first tile
@@ -413,71 +539,102 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
         s_tile[tid] = st;
     }
 
-    int j = 0, rt = 0, c0 = 0;
-    if (u0 < u1) decode(u0, j, rt, c0);
-    for (int64_t u = u0; u < u1;) {
-        const SkProj &P = a.p[j];
-        const int64_t rt_start = P.unit_base + (int64_t)rt * P.chunks, rt_end = rt_start + P.chunks;
-        const int64_t s1 = u1 < rt_end ? u1 : rt_end;
-        const int nblk = (int)(4 * (s1 - u));
-        const int Kb = P.K / QB;
-        float acc[UNIT_GROUPS][4];
-#pragma unroll
-        for (int r = 0; r < UNIT_GROUPS; r++)
-#pragma unroll
-            for (int i = 0; i < 4; i++) acc[r][i] = 0.0f;
+    int j = 0, rt = 0, c = 0;
+    if (n_units > 0) decode_unit(a, u0, j, rt, c);
+    const int q = warp >> 2, g = lane >> 2, t4 = lane & 3;
+    const uint32_t recs_q = ring + S::RECS + (uint32_t)q * 2 * 4 * BREC;
 
-        auto blk_of = [&](int jj) { return 4 * (c0 + (jj >> 2)) + (jj & 3); };
-        Raw next = {0u, 0u, 0u, 0u};
-        if (warp < nblk && blk_of(warp) < Kb) next = load_raw(imgB, imgS0, imgS1, blk_of(warp), t4);
-        for (int jj = warp; jj < nblk; jj += CW) {
-            const Raw cur = next;
-            const int jn = jj + CW;
-            if (jn < nblk && blk_of(jn) < Kb) next = load_raw(imgB, imgS0, imgS1, blk_of(jn), t4);
-            const int i = (int)(u - u0) + (jj >> 2);
-            const int slot = i % L::SLOTS;
-            if (ok) ok = mbar_wait(smem_addr(full + slot), ((uint32_t)i / L::SLOTS) & 1u);
-            const int jb = jj & 3;
-            if (ok && blk_of(jj) < Kb) {
-                BSide s;
-                bside<WT>(cur, s);
-                const uint32_t ub = smem_addr(ring + (size_t)slot * L::UNIT);
-                block_rows<WT, true>(nullptr, ub + jb * L::BLOCK, nullptr, ub + L::SCALES + jb * 256, lane, s, acc);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(empty + slot));
-        }
-
-        // CTA reduction over the consumer warps in fixed order, in two passes
-        // of 4 row groups (value v of pass h is accumulator index h*512 + v)
-        const bool whole = u == rt_start && s1 == rt_end;
-        const int part_slot = u0 >= rt_start ? 0 : 1;
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-#pragma unroll
-            for (int r = 0; r < UNIT_GROUPS / 2; r++)
-#pragma unroll
-                for (int i = 0; i < 4; i++) red[warp * HALF_VALS + (r * 4 + i) * 32 + lane] = acc[h * 4 + r][i];
-            consumer_sync();
-            for (int t = tid; t < HALF_VALS; t += CW * 32) {
-                float sum = 0.0f;
-#pragma unroll
-                for (int w = 0; w < CW; w++) sum += red[w * HALF_VALS + t];
-                const int tv = h * HALF_VALS + t;
-                if (whole) {
-                    int row, slot;
-                    val_pos(tv, row, slot);
-                    row += rt * UNIT_ROWS;
-                    if (row < P.N && slot < tl) P.y[(int64_t)slot * P.y_stride + row] = sum;
-                } else {
-                    keep[part_slot * VALS + tv] = sum;
+    // Image words of block p of this phase's units, IMG_AHEAD units ahead. The
+    // load cursor walks the phase's units (every fourth) with the current
+    // projection's sizes in registers.
+    const uint8_t *imgB = g < tl ? a.img + (int64_t)g * a.img_row_bytes : nullptr;
+    const uint8_t *imgS0 = 2 * t4 < tl ? a.img + (int64_t)(2 * t4) * a.img_row_bytes : nullptr;
+    const uint8_t *imgS1 = 2 * t4 + 1 < tl ? a.img + (int64_t)(2 * t4 + 1) * a.img_row_bytes : nullptr;
+    int lj = j, lrt = rt, lc = c, li = q;   // cursor at this phase's first unit
+    int l_kb = 0, l_chunks = 1, l_rtiles = 1;
+    if (n_units > 0) {
+        l_kb = a.p[lj].K / QB;
+        l_chunks = a.p[lj].chunks;
+        l_rtiles = a.p[lj].row_tiles;
+    }
+    auto cursor_step = [&](int n) {   // advance the cursor by n units
+        lc += n;
+        while (lc >= l_chunks) {
+            lc -= l_chunks;
+            if (++lrt == l_rtiles) {
+                lrt = 0;
+                if (++lj < a.n_proj) {
+                    l_kb = a.p[lj].K / QB;
+                    l_chunks = a.p[lj].chunks;
+                    l_rtiles = a.p[lj].row_tiles;
                 }
             }
-            consumer_sync();   // red is rewritten by the next pass / row tile
         }
-        u = s1;
-        // next segment starts at chunk 0 of the next row tile (or projection)
-        c0 = 0;
+    };
+    cursor_step(q);
+    auto load_next = [&]() -> Raw {   // image words of block p of unit li; then li += 4
+        Raw r = {0u, 0u, 0u, 0u};
+        if (li < n_units) {
+            const int b = 4 * lc + p;
+            if (b < l_kb) r = load_raw(imgB, imgS0, imgS1, b, t4);
+            cursor_step(4);
+        }
+        li += 4;
+        return r;
+    };
+    Raw img_r[IMG_AHEAD];
+#pragma unroll
+    for (int k = 0; k < IMG_AHEAD; k++) img_r[k] = load_next();
+    int kq = 0;   // this phase's unit count so far (picks the record buffer)
+
+    bool first_seg = true;       // the CTA's first segment keeps its part in slot 0, a later one in slot 1
+    for (int i_seg = 0; i_seg < n_units;) {   // segment = this CTA's units of one row tile
+        const SkProj &P = a.p[j];
+        const int seg_len = P.chunks - c < n_units - i_seg ? P.chunks - c : n_units - i_seg;
+        const bool whole = c == 0 && seg_len == P.chunks;
+        float acc[2][4];
+#pragma unroll
+        for (int r = 0; r < 2; r++)
+#pragma unroll
+            for (int k = 0; k < 4; k++) acc[r][k] = 0.0f;
+        for (int i = i_seg + ((q - i_seg) & 3); i < i_seg + seg_len; i += 4, kq++) {
+            // activation record of block p of this unit, from the image words loaded earlier
+            const Raw cur = img_r[0];
+#pragma unroll
+            for (int k = 0; k + 1 < IMG_AHEAD; k++) img_r[k] = img_r[k + 1];
+            img_r[IMG_AHEAD - 1] = load_next();
+            const uint32_t recs = recs_q + (uint32_t)(kq & 1) * 4 * BREC;
+            write_record<WT>(recs + p * BREC, cur, lane);
+            phase_sync(q);   // the phase's four records are written (double buffer: see below)
+            const int slot = i % L::SLOTS;
+            if (ok) ok = mbar_wait(smem_addr(full + slot), ((uint32_t)i / L::SLOTS) & 1u);
+            if (ok) unit_rows<WT>(ring + (uint32_t)slot * S::SLOT, recs, p, lane, acc);
+            mbar_arrive(smem_addr(empty + slot));   // after this thread's shared loads
+        }
+        // add the four unit phases' parts in fixed order
+#pragma unroll
+        for (int r = 0; r < 2; r++)
+#pragma unroll
+            for (int k = 0; k < 4; k++) red[warp * 256 + (r * 4 + k) * 32 + lane] = acc[r][k];
+        all_consumers_sync();
+        const int part_slot = first_seg ? 0 : 1;
+        for (int tv = tid; tv < VALS; tv += SK_CONS * 32) {
+            const int pp = tv >> 8, w_in = tv & 255;
+            const float sum = ((red[pp * 256 + w_in] + red[(pp + 4) * 256 + w_in]) + red[(pp + 8) * 256 + w_in]) +
+                              red[(pp + 12) * 256 + w_in];
+            if (whole) {
+                int row, tok;
+                val_pos(tv, row, tok);
+                row += rt * UNIT_ROWS;
+                if (row < P.N && tok < tl) P.y[(int64_t)tok * P.y_stride + row] = sum;
+            } else {
+                keep[part_slot * VALS + tv] = sum;
+            }
+        }
+        all_consumers_sync();   // red is rewritten by the next segment
+        first_seg = false;
+        i_seg += seg_len;
+        c = 0;                  // the next segment starts a row tile
         if (++rt == P.row_tiles) {
             rt = 0;
             j++;
@@ -492,9 +649,9 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
     for (int ps = 0; ps < 2; ps++) {
         if ((ps ? t1.R : t0.R) < 0) continue;
         float *mine = a.ws_part + ((int64_t)cta * 2 + ps) * VALS;
-        for (int t = tid; t < VALS; t += CW * 32) mine[t] = keep[ps * VALS + t];
+        for (int t = tid; t < VALS; t += SK_CONS * 32) mine[t] = keep[ps * VALS + t];
     }
-    consumer_sync();
+    all_consumers_sync();
     if (tid < 2) {
         const SharedTile &st = tid ? t1 : t0;
         int last = 0;
@@ -504,11 +661,11 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
         }
         s_last[tid] = last;
     }
-    consumer_sync();
+    all_consumers_sync();
     for (int ps = 0; ps < 2; ps++) {
         if (!s_last[ps]) continue;
         const SharedTile &st = ps ? t1 : t0;
-        constexpr int PER = (VALS + CW * 32 - 1) / (CW * 32);
+        constexpr int PER = VALS / (SK_CONS * 32);
         float sums[PER];
 #pragma unroll
         for (int k = 0; k < PER; k++) sums[k] = 0.0f;
@@ -522,26 +679,22 @@ __global__ void __launch_bounds__(THREADS, 1) mmvq_sk_kernel(const __grid_consta
             }
 #pragma unroll
             for (int k = 0; k < PER; k++) {
-                const int t = tid + k * CW * 32;
-                if (t < VALS) {
-                    float part[MAXP];
+                const int t = tid + k * SK_CONS * 32;
+                float part[MAXP];
 #pragma unroll
-                    for (int q = 0; q < MAXP; q++) part[q] = __ldcg(src[q] + t);
+                for (int q = 0; q < MAXP; q++) part[q] = __ldcg(src[q] + t);
 #pragma unroll
-                    for (int q = 0; q < MAXP; q++)
-                        if (cb + q <= st.c_last) sums[k] += part[q];
-                }
+                for (int q = 0; q < MAXP; q++)
+                    if (cb + q <= st.c_last) sums[k] += part[q];
             }
         }
 #pragma unroll
         for (int k = 0; k < PER; k++) {
-            const int t = tid + k * CW * 32;
-            if (t < VALS) {
-                int row, slot;
-                val_pos(t, row, slot);
-                row += st.rt * UNIT_ROWS;
-                if (row < st.N && slot < tl) st.y[(int64_t)slot * st.y_stride + row] = sums[k];
-            }
+            const int t = tid + k * SK_CONS * 32;
+            int row, tok;
+            val_pos(t, row, tok);
+            row += st.rt * UNIT_ROWS;
+            if (row < st.N && tok < tl) st.y[(int64_t)tok * st.y_stride + row] = sums[k];
         }
         if (tid == 0) a.ws_cnt[st.R] = 0u;
     }
@@ -696,8 +849,7 @@ int sm_count() {
 template <int WT>
 size_t sk_smem() {
     using L = Layout<WT>;
-    return (size_t)L::SLOTS * L::UNIT + ((size_t)CW * HALF_VALS + 2 * VALS) * sizeof(float) +
-           2 * L::SLOTS * sizeof(uint64_t);
+    return (size_t)SkLayout<WT>::BYTES;
 }
 
 }  // namespace
@@ -746,7 +898,7 @@ static qk_status launch_sk(const SkArgs &a, int G, cudaStream_t s) {
         if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq: shared memory attribute: %s", cudaGetErrorString(e));
         configured = true;
     }
-    return launch_pdl("mmvq", mmvq_sk_kernel<WT>, dim3(G), dim3(THREADS), smem, s, a);
+    return launch_pdl("mmvq", mmvq_sk_kernel<WT>, dim3(G), dim3(SK_THREADS), smem, s, a);
 }
 
 qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj, const qk_proj *projs,
