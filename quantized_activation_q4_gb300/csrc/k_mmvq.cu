@@ -49,6 +49,9 @@ constexpr int MAXP = 8;                      // partial sums loaded per batch
 // and gives up after SPIN_LIMIT tries (at most about a second).
 constexpr uint32_t SUSPEND_NS = 20000;
 constexpr uint32_t SPIN_LIMIT = 1u << 16;
+// An owner waits at most this many short sleeps for the other parts of its
+// tile before taking the general path (a matter of speed, not correctness).
+constexpr int OWNER_SPIN = 2000;
 
 template <int WT> struct Layout;
 template <> struct Layout<QK_W_Q4_0> {
@@ -139,6 +142,12 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
     unsigned old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // A row tile this CTA shares with others (stream-K): where its parts live.
@@ -335,7 +344,11 @@ __device__ __forceinline__ void block_rows(const uint8_t *gblk, uint32_t sblk, c
 // their operands from it (each thread arrives after its own loads). At the end
 // of a segment (the CTA's units of one row tile) the four phases' partial sums
 // are added in fixed order.
-constexpr int SK_CONS = 16;
+#ifndef QK_MMVQ_PHASES
+#define QK_MMVQ_PHASES 4
+#endif
+constexpr int NPH = QK_MMVQ_PHASES;   // units in work at once (unit phases)
+constexpr int SK_CONS = 4 * NPH;
 constexpr int SK_PRODUCER = SK_CONS;
 constexpr int SK_THREADS = (SK_CONS + 1) * 32;
 constexpr int BREC = 640;       // [0,512) fragments (16 B per lane), [512,576) C quads, [576,640) scales (per t4)
@@ -346,7 +359,7 @@ struct SkLayout {
     static constexpr int UNIT = Layout<WT>::UNIT, SLOTS = Layout<WT>::SLOTS;
     static constexpr int SLOT = UNIT;
     static constexpr int RECS = SLOTS * SLOT;                     // [4 phases][2][4 blocks][BREC]
-    static constexpr int RED = RECS + 4 * 2 * 4 * BREC;           // [SK_CONS][256] floats
+    static constexpr int RED = RECS + NPH * 2 * 4 * BREC;         // [SK_CONS][256] floats
     static constexpr int KEEP = RED + SK_CONS * 256 * 4;          // [2][VALS] floats
     static constexpr int BARS = KEEP + 2 * VALS * 4;              // full[SLOTS], empty[SLOTS]
     static constexpr int BYTES = BARS + 2 * SLOTS * 8;
@@ -539,6 +552,67 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
         s_tile[tid] = st;
     }
 
+    all_consumers_sync();   // s_tile is planned
+    int signalled = 0;          // thread 0: slot + 1 of a part signalled in the loop
+    unsigned signal_old = 0;
+
+    // Sum of the parts of shared tile st in CTA order (c_first first) and the
+    // store of the tile's outputs; the owner's own part comes from keep.
+    auto add_parts = [&](const SharedTile &st, int ls, bool own_from_keep) {
+        constexpr int PER = (VALS + SK_CONS * 32 - 1) / (SK_CONS * 32);
+        float sums[PER];
+#pragma unroll
+        for (int k = 0; k < PER; k++) {
+            const int t = tid + k * SK_CONS * 32;
+            sums[k] = own_from_keep && t < VALS ? keep[ls * VALS + t] : 0.0f;
+        }
+        const int cfirst = own_from_keep ? st.c_first + 1 : st.c_first;
+        for (int cb = cfirst; cb <= st.c_last; cb += MAXP) {   // MAXP parts in flight at once
+            const float *src[MAXP];
+#pragma unroll
+            for (int qq = 0; qq < MAXP; qq++) {
+                const int cc = cb + qq <= st.c_last ? cb + qq : st.c_last;
+                const int pslot = cc == st.c_first ? st.first_slot : 0;
+                src[qq] = a.ws_part + ((int64_t)cc * 2 + pslot) * VALS;
+            }
+#pragma unroll
+            for (int k = 0; k < PER; k++) {
+                const int t = tid + k * SK_CONS * 32;
+                if (t >= VALS) break;
+                float part[MAXP];
+#pragma unroll
+                for (int qq = 0; qq < MAXP; qq++) part[qq] = __ldcg(src[qq] + t);
+#pragma unroll
+                for (int qq = 0; qq < MAXP; qq++)
+                    if (cb + qq <= st.c_last) sums[k] += part[qq];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PER; k++) {
+            const int t = tid + k * SK_CONS * 32;
+            if (t >= VALS) break;
+            int row, tok;
+            val_pos(t, row, tok);
+            row += st.rt * UNIT_ROWS;
+            if (row < st.N && tok < tl) st.y[(int64_t)tok * st.y_stride + row] = sums[k];
+        }
+    };
+    // Once this CTA's part of st is in the workspace: signal it; the
+    // contributor that signals last adds all the parts. Thread 0's
+    // acquire-release atomic after the barrier covers the CTA's stores.
+    auto settle_part = [&](const SharedTile &st) {
+        if (tid == 0) {
+            const unsigned old = atom_add_acq_rel(a.ws_cnt + st.R, 1u);
+            s_last[1] = old == (unsigned)(st.c_last - st.c_first);
+        }
+        all_consumers_sync();
+        if (s_last[1]) {
+            add_parts(st, 0, false);
+            if (tid == 0) a.ws_cnt[st.R] = 0u;
+        }
+        all_consumers_sync();   // s_last is reused
+    };
+
     int j = 0, rt = 0, c = 0;
     if (n_units > 0) decode_unit(a, u0, j, rt, c);
     const int q = warp >> 2, g = lane >> 2, t4 = lane & 3;
@@ -572,14 +646,14 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
         }
     };
     cursor_step(q);
-    auto load_next = [&]() -> Raw {   // image words of block p of unit li; then li += 4
+    auto load_next = [&]() -> Raw {   // image words of block p of unit li; then li += NPH
         Raw r = {0u, 0u, 0u, 0u};
         if (li < n_units) {
             const int b = 4 * lc + p;
             if (b < l_kb) r = load_raw(imgB, imgS0, imgS1, b, t4);
-            cursor_step(4);
+            cursor_step(NPH);
         }
-        li += 4;
+        li += NPH;
         return r;
     };
     Raw img_r[IMG_AHEAD];
@@ -597,7 +671,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
         for (int r = 0; r < 2; r++)
 #pragma unroll
             for (int k = 0; k < 4; k++) acc[r][k] = 0.0f;
-        for (int i = i_seg + ((q - i_seg) & 3); i < i_seg + seg_len; i += 4, kq++) {
+        for (int i = i_seg + ((q - i_seg) % NPH + NPH) % NPH; i < i_seg + seg_len; i += NPH, kq++) {
             // activation record of block p of this unit, from the image words loaded earlier
             const Raw cur = img_r[0];
 #pragma unroll
@@ -620,18 +694,27 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
         const int part_slot = first_seg ? 0 : 1;
         for (int tv = tid; tv < VALS; tv += SK_CONS * 32) {
             const int pp = tv >> 8, w_in = tv & 255;
-            const float sum = ((red[pp * 256 + w_in] + red[(pp + 4) * 256 + w_in]) + red[(pp + 8) * 256 + w_in]) +
-                              red[(pp + 12) * 256 + w_in];
+            float sum = red[pp * 256 + w_in];
+#pragma unroll
+            for (int qq = 1; qq < NPH; qq++) sum += red[(pp + 4 * qq) * 256 + w_in];
             if (whole) {
                 int row, tok;
                 val_pos(tv, row, tok);
                 row += rt * UNIT_ROWS;
                 if (row < P.N && tok < tl) P.y[(int64_t)tok * P.y_stride + row] = sum;
+            } else if (cta == s_tile[part_slot].c_first) {
+                keep[part_slot * VALS + tv] = sum;   // owner: kept for the end
             } else {
-                keep[part_slot * VALS + tv] = sum;
+                __stcg(a.ws_part + ((int64_t)cta * 2 + part_slot) * VALS + tv, sum);
             }
         }
         all_consumers_sync();   // red is rewritten by the next segment
+        if (!whole && cta != s_tile[part_slot].c_first && tid == 0) {
+            // signal the part; the result is only looked at after the loop,
+            // so the atomic's latency is not waited for here
+            signalled = part_slot + 1;
+            signal_old = atom_add_acq_rel(a.ws_cnt + s_tile[part_slot].R, 1u);
+        }
         first_seg = false;
         i_seg += seg_len;
         c = 0;                  // the next segment starts a row tile
@@ -641,62 +724,54 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
         }
     }
 
-    // Publish this CTA's parts of shared row tiles; the last contributor of a
-    // tile adds every part in CTA order and writes the output. Thread 0/1's
-    // acquire-release atomic after the barrier covers the whole CTA's stores.
-    const SharedTile t0 = s_tile[0], t1 = s_tile[1];
-    if (t0.R < 0 && t1.R < 0) return;
-    for (int ps = 0; ps < 2; ps++) {
-        if ((ps ? t1.R : t0.R) < 0) continue;
-        float *mine = a.ws_part + ((int64_t)cta * 2 + ps) * VALS;
-        for (int t = tid; t < VALS; t += SK_CONS * 32) mine[t] = keep[ps * VALS + t];
+    // A signalled part whose atomic found all the others already there: this
+    // CTA adds the parts (only when the tile's owner took the general path).
+    if (tid == 0) {
+        s_last[1] = 0;
+        if (signalled) {
+            const SharedTile &st = s_tile[signalled - 1];
+            s_last[1] = signal_old == (unsigned)(st.c_last - st.c_first) ? signalled : 0;
+        }
     }
     all_consumers_sync();
-    if (tid < 2) {
-        const SharedTile &st = tid ? t1 : t0;
-        int last = 0;
-        if (st.R >= 0) {
-            const unsigned old = atom_add_acq_rel(a.ws_cnt + st.R, 1u);
-            last = old == (unsigned)(st.c_last - st.c_first);
-        }
-        s_last[tid] = last;
-    }
-    all_consumers_sync();
-    for (int ps = 0; ps < 2; ps++) {
-        if (!s_last[ps]) continue;
-        const SharedTile &st = ps ? t1 : t0;
-        constexpr int PER = VALS / (SK_CONS * 32);
-        float sums[PER];
-#pragma unroll
-        for (int k = 0; k < PER; k++) sums[k] = 0.0f;
-        for (int cb = st.c_first; cb <= st.c_last; cb += MAXP) {   // MAXP parts in flight at once
-            const float *src[MAXP];
-#pragma unroll
-            for (int q = 0; q < MAXP; q++) {
-                const int cc = cb + q <= st.c_last ? cb + q : st.c_last;
-                const int pslot = cc == st.c_first ? st.first_slot : 0;
-                src[q] = a.ws_part + ((int64_t)cc * 2 + pslot) * VALS;
-            }
-#pragma unroll
-            for (int k = 0; k < PER; k++) {
-                const int t = tid + k * SK_CONS * 32;
-                float part[MAXP];
-#pragma unroll
-                for (int q = 0; q < MAXP; q++) part[q] = __ldcg(src[q] + t);
-#pragma unroll
-                for (int q = 0; q < MAXP; q++)
-                    if (cb + q <= st.c_last) sums[k] += part[q];
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < PER; k++) {
-            const int t = tid + k * SK_CONS * 32;
-            int row, tok;
-            val_pos(t, row, tok);
-            row += st.rt * UNIT_ROWS;
-            if (row < st.N && tok < tl) st.y[(int64_t)tok * st.y_stride + row] = sums[k];
-        }
+    if (s_last[1]) {
+        const SharedTile &st = s_tile[s_last[1] - 1];
+        add_parts(st, 0, false);
         if (tid == 0) a.ws_cnt[st.R] = 0u;
+    }
+
+    // The owner of a shared row tile (the CTA holding its first unit; the
+    // tile is its last segment) adds the other contributors' parts as soon
+    // as all of them have signalled, without publishing its own. If they are
+    // late it takes the general path: it publishes too, and whichever
+    // contributor signals last adds all the parts.
+    if (n_units > 0) {
+        const int ls = s_tile[1].R >= 0 ? 1 : 0;   // slot of the last segment's tile
+        const SharedTile &st = s_tile[ls];
+        if (st.R >= 0 && cta == st.c_first) {
+            if (tid == 0) {
+                const unsigned want = (unsigned)(st.c_last - st.c_first);
+                int fast = 0;
+                for (int it = 0; it < OWNER_SPIN; it++) {
+                    if (ld_acquire(a.ws_cnt + st.R) == want) {
+                        fast = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                s_last[0] = fast;
+            }
+            all_consumers_sync();
+            if (s_last[0]) {
+                add_parts(st, ls, true);
+                if (tid == 0) a.ws_cnt[st.R] = 0u;
+            } else {
+                float *mine = a.ws_part + ((int64_t)cta * 2 + ls) * VALS;
+                for (int t = tid; t < VALS; t += SK_CONS * 32) __stcg(mine + t, keep[ls * VALS + t]);
+                all_consumers_sync();
+                settle_part(st);
+            }
+        }
     }
 }
 
