@@ -33,6 +33,7 @@
 // reset after use) adds the parts in CTA order. All sums run in a fixed order, so results do not depend on
 // timing or on the live-row count.
 
+#include <cstdlib>
 #include <mutex>
 
 #include "qk_internal.cuh"
@@ -50,7 +51,9 @@ constexpr int MAXP = 8;                      // partial sums loaded per batch
 constexpr uint32_t SUSPEND_NS = 20000;
 constexpr uint32_t SPIN_LIMIT = 1u << 16;
 // An owner waits at most this many short sleeps for the other parts of its
-// tile before taking the general path (a matter of speed, not correctness).
+// tile before taking the general path (a matter of speed, not correctness);
+// the environment variable QK_MMVQ_OWNER_SPIN overrides it (0 forces the
+// general path, which the tests use).
 constexpr int OWNER_SPIN = 2000;
 
 template <int WT> struct Layout;
@@ -78,6 +81,7 @@ struct SkArgs {
     int64_t U;           // total units
     float *ws_part;      // [G][2][VALS]
     unsigned int *ws_cnt;
+    int owner_spin;      // short sleeps an owner waits for the other parts (0: general path at once)
     SkProj p[MAX_PROJ];
 };
 
@@ -752,7 +756,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
             if (tid == 0) {
                 const unsigned want = (unsigned)(st.c_last - st.c_first);
                 int fast = 0;
-                for (int it = 0; it < OWNER_SPIN; it++) {
+                for (int it = 0; it < a.owner_spin; it++) {
                     if (ld_acquire(a.ws_cnt + st.R) == want) {
                         fast = 1;
                         break;
@@ -1001,6 +1005,11 @@ qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj,
         R += d.row_tiles;
     }
     a.U = U;
+    static const int owner_spin = [] {
+        const char *e = getenv("QK_MMVQ_OWNER_SPIN");
+        return e ? atoi(e) : OWNER_SPIN;
+    }();
+    a.owner_spin = owner_spin;
     const int G = (int)(U < sm_count() ? U : sm_count());
     const int64_t need = mmvq_workspace_bytes(n_proj, projs);
     if (!ws || ws_bytes < (size_t)need)

@@ -183,3 +183,48 @@ def test_fresh_and_reused_workspace_agree():
         qk.qk_mmvq(img, 112, T, projs, fresh, n)
     assert np.array_equal(host(y).view(np.uint32), first.view(np.uint32))
     assert qk.qk_device_faults() == 0
+
+
+_OWNER_SCRIPT = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+from quantized_activation_q4_gb300 import binding as qk, synth
+T, N, K = 8, 4096, 8192
+dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+img = torch.empty((T * (K // 32) * 36,), dtype=torch.uint8, device="cuda")
+qk.qk_quantize_q8_1(dev(synth.activations(90, T, K)), T, K, K, img, K // 32)
+nb = qk.qk_weight_packed_bytes("q4_0", N, K)
+w = torch.empty((nb,), dtype=torch.uint8, device="cuda")
+qk.qk_weight_pack("q4_0", dev(synth.q4_0_weight(91, N, K).reshape(-1)), N, K, w, nb)
+y = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
+projs = [qk.make_proj("q4_0", w, N, K, y, N)]
+n = qk.qk_mmvq_workspace_bytes(projs)
+ws = torch.zeros((n,), dtype=torch.uint8, device="cuda")
+for _ in range(3):
+    qk.qk_mmvq(img, K // 32, T, projs, ws, n)
+torch.cuda.synchronize()
+assert qk.qk_device_faults() == 0
+np.save(sys.argv[2], y.cpu().numpy())
+"""
+
+
+def test_split_tile_general_path_same_bits(tmp_path):
+    """Row tiles split between CTAs are finished by their owner as soon as the other parts
+    are in; with QK_MMVQ_OWNER_SPIN=0 every owner takes the general path (publish, and the
+    last to signal adds). Both paths add the parts in the same order: identical bits."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = {}
+    for spin in ("2000", "0"):
+        env = dict(os.environ, QK_MMVQ_OWNER_SPIN=spin)
+        path = str(tmp_path / f"y_{spin}.npy")
+        subprocess.run([sys.executable, "-c", _OWNER_SCRIPT, root, path], env=env, check=True, timeout=600)
+        outs[spin] = np.load(path)
+    assert not np.isnan(outs["0"]).any()
+    assert np.array_equal(outs["2000"].view(np.uint32), outs["0"].view(np.uint32))
+    x = synth.activations(90, 8, 8192)
+    W = synth.q4_0_weight(91, 4096, 8192)
+    rows = np.arange(0, 4096, 97)
+    assert O.nmse(outs["0"][:, rows], O.proj_plain("q4_0", W[rows], len(rows), 8192, x)) <= NMSE_GATE
