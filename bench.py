@@ -315,6 +315,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     achieved = MMVQ_BIG_BYTES / (us_m * 1e-6) / 1e9
     value = world * W_STEP / (ms_per_step * 1e-3) / 1e9
     clocks = clk.summary()
+    others = None if args.no_other_configs else other_configs(qk, synth, torch, dev, hbm, l2)
     if rank != 0:
         return None
     comp = {
@@ -345,6 +346,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                    "graphs": "one CUDA graph per step (4 kernels, programmatic dependent launch between them)",
                    "parallelism": "replicas only" if world > 1 else "single GPU"},
         "components": comp,
+        "other_configs": others,
         "roofline": {"kernel": "mmvq (Q4_0, K=N=8192, T=8)", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy burst)",
@@ -356,6 +358,188 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         "gpu_launches": launches,
         "clocks": clocks,
     }
+
+
+# ------------------------------------------------------------------ other configurations
+def _graph_us(torch, stream, fns, replays):
+    """Capture fns (one call per rotation replica) back to back in one graph and
+    return microseconds per replica over `replays` replays (after one warm-up)."""
+    with torch.cuda.stream(stream):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for f in fns:
+            f()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (replays * len(fns))
+
+
+def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
+    """Per-component microseconds for the other workloads of the metric (cold L2:
+    weights rotate over replicas totalling > 3x L2), each component a CUDA graph.
+    Also the unfused control of config 1 (RMS, then the standalone quantiser, then
+    MMVQ), timed the same way."""
+    stream = torch.cuda.Stream()
+    out = {}
+    gb = lambda nbytes, us: round(nbytes / (us * 1e-6) / 1e9, 1)
+
+    def packed(seed, N, K):
+        nbytes = qk.qk_weight_packed_bytes("q4_0", N, K)
+        buf = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
+        qk.qk_weight_pack("q4_0", dev(synth.q4_0_weight(seed, N, K).reshape(-1)), N, K, buf, nbytes)
+        return buf
+
+    # ---- config 1 control: RMS writing F32 only, then quantize, then MMVQ (q/k/v)
+    x = dev(synth.activations(100, T, D_ATTN))
+    w = dev(synth.norm_weight(101, D_ATTN))
+    y = torch.empty((T, D_ATTN), dtype=torch.float32, device="cuda")
+    img = torch.empty((IMG_ATTN,), dtype=torch.uint8, device="cuda")
+    scratch = torch.empty((IMG_ATTN,), dtype=torch.uint8, device="cuda")
+    R1 = max(2, -(-3 * l2 // W_QKV))
+    qkv_w = [[packed(600 + 10 * r + i, N, D_ATTN) for i, (_, N) in enumerate(QKV)] for r in range(R1)]
+    qkv_y = [torch.empty((T, N), dtype=torch.float32, device="cuda") for _, N in QKV]
+    pr = lambda r: [qk.make_proj("q4_0", qkv_w[r][i], N, D_ATTN, qkv_y[i], N) for i, (_, N) in enumerate(QKV)]
+    ws1_n = qk.qk_mmvq_workspace_bytes(pr(0))
+    ws1 = torch.zeros((ws1_n,), dtype=torch.uint8, device="cuda")
+
+    def fused(r):
+        qk.qk_rmsnorm_q8_1(x, T, D_ATTN, D_ATTN, "mul", w, None, 1.0, 1e-6, y, D_ATTN, img, D_ATTN // 32)
+        qk.qk_mmvq(img, D_ATTN // 32, T, pr(r), ws1, ws1_n)
+
+    def control(r):   # the producer's own image is ignored; a separate pass re-reads y
+        qk.qk_rmsnorm_q8_1(x, T, D_ATTN, D_ATTN, "mul", w, None, 1.0, 1e-6, y, D_ATTN, scratch, D_ATTN // 32)
+        qk.qk_quantize_q8_1(y, T, D_ATTN, D_ATTN, img, D_ATTN // 32)
+        qk.qk_mmvq(img, D_ATTN // 32, T, pr(r), ws1, ws1_n)
+
+    us_f = _graph_us(torch, stream, [lambda r=r: fused(r) for r in range(R1)], 10)
+    us_c = _graph_us(torch, stream, [lambda r=r: control(r) for r in range(R1)], 10)
+    out["c1_control"] = {"fused_us": round(us_f, 3), "unfused_us": round(us_c, 3),
+                         "kernels_fused": ["rmsnorm_q8_1", "mmvq(q,k,v)"],
+                         "kernels_unfused": ["rmsnorm_q8_1", "quantize_q8_1", "mmvq(q,k,v)"]}
+    del qkv_w
+
+    # ---- config 2: SwiGLU (packed [8, 37888]) -> image -> down 18944 -> 3584
+    NF, DM = 18944, 3584
+    a = dev(np.concatenate([synth.activations(110, T, NF), synth.activations(111, T, NF)], axis=1))
+    gout = torch.empty((T, NF), dtype=torch.float32, device="cuda")
+    gimg = torch.empty((T * (NF // 32) * 36,), dtype=torch.uint8, device="cuda")
+    W_DOWN = weight_bytes(DM, NF)
+    R2 = max(2, -(-3 * l2 // W_DOWN))
+    down_w = [packed(700 + r, DM, NF) for r in range(R2)]
+    down_y = torch.empty((T, DM), dtype=torch.float32, device="cuda")
+    pd = lambda r: [qk.make_proj("q4_0", down_w[r], DM, NF, down_y, DM)]
+    ws2_n = qk.qk_mmvq_workspace_bytes(pd(0))
+    ws2 = torch.zeros((ws2_n,), dtype=torch.uint8, device="cuda")
+    glu = lambda: qk.qk_glu_q8_1("swiglu", "packed", a, 2 * NF, None, 0, T, NF, gout, NF, gimg, NF // 32)
+    down = lambda r: qk.qk_mmvq(gimg, NF // 32, T, pd(r), ws2, ws2_n)
+    us_2 = _graph_us(torch, stream, [lambda r=r: (glu(), down(r)) for r in range(R2)], 10)
+    us_2d = _graph_us(torch, stream, [lambda r=r: down(r) for r in range(R2)], 10)
+    us_2g = _graph_us(torch, stream, [glu for _ in range(R2)], 10)
+    out["c2_glu_down"] = {"us": round(us_2, 3), "glu_us": round(us_2g, 3), "down_us": round(us_2d, 3),
+                          "weight_bytes": W_DOWN, "weight_gbs": gb(W_DOWN, us_2),
+                          "down_gbs": gb(W_DOWN, us_2d), "down_hbm_frac": round(W_DOWN / (us_2d * 1e-6) / 1e9 / hbm, 4),
+                          "replicas": R2}
+    del down_w
+
+    # ---- config 3: routed MoE, RMS -> image; top-8 of 128; plan; gate/up 2560 -> 768 per expert
+    E, KTOP, DR, NE = 128, 8, 2560, 768
+    per = qk.qk_weight_packed_bytes("q4_0", NE, DR)
+    R3 = 2
+    experts = []
+    for r in range(R3):
+        pair = []
+        for pj in range(2):
+            buf = torch.empty((E * per,), dtype=torch.uint8, device="cuda")
+            for e in range(E):
+                qk.qk_weight_pack("q4_0", dev(synth.q4_0_weight(5000 + 1000 * r + 500 * pj + e, NE, DR).reshape(-1)),
+                                  NE, DR, buf[e * per:(e + 1) * per], per)
+            pair.append(buf)
+        experts.append(pair)
+    c3 = {}
+    for bucket, live in ((16, 1), (16, 9), (128, 128)):
+        xr = dev(synth.activations(120 + live, bucket, DR))
+        wr = dev(synth.norm_weight(121, DR))
+        yr = torch.empty((bucket, DR), dtype=torch.float32, device="cuda")
+        rimg = torch.empty((bucket * (DR // 32) * 36,), dtype=torch.uint8, device="cuda")
+        logits = dev(synth.router_logits(122 + live, bucket, E))
+        ids = torch.empty((bucket, KTOP), dtype=torch.int32, device="cuda")
+        wts = torch.empty((bucket, KTOP), dtype=torch.float32, device="cuda")
+        counts = torch.empty((E,), dtype=torch.int32, device="cuda")
+        offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+        items = torch.empty((bucket * KTOP,), dtype=torch.int32, device="cuda")
+        lv = torch.tensor([live], dtype=torch.int32, device="cuda")
+        ys = [torch.empty((bucket * KTOP, NE), dtype=torch.float32, device="cuda") for _ in range(2)]
+
+        def routed(r):
+            qk.qk_rmsnorm_q8_1(xr, bucket, DR, DR, "mul", wr, None, 1.0, 1e-6, yr, DR, rimg, DR // 32, d_live_rows=lv)
+            qk.qk_topk_route(logits, bucket, E, KTOP, ids, wts, d_live_rows=lv)
+            qk.qk_moe_plan(ids, bucket, KTOP, E, counts, offsets, items, d_live_rows=lv)
+            qk.qk_mmvq_id(rimg, DR // 32, bucket, KTOP, [qk.make_proj_id("q4_0", E, experts[r][pj], NE, DR, ys[pj])
+                                                          for pj in range(2)], counts, offsets, items)
+
+        us_3 = _graph_us(torch, stream, [lambda r=r: routed(r) for r in range(R3)], 10)
+        touched = int((counts > 0).sum().item())
+        wb = touched * 2 * per
+        c3[f"live{live}_bucket{bucket}"] = {"us": round(us_3, 3), "distinct_experts": touched, "weight_bytes": wb,
+                                            "weight_gbs": gb(wb, us_3),
+                                            "kernels": ["rmsnorm_q8_1", "topk_route", "moe_plan", "mmvq_id(gate,up)"]}
+    out["c3_routed"] = c3
+    del experts
+
+    # ---- config 4: prefill layer, Q8_0 image once per activation, MMQ q/k/v and gate/up
+    TP, DP, NFF = 3325, 3584, 18944
+    rb = DP // 32
+    xa = dev(synth.activations(130, TP, DP))
+    xb = dev(synth.activations(131, TP, DP))
+    qa = torch.empty((TP * rb * 32,), dtype=torch.int8, device="cuda")
+    da = torch.empty((TP * rb,), dtype=torch.int16, device="cuda")
+    qb = torch.empty_like(qa)
+    db = torch.empty_like(da)
+    shapes = [3584, 512, 512, NFF, NFF]
+    layer_w = sum(weight_bytes(n, DP) for n in shapes)
+    R4 = max(2, -(-3 * l2 // layer_w))
+    layers = [[packed(800 + 10 * r + i, n, DP) for i, n in enumerate(shapes)] for r in range(R4)]
+    ys4 = [torch.empty((TP, n), dtype=torch.float32, device="cuda") for n in shapes]
+    mk = lambda r, idx: [qk.make_proj("q4_0", layers[r][i], shapes[i], DP, ys4[i], shapes[i]) for i in idx]
+
+    def layer(r):
+        qk.qk_quantize_q8_0(xa, TP, DP, DP, qa, da, rb)
+        qk.qk_mmq(qa, da, rb, TP, mk(r, (0, 1, 2)))
+        qk.qk_quantize_q8_0(xb, TP, DP, DP, qb, db, rb)
+        qk.qk_mmq(qb, db, rb, TP, mk(r, (3, 4)))
+
+    us_4 = _graph_us(torch, stream, [lambda r=r: layer(r) for r in range(R4)], 2)
+    us_4q = _graph_us(torch, stream, [lambda: qk.qk_quantize_q8_0(xa, TP, DP, DP, qa, da, rb) for _ in range(R4)], 3)
+    us_4a = _graph_us(torch, stream, [lambda r=r: qk.qk_mmq(qa, da, rb, TP, mk(r, (0, 1, 2))) for r in range(R4)], 2)
+    us_4b = _graph_us(torch, stream, [lambda r=r: qk.qk_mmq(qb, db, rb, TP, mk(r, (3, 4))) for r in range(R4)], 2)
+    flops = 2 * TP * DP * sum(shapes)
+    ops_qkv, ops_gu = 2 * TP * DP * 4608, 2 * TP * DP * 2 * NFF
+    peak_t = None
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peak_t = json.load(f).get("bf16_tflops")
+    out["c4_prefill_layer"] = {
+        "us": round(us_4, 2), "quantize_q8_0_us": round(us_4q, 2), "mmq_qkv_us": round(us_4a, 2),
+        "mmq_gate_up_us": round(us_4b, 2), "mmq_tflops": round((ops_qkv + ops_gu) / ((us_4a + us_4b) * 1e-6) / 1e12, 1),
+        "layer_ops": flops, "quantize_gbs": gb(TP * DP * 4 + TP * DP + TP * rb * 2, us_4q),
+        "mmq_frac_of_measured_bf16_dense_peak": (round((ops_qkv + ops_gu) / ((us_4a + us_4b) * 1e-6) / 1e12 / peak_t, 4)
+                                                 if peak_t else None),
+        "note": "MMQ runs f16 mma.sync with exact integer operands (tcgen05 kind::i8 is not available on "
+                "sm_103a); its fraction is against the measured cuBLAS bf16 dense peak",
+        "replicas": R4}
+    return out
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -430,6 +614,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the per-component times of the other workloads (GLU+down, routed MoE, prefill MMQ)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
