@@ -358,6 +358,9 @@ constexpr int SK_THREADS = (SK_CONS + 1) * 32;
 constexpr int BREC = 640;       // [0,512) fragments (16 B per lane), [512,576) C quads, [576,640) scales (per t4)
 constexpr int IMG_AHEAD = 3;    // units of image words a consumer warp has in flight
 
+static_assert(Layout<QK_W_Q4_0>::SLOTS % NPH == 0 && Layout<QK_W_Q8_0>::SLOTS % NPH == 0,
+              "a ring slot must come back to the same unit phase");
+
 template <int WT>
 struct SkLayout {
     static constexpr int UNIT = Layout<WT>::UNIT, SLOTS = Layout<WT>::SLOTS;
@@ -780,12 +783,26 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------- routed path
-// One CTA of 8 warps per (projection, expert, 128-row tile). Experts with no
-// planned pair return at once. Warps take the K blocks round-robin, reading
-// the expert's packed units from global memory, and reduce in shared memory
-// in fixed warp order. Up to 8 planned pairs per pass; more pairs re-run the
-// pass (the weights then come from L2).
+// One CTA per (projection, expert, 128-row tile); experts with no planned pair
+// return at once and read no weights. A live tile streams its 128x128 units
+// with TMA bulk copies into a small ring (a producer warp), and 8 consumer
+// warps take the blocks: warp w does block w & 3 of the units with index
+// = w >> 2 mod 2, for all 128 rows and up to 8 planned pairs at a time (more
+// pairs re-run the pass; the weights then come from L2). The warps' partial
+// sums are added in fixed warp order, so a row's bits depend neither on the
+// other rows routed with it nor on the live count.
 constexpr int RW = 8;
+constexpr int ID_PAR = RW / 4;   // units in work at once
+constexpr int ID_THREADS = (RW + 1) * 32;
+
+template <int WT> struct IdLayout;
+// Slot s is reused by unit s + SLOTS, which must belong to the same warps
+// (units in work at once divide SLOTS): a waiter two phases ahead would see
+// the barrier's parity alias and pass early.
+template <> struct IdLayout<QK_W_Q4_0> { static constexpr int SLOTS = 6; };
+template <> struct IdLayout<QK_W_Q8_0> { static constexpr int SLOTS = 4; };
+static_assert(IdLayout<QK_W_Q4_0>::SLOTS % ID_PAR == 0 && IdLayout<QK_W_Q8_0>::SLOTS % ID_PAR == 0,
+              "a ring slot must come back to the same unit phase");
 
 struct IdProj {
     const uint8_t *w;
@@ -802,12 +819,26 @@ struct IdArgs {
 };
 
 template <int WT>
-__global__ void __launch_bounds__(RW * 32) mmvq_id_kernel(const __grid_constant__ IdArgs a) {
+size_t id_smem() {
+    return (size_t)IdLayout<WT>::SLOTS * Layout<WT>::UNIT + (size_t)RW * VALS * sizeof(float) +
+           2 * IdLayout<WT>::SLOTS * sizeof(uint64_t);
+}
+
+__device__ __forceinline__ void id_consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(RW * 32) : "memory");
+}
+
+template <int WT>
+__global__ void __launch_bounds__(ID_THREADS) mmvq_id_kernel(const __grid_constant__ IdArgs a) {
     using L = Layout<WT>;
-    extern __shared__ __align__(16) float red_id[];   // [RW][VALS]
+    constexpr int SLOTS = IdLayout<WT>::SLOTS;
+    extern __shared__ __align__(128) uint8_t smem[];
+    float *red = reinterpret_cast<float *>(smem + SLOTS * L::UNIT);   // [RW][VALS]
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + RW * VALS);
+    uint64_t *empty = full + SLOTS;
     __shared__ int tok_img[8], tok_out[8];
     pdl_trigger();
-    pdl_wait();
+    pdl_wait();   // counts, offsets and items come from the plan kernel
     const int tile = blockIdx.x;
     int j = 0;
     while (j + 1 < a.n_proj && tile >= a.p[j + 1].tiles_begin) j++;
@@ -819,9 +850,36 @@ __global__ void __launch_bounds__(RW * 32) mmvq_id_kernel(const __grid_constant_
     const int item0 = __ldg(a.offsets + e);
     const uint8_t *wbase = P.w + (int64_t)e * P.expert_bytes + (int64_t)rt * P.chunks * L::UNIT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t4 = lane & 3, g = lane >> 2;
-    const int Kb = P.K / QB;
+    const int Kb = P.K / QB, chunks = P.chunks, passes = (n_items + 7) / 8;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SLOTS; s++) {
+            mbar_init(smem_addr(full + s), 1);
+            mbar_init(smem_addr(empty + s), 4 * 32);   // the four warps that take a unit
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const uint32_t ring = smem_addr(smem);
 
-    for (int pass = 0; pass * 8 < n_items; pass++) {
+    if (warp == RW) {   // ---------------- producer
+        if (lane == 0) {
+            const uint64_t pol = evict_first_policy();
+            for (int s = 0; s < passes * chunks; s++) {
+                const int slot = s % SLOTS;
+                const uint32_t n = (uint32_t)s / SLOTS;
+                if (n > 0 && !mbar_wait(smem_addr(empty + slot), (n - 1) & 1u)) break;
+                mbar_expect_tx(smem_addr(full + slot), L::UNIT);
+                bulk_g2s(ring + (uint32_t)slot * L::UNIT, wbase + (int64_t)(s % chunks) * L::UNIT, L::UNIT,
+                         smem_addr(full + slot), pol);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    bool ok = true;
+    const int jb = warp & 3, par = warp >> 2;
+    for (int pass = 0; pass < passes; pass++) {
         if (threadIdx.x < 8) {
             const int idx = pass * 8 + threadIdx.x;
             int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
@@ -829,7 +887,7 @@ __global__ void __launch_bounds__(RW * 32) mmvq_id_kernel(const __grid_constant_
             tok_img[threadIdx.x] = p >= 0 ? p / a.k : -1;
             tok_out[threadIdx.x] = p;
         }
-        __syncthreads();
+        id_consumers_sync();
         const int rB = tok_img[g], rS0 = tok_img[2 * t4], rS1 = tok_img[2 * t4 + 1];
         const uint8_t *imgB = rB >= 0 ? a.img + (int64_t)rB * a.img_row_bytes : nullptr;
         const uint8_t *imgS0 = rS0 >= 0 ? a.img + (int64_t)rS0 * a.img_row_bytes : nullptr;
@@ -839,28 +897,40 @@ __global__ void __launch_bounds__(RW * 32) mmvq_id_kernel(const __grid_constant_
         for (int r = 0; r < UNIT_GROUPS; r++)
 #pragma unroll
             for (int i = 0; i < 4; i++) acc[r][i] = 0.0f;
-        for (int b = warp; b < Kb; b += RW) {
-            const uint8_t *unit = wbase + (int64_t)(b >> 2) * L::UNIT;
-            BSide s;
-            bside<WT>(load_raw(imgB, imgS0, imgS1, b, t4), s);
-            block_rows<WT, false>(unit + (b & 3) * L::BLOCK, 0, unit + L::SCALES + (b & 3) * 256, 0, lane, s, acc);
+        // this warp's units: u = par mod ID_PAR; the image words one unit ahead
+        int u = par;
+        Raw next = {0u, 0u, 0u, 0u};
+        if (u < chunks && 4 * u + jb < Kb) next = load_raw(imgB, imgS0, imgS1, 4 * u + jb, t4);
+        for (; u < chunks; u += ID_PAR) {
+            const Raw cur = next;
+            if (u + ID_PAR < chunks && 4 * (u + ID_PAR) + jb < Kb)
+                next = load_raw(imgB, imgS0, imgS1, 4 * (u + ID_PAR) + jb, t4);
+            const int s = pass * chunks + u, slot = s % SLOTS;
+            if (ok) ok = mbar_wait(smem_addr(full + slot), ((uint32_t)s / SLOTS) & 1u);
+            if (ok && 4 * u + jb < Kb) {
+                BSide bs;
+                bside<WT>(cur, bs);
+                const uint32_t ub = ring + (uint32_t)slot * L::UNIT;
+                block_rows<WT, true>(nullptr, ub + jb * L::BLOCK, nullptr, ub + L::SCALES + jb * 256, lane, bs, acc);
+            }
+            mbar_arrive(smem_addr(empty + slot));   // after this thread's shared loads
         }
 #pragma unroll
         for (int r = 0; r < UNIT_GROUPS; r++)
 #pragma unroll
-            for (int i = 0; i < 4; i++) red_id[warp * VALS + (r * 4 + i) * 32 + lane] = acc[r][i];
-        __syncthreads();
+            for (int i = 0; i < 4; i++) red[warp * VALS + (r * 4 + i) * 32 + lane] = acc[r][i];
+        id_consumers_sync();
         for (int t = threadIdx.x; t < VALS; t += RW * 32) {
             float sum = 0.0f;
 #pragma unroll
-            for (int w = 0; w < RW; w++) sum += red_id[w * VALS + t];
+            for (int w = 0; w < RW; w++) sum += red[w * VALS + t];
             int row, slot;
             val_pos(t, row, slot);
             row += rt * UNIT_ROWS;
             const int orow = tok_out[slot];
             if (row < P.N && orow >= 0) P.y[(int64_t)orow * P.N + row] = sum;
         }
-        __syncthreads();   // tok_* and red_id are reused by the next pass
+        id_consumers_sync();   // tok_* and red are reused by the next pass
     }
 }
 
@@ -1044,10 +1114,24 @@ qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k
         d.tiles_begin = tiles;
         tiles += d.row_tiles * projs[j].n_experts;
     }
-    const size_t smem = (size_t)RW * VALS * sizeof(float);
-    if (projs[0].wtype == QK_W_Q4_0)
-        return launch_pdl("mmvq_id", mmvq_id_kernel<QK_W_Q4_0>, dim3(tiles), dim3(RW * 32), smem, s, a);
-    return launch_pdl("mmvq_id", mmvq_id_kernel<QK_W_Q8_0>, dim3(tiles), dim3(RW * 32), smem, s, a);
+    if (projs[0].wtype == QK_W_Q4_0) {
+        static bool configured = false;
+        if (!configured) {
+            cudaError_t e = cudaFuncSetAttribute(mmvq_id_kernel<QK_W_Q4_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)id_smem<QK_W_Q4_0>());
+            if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq_id: shared memory attribute: %s", cudaGetErrorString(e));
+            configured = true;
+        }
+        return launch_pdl("mmvq_id", mmvq_id_kernel<QK_W_Q4_0>, dim3(tiles), dim3(ID_THREADS), id_smem<QK_W_Q4_0>(), s, a);
+    }
+    static bool configured8 = false;
+    if (!configured8) {
+        cudaError_t e = cudaFuncSetAttribute(mmvq_id_kernel<QK_W_Q8_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)id_smem<QK_W_Q8_0>());
+        if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq_id: shared memory attribute: %s", cudaGetErrorString(e));
+        configured8 = true;
+    }
+    return launch_pdl("mmvq_id", mmvq_id_kernel<QK_W_Q8_0>, dim3(tiles), dim3(ID_THREADS), id_smem<QK_W_Q8_0>(), s, a);
 }
 
 }  // namespace qk

@@ -17,6 +17,8 @@ duration with the case's algorithmic bytes (or flops) per launch. Cases:
   quantize      qk_quantize_q8_1, [8, 8192]         (kernel quantize)
   glu           qk_glu_q8_1 SwiGLU packed [8, 18944] (kernel glu_q8_1)
   mmvq_id_<R>   qk_mmvq_id, gate+up 2560->768 over 128 experts, top-8 of R rows (kernel mmvq_id)
+  routed_<R>    the routed chain for R live rows of a 16/128 bucket: RMSNorm*w -> image, top-8 of
+                128, plan, mmvq_id gate+up (kernels rmsnorm_q8_1, topk, plan, mmvq_id)
   mmq_qkv       qk_mmq, 3325 tokens, q/k/v          (kernel mmq)
   quantize_q8_0 qk_quantize_q8_0, [3325, 3584]      (kernel quantize)
 """
@@ -131,6 +133,42 @@ def build_case(name):
         nbytes = 2 * live * NF * (K // 32) * Q4_ROW_BYTES + 2 * rows * k * NF * 4 + rows * (K // 32) * Q8_1_BLOCK
         return (lambda: qk.qk_mmvq_id(img, K // 32, rows, k, projs, counts, offsets, items), keep,
                 {"bytes": nbytes, "live_experts": live})
+    if name.startswith("routed_"):
+        E, k, K, NF, live = 128, 8, 2560, 768, int(name.rsplit("_", 1)[1])
+        bucket = 16 if live <= 16 else 128
+        per = qk.qk_weight_packed_bytes("q4_0", NF, K)
+        ws = []
+        for p in range(2):
+            buf = torch.empty((E * per,), dtype=torch.uint8, device="cuda")
+            for e in range(E):
+                qk.qk_weight_pack("q4_0", _dev(synth.q4_0_weight(1000 * p + e, NF, K).reshape(-1)), NF, K,
+                                  buf[e * per:(e + 1) * per], per)
+            ws.append(buf)
+        x, w = _dev(synth.activations(5, bucket, K)), _dev(synth.norm_weight(6, K))
+        y = torch.empty((bucket, K), dtype=torch.float32, device="cuda")
+        img = torch.empty((bucket * (K // 32) * 36,), dtype=torch.uint8, device="cuda")
+        logits = _dev(synth.router_logits(3, bucket, E))
+        ids = torch.empty((bucket, k), dtype=torch.int32, device="cuda")
+        wts = torch.empty((bucket, k), dtype=torch.float32, device="cuda")
+        counts = torch.empty((E,), dtype=torch.int32, device="cuda")
+        offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+        items = torch.empty((bucket * k,), dtype=torch.int32, device="cuda")
+        lv = torch.tensor([live], dtype=torch.int32, device="cuda")
+        ys = [torch.empty((bucket * k, NF), dtype=torch.float32, device="cuda") for _ in range(2)]
+        projs = [qk.make_proj_id("q4_0", E, ws[p], NF, K, ys[p]) for p in range(2)]
+
+        def chain():
+            qk.qk_rmsnorm_q8_1(x, bucket, K, K, "mul", w, None, 1.0, 1e-6, y, K, img, K // 32, d_live_rows=lv)
+            qk.qk_topk_route(logits, bucket, E, k, ids, wts, d_live_rows=lv)
+            qk.qk_moe_plan(ids, bucket, k, E, counts, offsets, items, d_live_rows=lv)
+            qk.qk_mmvq_id(img, K // 32, bucket, k, projs, counts, offsets, items)
+
+        chain()
+        torch.cuda.synchronize()
+        live_e = int((counts > 0).sum().item())
+        keep = ws + ys + [x, w, y, img, logits, ids, wts, counts, offsets, items, lv]
+        nbytes = 2 * live_e * per + 2 * bucket * k * NF * 4 + bucket * (K // 32) * Q8_1_BLOCK
+        return chain, keep, {"bytes": nbytes, "live_experts": live_e}
     if name in ("mmq_qkv", "quantize_q8_0"):
         T, K = 3325, 3584
         x = _dev(synth.activations(4, T, K))
