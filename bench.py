@@ -512,17 +512,20 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
     layers = [[packed(800 + 10 * r + i, n, DP) for i, n in enumerate(shapes)] for r in range(R4)]
     ys4 = [torch.empty((TP, n), dtype=torch.float32, device="cuda") for n in shapes]
     mk = lambda r, idx: [qk.make_proj("q4_0", layers[r][i], shapes[i], DP, ys4[i], shapes[i]) for i in idx]
+    ws4_n = qk.qk_mmq_workspace_bytes(TP, mk(0, (0,)))
+    ws4 = torch.empty((ws4_n,), dtype=torch.uint8, device="cuda")
+    mmq = lambda q_, d_, projs: qk.qk_mmq(q_, d_, rb, TP, projs, ws4, ws4_n)
 
     def layer(r):
         qk.qk_quantize_q8_0(xa, TP, DP, DP, qa, da, rb)
-        qk.qk_mmq(qa, da, rb, TP, mk(r, (0, 1, 2)))
+        mmq(qa, da, mk(r, (0, 1, 2)))
         qk.qk_quantize_q8_0(xb, TP, DP, DP, qb, db, rb)
-        qk.qk_mmq(qb, db, rb, TP, mk(r, (3, 4)))
+        mmq(qb, db, mk(r, (3, 4)))
 
     us_4 = _graph_us(torch, stream, [lambda r=r: layer(r) for r in range(R4)], 2)
     us_4q = _graph_us(torch, stream, [lambda: qk.qk_quantize_q8_0(xa, TP, DP, DP, qa, da, rb) for _ in range(R4)], 3)
-    us_4a = _graph_us(torch, stream, [lambda r=r: qk.qk_mmq(qa, da, rb, TP, mk(r, (0, 1, 2))) for r in range(R4)], 2)
-    us_4b = _graph_us(torch, stream, [lambda r=r: qk.qk_mmq(qb, db, rb, TP, mk(r, (3, 4))) for r in range(R4)], 2)
+    us_4a = _graph_us(torch, stream, [lambda r=r: mmq(qa, da, mk(r, (0, 1, 2))) for r in range(R4)], 2)
+    us_4b = _graph_us(torch, stream, [lambda r=r: mmq(qb, db, mk(r, (3, 4))) for r in range(R4)], 2)
     flops = 2 * TP * DP * sum(shapes)
     ops_qkv, ops_gu = 2 * TP * DP * 4608, 2 * TP * DP * 2 * NFF
     peak_t = None
@@ -536,8 +539,9 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
         "layer_ops": flops, "quantize_gbs": gb(TP * DP * 4 + TP * DP + TP * rb * 2, us_4q),
         "mmq_frac_of_measured_bf16_dense_peak": (round((ops_qkv + ops_gu) / ((us_4a + us_4b) * 1e-6) / 1e12 / peak_t, 4)
                                                  if peak_t else None),
-        "note": "MMQ runs f16 mma.sync with exact integer operands (tcgen05 kind::i8 is not available on "
-                "sm_103a); its fraction is against the measured cuBLAS bf16 dense peak",
+        "note": "MMQ runs tcgen05.mma kind::f16 (binary16 dequantised operands, f32 accumulation in tensor "
+                "memory; kind::i8 is not available on sm_103a); its fraction is against the measured cuBLAS "
+                "bf16 dense peak (f16 and bf16 share the dense rate)",
         "replicas": R4}
     return out
 

@@ -112,7 +112,8 @@ QK_API uint64_t qk_launch_count(void);
 /*
  * Device-side fault word of the current device, then cleared. Bit 0: a
  * kernel's bounded wait on a shared-memory barrier gave up (the kernel then
- * stopped early and its outputs are not valid). Synchronises the device.
+ * stopped early and its outputs are not valid). Covers qk_mmvq, qk_mmvq_id
+ * and qk_mmq. Synchronises the device.
  */
 QK_API qk_status qk_device_faults(uint32_t *faults);
 
@@ -354,10 +355,19 @@ QK_API qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t row
  *   qs [T][row_blocks*32] int8 and d [T][row_blocks] half: qk_quantize_q8_0
  *   C[t][n] = sum_b d_w[n][b] * d_a[t][b] * sum_{i in b} w_i * q_i
  *   (Q4_0: w_i = nibble - 8) written to projs[j].y ([T][y_stride] F32)
- * Errors: QK_ERR_ARG, QK_ERR_SHAPE, QK_ERR_UNSUPPORTED, QK_ERR_ALIAS.
+ * Runs on the tensor cores with binary16 operands (nibble - 8) * d_w and
+ * q * d_a, each rounded once, accumulated in binary32: within about 2^-11
+ * relative per product of the exact block form (NMSE ~1e-7).
+ *   ws: caller workspace of qk_mmq_workspace_bytes bytes, 128-byte aligned;
+ *   it holds the dequantised image for this call (scratch, no state kept).
+ *   Two launches on the stream (the dequantisation, then the GEMM).
+ * Errors: QK_ERR_ARG, QK_ERR_SHAPE, QK_ERR_UNSUPPORTED, QK_ERR_ALIAS,
+ * QK_ERR_WORKSPACE.
  */
+QK_API size_t qk_mmq_workspace_bytes(int64_t T, int32_t n_proj, const qk_proj *projs);
 QK_API qk_status qk_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int64_t T,
-                 int32_t n_proj, const qk_proj *projs, qk_stream stream);
+                 int32_t n_proj, const qk_proj *projs, void *ws, size_t ws_bytes,
+                 qk_stream stream);
 
 #ifdef __cplusplus
 }

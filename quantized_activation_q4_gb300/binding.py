@@ -65,7 +65,8 @@ _SIGS = {
     "qk_topk_route": ([P, I64, I32, I32, P, P, P, P], C.c_int),
     "qk_moe_plan": ([P, I64, I32, I32, P, P, P, P, P], C.c_int),
     "qk_mmvq_id": ([P, I64, I64, I32, I32, C.POINTER(qk_proj_id), P, P, P, P], C.c_int),
-    "qk_mmq": ([P, P, I64, I64, I32, C.POINTER(qk_proj), P], C.c_int),
+    "qk_mmq_workspace_bytes": ([I64, I32, C.POINTER(qk_proj)], C.c_size_t),
+    "qk_mmq": ([P, P, I64, I64, I32, C.POINTER(qk_proj), P, C.c_size_t, P], C.c_int),
 }
 
 
@@ -208,9 +209,15 @@ def qk_mmvq_id(img, img_row_blocks, rows, k, projs, counts, offsets, items, stre
                                            _ptr(offsets), _ptr(items), _stream(stream)))
 
 
-def qk_mmq(qs, d, row_blocks, T, projs, stream=None):
+def qk_mmq_workspace_bytes(T, projs) -> int:
     arr = (qk_proj * len(projs))(*projs)
-    _check("qk_mmq", load().qk_mmq(_ptr(qs), _ptr(d), row_blocks, T, len(projs), arr, _stream(stream)))
+    return int(load().qk_mmq_workspace_bytes(T, len(projs), arr))
+
+
+def qk_mmq(qs, d, row_blocks, T, projs, ws, ws_bytes, stream=None):
+    arr = (qk_proj * len(projs))(*projs)
+    _check("qk_mmq", load().qk_mmq(_ptr(qs), _ptr(d), row_blocks, T, len(projs), arr, _ptr(ws), ws_bytes,
+                                   _stream(stream)))
 
 
 # ------------------------------------------------------------------ routing

@@ -1,35 +1,62 @@
-// Prefill dense contraction on a Q8_0 activation image (minfer doc 52 "r49
+// Prefill dense contraction on a Q8_0 activation image (minfer doc 52, "r49
 // A-quantize prepass shared-A dedup", sections 1 and 5: the q/k/v and
 // gate/up GEMMs that read one quantised A).
 //
-//   C[t][n] = sum_b d_w[n][b] * d_a[t][b] * D,   D = sum_{i in b} (nibble_i - 8) * q_i
+//   C[t][n] = sum_b d_w[n][b] * d_a[t][b] * sum_{i in b} (nibble_i - 8) * q_i
 //
-// Like the MMVQ kernels, the exact integer block dot D runs on the f16 tensor
-// path (mma.sync m16n8k16): nibbles and codes are exact halves and every
-// partial sum stays below 2^22. Nibbles are turned into halves by OR-ing them
-// under an exponent (1024 + lo, 64 + hi); the per-token correction
-// -(1032 * sum of the low-half codes + 72 * sum of the high-half codes)
-// removes both that bias and the "- 8" of Q4_0 at once, so it seeds the
-// accumulator and D comes out exact. The block scales d_w * d_a are applied
-// per block in f32 (two FP operations per output per block), which makes this
-// contraction bound by FP32 issue rather than by the tensor pipe.
+// On the 5th-generation tensor cores (tcgen05.mma kind::f16, accumulator in
+// tensor memory). Both operands enter as binary16 values of the dequantised
+// blocks, each rounded once: A[n][k] = f16((nibble - 8) * d_w) and
+// B[t][k] = f16(q * d_a), and the MMA accumulates over all of K in binary32.
+// The pages scale an exact int8 block dot in f32 instead; the two agree to
+// about 2^-11 relative per product (NMSE ~1e-7), far inside their 5e-4 bound.
+// (tcgen05 kind::i8 does not exist on sm_103a, and applying the scales block
+// by block from tensor memory would bound the kernel by FP32 issue.)
 //
-// CTA: 8 warps, a 128-row weight tile (one packed unit row, warp w = row
-// group w) by 64 tokens (8 token groups). Per 128-column chunk the CTA stages
-// the unit (cp.async, 9216 B) and the 64 tokens' codes and scales, converts
-// the codes once into f16 B fragments with their corrections, then every warp
-// runs 8 token groups x 4 blocks of MMAs. Two stages double-buffer the
-// copies.
+// Two kernels per call:
+//   dequant_b: the image -> B, [T][K] binary16 in the caller's workspace,
+//     once per call (it is read by every 128-row weight tile).
+//   mmq_tc: one CTA per (projection, 128-row weight tile, 256-token tile).
+//     warp 0: TMA -- the B tiles (2D tensor copies, 128-byte swizzle) and the
+//             packed weight units (bulk copies) into shared-memory rings;
+//     warps 2-5: turn each unit's nibbles into the swizzled f16 A tile;
+//     warp 1: allocates tensor memory and issues the MMAs (one thread), then
+//             warps 2-5 read the 128 x 256 f32 accumulator and store C.
+// Within a 32-block the K positions follow the order in which a packed
+// weight word converts (see a_word); dequant_b writes B in the same order.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "qk_internal.cuh"
 
 namespace qk {
 namespace {
 
-constexpr int MW = 8;        // warps = row groups of the 128-row tile
-constexpr int TT = 64;       // tokens per CTA
-constexpr int TG = TT / 8;   // token groups
 constexpr int MAX_PROJ = 8;
+constexpr int TM = 128;              // weight rows per CTA (MMA M)
+constexpr int TN = 256;              // tokens per CTA (MMA N)
+constexpr int KC = 64;               // K elements per stage (one 128-byte swizzle row of f16)
+constexpr int NS = 4;                // stages
+constexpr int NU = 2;                // packed-unit staging slots (a unit = 2 stages)
+constexpr int A_TILE = TM * KC * 2;  // 16 KB
+constexpr int B_TILE = TN * KC * 2;  // 32 KB
+constexpr int THREADS = 6 * 32;
+constexpr uint32_t SPIN_LIMIT = 1u << 16;
+constexpr uint32_t SUSPEND_NS = 20000;
+
+// shared memory: [A tiles][B tiles][units][barriers][tensor-memory address]
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + NS * A_TILE;
+constexpr int OFF_U = OFF_B + NS * B_TILE;
+constexpr int OFF_BAR = OFF_U + NU * Q4_UNIT_BYTES;
+constexpr int N_BARS = 3 * NS + 2 * NU + 1;
+constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + slack to align the base to 1024
+
+// instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 256, M = 128
+constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
+
+__device__ unsigned int g_mmq_faults = 0;
 
 struct MmqProj {
     const uint8_t *w;
@@ -38,207 +65,284 @@ struct MmqProj {
     int N, K, chunks, row_tiles, tiles_begin;
 };
 struct MmqArgs {
-    const int8_t *qs;
-    const uint16_t *d;
-    int64_t row_blocks;
+    CUtensorMap bmap;    // B [T][K] f16, box 64 x 256, 128-byte swizzle
     int T, n_proj;
     MmqProj p[MAX_PROJ];
 };
 
-// shared memory per stage
-struct Stage {
-    uint8_t unit[Q4_UNIT_BYTES];       // packed weights of the chunk
-    int8_t codes[TT][128];             // the chunk's codes of 64 tokens
-    uint16_t dh[TT][4];                // their block scales (half bits)
-};
-struct Frags {
-    uint4 b[4][TG][32];                // [block][token group][lane]: (lo02, lo13, hi02, hi13)
-    float corr[4][TT];                 // -(1032 S_lo + 72 S_hi) per block and token
-    float da[4][TT];                   // d_a per block and token
-};
-
+// ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
-    const int n = valid ? 16 : 0;   // 0 source bytes: the 16 destination bytes are zero-filled
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(n) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1,
-                                        const float c[4]) {
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+// Bounded wait: suspends until the phase completes (or SUSPEND_NS), gives up
+// after SPIN_LIMIT tries (about a second at most), records a fault and
+// returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+    for (uint32_t i = 0; i < SPIN_LIMIT; i++) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(a), "r"(parity), "r"(SUSPEND_NS)
+            : "memory");
+        if (ok) return true;
+    }
+    atomicOr(&g_mmq_faults, 1u);
+    return false;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t mbar) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
-          "f"(c[2]), "f"(c[3]));
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
+        : "memory");
 }
-
-// Four int8 codes -> exact half2 (c0, c2) and (c1, c3) (XOR 0x80, exponent of
-// 1024, minus 1152).
-__device__ __forceinline__ void codes_to_half2(uint32_t w, uint32_t &h02, uint32_t &h13) {
-    const uint32_t u = w ^ 0x80808080u;
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    uint32_t a = __byte_perm(u, 0x64646464u, 0x4240);
-    uint32_t b = __byte_perm(u, 0x64646464u, 0x4341);
-    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
-    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
-    h02 = *reinterpret_cast<uint32_t *>(&ha);
-    h13 = *reinterpret_cast<uint32_t *>(&hb);
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
 }
+__device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
+        "l"(a), "l"(b), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void nibbles_to_half2(uint32_t w, uint32_t &lo02, uint32_t &lo13, uint32_t &hi02,
-                                                 uint32_t &hi13) {
+// Four weight bytes (word t of one row of a Q4_0 block) -> 16 bytes of f16
+// A values (nibble - 8) * dw, K order: e(4t), e(4t+2), e(4t+1), e(4t+3),
+// e(16+4t), e(16+4t+2), e(16+4t+1), e(16+4t+3). The nibble becomes an exact
+// half by OR-ing it under an exponent (1024 + lo, 64 + hi); subtracting
+// 1032 / 72 leaves the exact nibble - 8; one rounding in the multiply by dw.
+__device__ __forceinline__ uint32_t a_pair(uint32_t v, __half2 bias, __half2 dw) {
+    const __half2 r = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&v), bias), dw);
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+__device__ __forceinline__ uint4 a_word(uint32_t w, __half2 dw) {
     const uint32_t w8 = w >> 8;
-    lo02 = (w & 0x000F000Fu) | 0x64006400u;
-    hi02 = (w & 0x00F000F0u) | 0x54005400u;
-    lo13 = (w8 & 0x000F000Fu) | 0x64006400u;
-    hi13 = (w8 & 0x00F000F0u) | 0x54005400u;
+    const __half2 blo = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    const __half2 bhi = __halves2half2(__ushort_as_half(0x5480), __ushort_as_half(0x5480));   // 72
+    return make_uint4(a_pair((w & 0x000F000Fu) | 0x64006400u, blo, dw), a_pair((w8 & 0x000F000Fu) | 0x64006400u, blo, dw),
+                      a_pair((w & 0x00F000F0u) | 0x54005400u, bhi, dw),
+                      a_pair((w8 & 0x00F000F0u) | 0x54005400u, bhi, dw));
 }
 
-// Sum of four signed bytes.
-__device__ __forceinline__ int sum4(uint32_t w) {
-    return (int)(int8_t)(w & 0xff) + (int)(int8_t)((w >> 8) & 0xff) + (int)(int8_t)((w >> 16) & 0xff) +
-           (int)(int8_t)(w >> 24);
+// ------------------------------------------------------------------ B = dequantised image
+__device__ __forceinline__ uint32_t b_pair(uint32_t v, int k0, int k1, float da) {
+    const float x = (float)(int8_t)(v >> (8 * k0)), y = (float)(int8_t)(v >> (8 * k1));
+    const __half2 r = __floats2half2_rn(x * da, y * da);   // products exact in f32; one rounding
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-__global__ void __launch_bounds__(MW * 32) mmq_kernel(const __grid_constant__ MmqArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    Stage *st = reinterpret_cast<Stage *>(smem);                       // [2]
-    Frags *fr = reinterpret_cast<Frags *>(smem + 2 * sizeof(Stage));
+// One thread per (token, block, word): 8 codes -> 16 bytes of f16 q * d_a in
+// the K order of a_word.
+__global__ void __launch_bounds__(256) dequant_b_kernel(const int8_t *__restrict__ qs, const uint16_t *__restrict__ d,
+                                                        int64_t row_blocks, int T, int kb, __half *__restrict__ B) {
     pdl_trigger();
     pdl_wait();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)T * kb * 4) return;
+    const int w = (int)(i & 3);
+    const int64_t tb = i >> 2;
+    const int t = (int)(tb / kb), b = (int)(tb % kb);
+    const int8_t *src = qs + ((int64_t)t * row_blocks + b) * QB;
+    const uint32_t lo = __ldg(reinterpret_cast<const unsigned int *>(src + 4 * w));
+    const uint32_t hi = __ldg(reinterpret_cast<const unsigned int *>(src + 16 + 4 * w));
+    const float da = __half2float(__ushort_as_half(__ldg(d + (int64_t)t * row_blocks + b)));
+    const uint4 out = make_uint4(b_pair(lo, 0, 2, da), b_pair(lo, 1, 3, da), b_pair(hi, 0, 2, da), b_pair(hi, 1, 3, da));
+    *reinterpret_cast<uint4 *>(B + ((int64_t)t * kb + b) * QB + 8 * w) = out;
+}
 
-    const int tile = blockIdx.x;
+// ------------------------------------------------------------------ the GEMM
+__global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constant__ MmqArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t full_a = sbase + OFF_BAR, full_b = full_a + NS * 8, empty = full_b + NS * 8;
+    const uint32_t ufull = empty + NS * 8, uempty = ufull + NU * 8, done = uempty + NU * 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + N_BARS * 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int j = 0;
-    while (j + 1 < a.n_proj && tile >= a.p[j + 1].tiles_begin) j++;
+    while (j + 1 < a.n_proj && (int)blockIdx.x >= a.p[j + 1].tiles_begin) j++;
     const MmqProj &P = a.p[j];
-    const int rt = tile - P.tiles_begin;
-    const int tok0 = blockIdx.y * TT;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    const int Kb = P.K / QB;
-    const uint8_t *wtile = P.w + (int64_t)rt * P.chunks * Q4_UNIT_BYTES;
+    const int rt = blockIdx.x - P.tiles_begin, tok0 = blockIdx.y * TN;
+    const int nkc = (P.K + KC - 1) / KC;
 
-    auto issue = [&](int c, int s) {
-        Stage &S = st[s];
-        const uint8_t *src = wtile + (int64_t)c * Q4_UNIT_BYTES;
-        for (int i = tid; i < Q4_UNIT_BYTES / 16; i += MW * 32) cp_async16(S.unit + i * 16, src + i * 16, true);
-        // codes: 64 tokens x 8 x 16 bytes; blocks past K and tokens past T read as zero
-        for (int i = tid; i < TT * 8; i += MW * 32) {
-            const int tk = i >> 3, part = i & 7, b = 4 * c + (part >> 1);
-            const bool ok = tok0 + tk < a.T && b < Kb;
-            const int8_t *s8 = ok ? a.qs + (int64_t)(tok0 + tk) * a.row_blocks * QB + (int64_t)4 * c * QB + part * 16
-                                  : a.qs;
-            cp_async16(&S.codes[tk][part * 16], s8, ok);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; s++) {
+            mbar_init(full_a + 8 * s, 128);   // the four converter warps
+            mbar_init(full_b + 8 * s, 1);     // the producer, with the bytes
+            mbar_init(empty + 8 * s, 1);      // the MMA commit
         }
-        // scales (4 halves per token; plain loads: the scale rows are only 2-byte aligned)
-        for (int i = tid; i < TT; i += MW * 32) {
-            const bool ok = tok0 + i < a.T;
-            const uint16_t *s16 = a.d + (int64_t)(tok0 + i) * a.row_blocks + 4 * c;
-#pragma unroll
-            for (int q = 0; q < 4; q++) S.dh[i][q] = ok && 4 * c + q < Kb ? __ldg(s16 + q) : (uint16_t)0;
+        for (int u = 0; u < NU; u++) {
+            mbar_init(ufull + 8 * u, 1);
+            mbar_init(uempty + 8 * u, 128);
         }
-        cp_commit();
-    };
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {   // tensor memory: 256 columns x 128 lanes of f32 for the accumulator
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();   // B comes from the previous kernel
 
-    float acc[TG][4];
-#pragma unroll
-    for (int q = 0; q < TG; q++)
-#pragma unroll
-        for (int i = 0; i < 4; i++) acc[q][i] = 0.0f;
-
-    issue(0, 0);
-    for (int c = 0; c < P.chunks; c++) {
-        const int s = c & 1;
-        if (c + 1 < P.chunks) {
-            issue(c + 1, s ^ 1);
-            cp_wait<1>();
-        } else {
-            cp_wait<0>();
-        }
-        __syncthreads();   // stage s landed; fr free (previous chunk's MMAs done)
-        // convert codes -> f16 fragments, corrections and scales (one item per thread per block)
-        Stage &S = st[s];
-#pragma unroll
-        for (int jb = 0; jb < 4; jb++) {
-            const int qg = tid >> 5, l = tid & 31, tg_ = l >> 2, tt = l & 3;   // tid = tg*32 + lane
-            const int tk = qg * 8 + tg_;
-            const uint32_t lo = *reinterpret_cast<const uint32_t *>(&S.codes[tk][jb * 32 + 4 * tt]);
-            const uint32_t hi = *reinterpret_cast<const uint32_t *>(&S.codes[tk][jb * 32 + 16 + 4 * tt]);
-            uint4 f;
-            codes_to_half2(lo, f.x, f.y);
-            codes_to_half2(hi, f.z, f.w);
-            fr->b[jb][qg][l] = f;
-            if (tid < TT) {
-                int slo = 0, shi = 0;
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    slo += sum4(*reinterpret_cast<const uint32_t *>(&S.codes[tid][jb * 32 + 4 * q]));
-                    shi += sum4(*reinterpret_cast<const uint32_t *>(&S.codes[tid][jb * 32 + 16 + 4 * q]));
+    if (warp == 0) {   // ---------------- producer
+        if (lane == 0) {
+            const uint8_t *units = P.w + (int64_t)rt * P.chunks * Q4_UNIT_BYTES;
+            for (int kc = 0; kc < nkc; kc++) {
+                const int s = kc % NS;
+                if ((kc & 1) == 0) {   // a packed unit covers two stages
+                    const int u = kc >> 1, us = u % NU;
+                    if (u >= NU && !mbar_wait(uempty + 8 * us, ((u / NU) - 1) & 1u)) break;
+                    mbar_expect_tx(ufull + 8 * us, Q4_UNIT_BYTES);
+                    bulk_g2s(sbase + OFF_U + us * Q4_UNIT_BYTES, units + (int64_t)u * Q4_UNIT_BYTES, Q4_UNIT_BYTES,
+                             ufull + 8 * us);
                 }
-                fr->corr[jb][tid] = -(1032.0f * (float)slo + 72.0f * (float)shi);
-                const bool ok = 4 * c + jb < Kb;
-                fr->da[jb][tid] = ok ? __half2float(__ushort_as_half(S.dh[tid][jb])) : 0.0f;
+                if (kc >= NS && !mbar_wait(empty + 8 * s, ((kc / NS) - 1) & 1u)) break;
+                mbar_expect_tx(full_b + 8 * s, B_TILE);
+                tma_2d(sbase + OFF_B + s * B_TILE, &a.bmap, kc * KC, tok0, full_b + 8 * s);
             }
         }
-        __syncthreads();
-        // MMAs: warp = row group, all token groups, 4 blocks
+    } else if (warp == 1) {   // ---------------- MMA issue (one thread)
+        if (lane == 0) {
+            for (int kc = 0; kc < nkc; kc++) {
+                const int s = kc % NS;
+                const uint32_t par = (kc / NS) & 1u;
+                if (!mbar_wait(full_a + 8 * s, par) || !mbar_wait(full_b + 8 * s, par)) break;
+                tc_fence_after();
+                const uint32_t at = sbase + OFF_A + s * A_TILE, bt = sbase + OFF_B + s * B_TILE;
 #pragma unroll
-        for (int jb = 0; jb < 4; jb++) {
-            if (4 * c + jb >= Kb) break;
-            const uint8_t *blk = S.unit + jb * Q4_BLOCK_STRIDE;
-            const uint4 v = *reinterpret_cast<const uint4 *>(blk + (warp >> 1) * 512 + lane * 16);
-            const uint32_t wg = (warp & 1) ? v.z : v.x, wg8 = (warp & 1) ? v.w : v.y;
-            uint32_t a_lo[4], a_hi[4];
-            nibbles_to_half2(wg, a_lo[0], a_lo[2], a_hi[0], a_hi[2]);
-            nibbles_to_half2(wg8, a_lo[1], a_lo[3], a_hi[1], a_hi[3]);
-            const uint32_t dw2 = *reinterpret_cast<const uint32_t *>(S.unit + 8192 + jb * 256 + g * 32 + warp * 4);
-            const float2 dw = __half22float2(*reinterpret_cast<const __half2 *>(&dw2));
+                for (int ks = 0; ks < KC / 16; ks++)   // 16 f16 = 32 bytes along K per MMA
+                    tc_mma(tmem, sdesc(at + 32 * ks), sdesc(bt + 32 * ks), (kc | ks) != 0);
+                tc_commit(empty + 8 * s);   // frees the stage once these MMAs are done
+            }
+            tc_commit(done);                // the accumulator is final once every MMA issued is done
+        }
+    } else {   // ---------------- warps 2..5: A conversion, then the epilogue
+        // Tile row n: in the packed unit, row 32 k4 + {g, g+8, 16+g, 24+g}[r] of region k4, lane
+        // group g, word slot r; its scale is half h8 of word g*8.. of row group rr (rows 16rr+g, +8).
+        const int n = threadIdx.x - 64;
+        const int g = n & 7, r = (n >> 3) & 3, k4 = n >> 5, rr = n >> 4, h8 = (n >> 3) & 1;
+        bool ok = true;
+        for (int kc = 0; kc < nkc; kc++) {
+            const int s = kc % NS, u = kc >> 1, us = u % NU, h = kc & 1;
+            if (h == 0) ok = mbar_wait(ufull + 8 * us, (u / NU) & 1u);
+            if (ok && kc >= NS) ok = mbar_wait(empty + 8 * s, ((kc / NS) - 1) & 1u);
+            if (!ok) break;
+            const uint8_t *unit = smem + OFF_U + us * Q4_UNIT_BYTES;
+            uint8_t *arow = smem + OFF_A + s * A_TILE + n * 128;
 #pragma unroll
-            for (int q = 0; q < TG; q++) {
-                const uint4 bf = fr->b[jb][q][lane];
-                const float2 cr = *reinterpret_cast<const float2 *>(&fr->corr[jb][q * 8 + 2 * t4]);
-                const float2 da = *reinterpret_cast<const float2 *>(&fr->da[jb][q * 8 + 2 * t4]);
-                const float c4[4] = {cr.x, cr.y, cr.x, cr.y};
-                float d1[4], dv[4];
-                mma_f16(d1, a_lo, bf.x, bf.y, c4);
-                mma_f16(dv, a_hi, bf.z, bf.w, d1);
-                acc[q][0] = fmaf(dw.x, da.x * dv[0], acc[q][0]);
-                acc[q][1] = fmaf(dw.x, da.y * dv[1], acc[q][1]);
-                acc[q][2] = fmaf(dw.y, da.x * dv[2], acc[q][2]);
-                acc[q][3] = fmaf(dw.y, da.y * dv[3], acc[q][3]);
+            for (int q = 0; q < 2; q++) {
+                const int jb = 2 * h + q;
+                const uint32_t sc = *reinterpret_cast<const uint32_t *>(unit + 8192 + jb * 256 + g * 32 + rr * 4);
+                const __half dh = __ushort_as_half((uint16_t)(h8 ? sc >> 16 : sc & 0xFFFFu));
+                const __half2 dw = __halves2half2(dh, dh);
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    const uint32_t w =
+                        *reinterpret_cast<const uint32_t *>(unit + jb * 2048 + k4 * 512 + (g * 4 + t) * 16 + r * 4);
+                    const int chunk = q * 4 + t;   // 16-byte chunk of the 128-byte row, 128-byte swizzle
+                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ (n & 7)) * 16)) = a_word(w, dw);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor core
+            mbar_arrive(full_a + 8 * s);
+            if (h == 1 || kc == nkc - 1) mbar_arrive(uempty + 8 * us);
+        }
+        // epilogue: accumulator lane = tile row, column = token
+        const bool fin = mbar_wait(done, 0);
+        tc_fence_after();
+        const int quad = warp & 3, row = rt * TM + quad * 32 + lane;
+        if (fin) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < TN; c0 += 32) {
+                uint32_t v[32];
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                      "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                      "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+                      "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                    : "r"(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (row < P.N) {
+#pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        const int t = tok0 + c0 + i;
+                        if (t < a.T) P.y[(int64_t)t * P.y_stride + row] = __uint_as_float(v[i]);
+                    }
+                }
             }
         }
-        __syncthreads();   // stage s and fr are rewritten next
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TN) : "memory");
+}
 
-    // outputs: row = 16*warp + g (+8), token = tok0 + 8q + 2*t4 (+1)
-    const int row0 = rt * UNIT_ROWS + 16 * warp + g;
-#pragma unroll
-    for (int q = 0; q < TG; q++) {
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int row = row0 + ((i & 2) ? 8 : 0);
-            const int tok = tok0 + 8 * q + 2 * t4 + (i & 1);
-            if (row < P.N && tok < a.T) P.y[(int64_t)tok * P.y_stride + row] = acc[q][i];
-        }
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
+    return fn;
 }
 
 }  // namespace
 
+int64_t mmq_workspace_bytes(int64_t T, int64_t kmax) { return (T * kmax * 2 + 127) / 128 * 128; }
+
+qk_status read_mmq_faults(uint32_t *faults) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_mmq_faults, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_mmq_faults, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(QK_ERR_CUDA, "qk_device_faults: %s", cudaGetErrorString(e));
+    *faults = v;
+    return QK_OK;
+}
+
 qk_status launch_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int T, int n_proj,
-                     const qk_proj *projs, cudaStream_t s) {
+                     const qk_proj *projs, void *ws, size_t ws_bytes, cudaStream_t s) {
     MmqArgs a = {};
-    a.qs = qs;
-    a.d = d;
-    a.row_blocks = row_blocks;
     a.T = T;
     a.n_proj = n_proj;
-    int tiles = 0;
+    int tiles = 0, kmax = 0;
     for (int j = 0; j < n_proj; j++) {
         MmqProj &p = a.p[j];
         p.w = static_cast<const uint8_t *>(projs[j].w);
@@ -250,16 +354,34 @@ qk_status launch_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, in
         p.row_tiles = (int)ceil_div(p.N, UNIT_ROWS);
         p.tiles_begin = tiles;
         tiles += p.row_tiles;
+        kmax = p.K > kmax ? p.K : kmax;
     }
-    const size_t smem = 2 * sizeof(Stage) + sizeof(Frags);
+    if (!ws || ws_bytes < (size_t)mmq_workspace_bytes(T, kmax))
+        return fail(QK_ERR_WORKSPACE, "mmq: workspace %zu < %lld bytes", ws_bytes,
+                    (long long)mmq_workspace_bytes(T, kmax));
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail(QK_ERR_CUDA, "mmq: cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {(cuuint64_t)kmax, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)kmax * 2};
+    const cuuint32_t box[2] = {KC, TN}, estr[2] = {1, 1};
+    const CUresult r = enc(&a.bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QK_ERR_CUDA, "mmq: tensor map encoding failed (%d)", (int)r);
+
+    const int kb = kmax / QB;
+    const int64_t nthr = (int64_t)T * kb * 4;
+    qk_status st = launch_pdl("mmq_dequant_b", dequant_b_kernel, dim3((unsigned)ceil_div(nthr, 256)), dim3(256), 0, s,
+                              qs, d, row_blocks, T, kb, static_cast<__half *>(ws));
+    if (st != QK_OK) return st;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(mmq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmq: shared memory attribute: %s", cudaGetErrorString(e));
         configured = true;
     }
-    dim3 grid((unsigned)tiles, (unsigned)ceil_div(T, TT));
-    return launch_pdl("mmq", mmq_kernel, grid, dim3(MW * 32), smem, s, a);
+    dim3 grid((unsigned)tiles, (unsigned)ceil_div(T, TN));
+    return launch_pdl("mmq", mmq_tc_kernel, grid, dim3(THREADS), (size_t)SMEM_BYTES, s, a);
 }
 
 }  // namespace qk

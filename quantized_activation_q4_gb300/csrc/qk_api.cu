@@ -207,7 +207,11 @@ size_t qk_mmvq_workspace_bytes(int32_t n_proj, const qk_proj *projs) {
 
 qk_status qk_device_faults(uint32_t *faults) {
     REQUIRE(faults, QK_ERR_ARG, "faults is null");
-    return read_device_faults(faults);
+    uint32_t a = 0, b = 0;
+    qk_status st = read_device_faults(&a);
+    if (st == QK_OK) st = read_mmq_faults(&b);
+    *faults = a | b;
+    return st;
 }
 
 qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_proj, const qk_proj *projs,
@@ -326,8 +330,15 @@ qk_status qk_moe_plan(const int32_t *ids, int64_t rows, int32_t k, int32_t E, in
 }
 
 // ------------------------------------------------------------------ prefill
+size_t qk_mmq_workspace_bytes(int64_t T, int32_t n_proj, const qk_proj *projs) {
+    if (T < 1 || n_proj < 1 || n_proj > 8 || !projs) return 0;
+    int64_t kmax = 0;
+    for (int j = 0; j < n_proj; j++) kmax = projs[j].K > kmax ? projs[j].K : kmax;
+    return (size_t)mmq_workspace_bytes(T, kmax);
+}
+
 qk_status qk_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int64_t T, int32_t n_proj,
-                 const qk_proj *projs, qk_stream stream) {
+                 const qk_proj *projs, void *ws, size_t ws_bytes, qk_stream stream) {
     REQUIRE(qs && d && projs, QK_ERR_ARG, "null pointer");
     REQUIRE(T >= 1 && T <= INT32_MAX && row_blocks >= 1, QK_ERR_ARG, "T or row_blocks out of range");
     REQUIRE(n_proj >= 1 && n_proj <= 8, QK_ERR_UNSUPPORTED, "n_proj=%d not in 1..8", (int)n_proj);
@@ -346,7 +357,16 @@ qk_status qk_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int64_
             REQUIRE(!overlap(sy, span(projs[i].y, rows_span(T, projs[i].y_stride * 4, projs[i].N * 4))), QK_ERR_ALIAS,
                     "outputs of projections %d and %d overlap", i, j);
     }
-    return launch_mmq(qs, d, row_blocks, (int)T, n_proj, projs, (cudaStream_t)stream);
+    const size_t need = qk_mmq_workspace_bytes(T, n_proj, projs);
+    REQUIRE(ws && aligned(ws, 128), QK_ERR_WORKSPACE, "workspace null or not 128-byte aligned");
+    REQUIRE(ws_bytes >= need, QK_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+    Span sws = span(ws, need);
+    REQUIRE(!overlap(sws, sq) && !overlap(sws, sd), QK_ERR_ALIAS, "workspace overlaps the image");
+    for (int j = 0; j < n_proj; j++)
+        REQUIRE(!overlap(sws, span(projs[j].y, rows_span(T, projs[j].y_stride * 4, projs[j].N * 4))) &&
+                    !overlap(sws, span(projs[j].w, (size_t)packed_bytes(projs[j].wtype, projs[j].N, projs[j].K))),
+                QK_ERR_ALIAS, "workspace overlaps projection %d", j);
+    return launch_mmq(qs, d, row_blocks, (int)T, n_proj, projs, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -19,7 +19,7 @@ duration with the case's algorithmic bytes (or flops) per launch. Cases:
   mmvq_id_<R>   qk_mmvq_id, gate+up 2560->768 over 128 experts, top-8 of R rows (kernel mmvq_id)
   routed_<R>    the routed chain for R live rows of a 16/128 bucket: RMSNorm*w -> image, top-8 of
                 128, plan, mmvq_id gate+up (kernels rmsnorm_q8_1, topk, plan, mmvq_id)
-  mmq_qkv       qk_mmq, 3325 tokens, q/k/v          (kernel mmq)
+  mmq_qkv       qk_mmq, 3325 tokens, q/k/v          (kernels dequant_b, mmq_tc)
   quantize_q8_0 qk_quantize_q8_0, [3325, 3584]      (kernel quantize)
 """
 from __future__ import annotations
@@ -184,7 +184,10 @@ def build_case(name):
             y = torch.empty((T, N), dtype=torch.float32, device="cuda")
             keep += [w, y]
             projs.append(qk.make_proj("q4_0", w, N, K, y, N))
-        return lambda: qk.qk_mmq(qs, d, 112, T, projs), keep, {"flops": 2 * T * K * (3584 + 512 + 512)}
+        n = qk.qk_mmq_workspace_bytes(T, projs)
+        ws = torch.empty((n,), dtype=torch.uint8, device="cuda")
+        keep.append(ws)
+        return lambda: qk.qk_mmq(qs, d, 112, T, projs, ws, n), keep, {"flops": 2 * T * K * (3584 + 512 + 512)}
     raise SystemExit(f"unknown case {name!r}")
 
 

@@ -1,9 +1,14 @@
 """GPU parity: prefill contraction qk_mmq on a Q8_0 image, against the oracle.
 
-Gates as for MMVQ: NMSE <= 5e-4 against the plain definition (the pages'
-bound) and NMSE <= 1e-10 against the oracle's exact quantised path. At the
-prefill size (3325 tokens, d = 3584) the oracle computes every row of 64
-seeded random columns plus 16 full rows of each projection.
+Gate: NMSE <= 5e-4 against the plain definition (the pages' bound).
+Diagnostic against the oracle's exact quantised path: the GEMM runs on the
+tensor cores with binary16 operands (nibble - 8) * d_w and q * d_a, each
+rounded once (unit roundoff u = 2^-11), accumulated in binary32. Each product
+then carries a relative error of at most about 2u with random sign, so the
+NMSE against the exact block form is about 2u^2/3 = 1.6e-7; the test allows
+2e-6. A wrong block, scale or index gives an NMSE above 1e-3.
+At the prefill size (3325 tokens, d = 3584) the oracle computes every row of
+64 seeded random columns plus 16 full rows of each projection.
 """
 import numpy as np
 import pytest
@@ -16,7 +21,7 @@ from tests.gpu_helpers import dev, host, pack_weight
 pytestmark = pytest.mark.gpu
 
 NMSE_GATE = 5e-4
-NMSE_EXACT = 1e-10
+NMSE_EXACT = 2e-6   # binary16 operand rounding, see the module docstring
 
 
 def quantize_q8_0(x, K, rb):
@@ -37,8 +42,13 @@ def run_mmq(qs, d, rb, T, specs):
         keep.append(pw)                   # the descriptors hold raw pointers only
         outs.append(y)
         projs.append(qk.make_proj("q4_0", pw, N, K, y, N))
-    qk.qk_mmq(qs, d, rb, T, projs)
-    return [host(y) for y in outs], keep
+    n = qk.qk_mmq_workspace_bytes(T, projs)
+    ws = torch.empty((n,), dtype=torch.uint8, device="cuda")
+    keep.append(ws)
+    qk.qk_mmq(qs, d, rb, T, projs, ws, n)
+    outs = [host(y) for y in outs]
+    assert qk.qk_device_faults() == 0
+    return outs, keep
 
 
 @pytest.mark.parametrize("T,N,K,rb", [(100, 200, 384, 12), (65, 130, 160, 6), (1, 128, 128, 4), (64, 256, 256, 8),
@@ -77,8 +87,9 @@ def test_prefill_qkv_one_image_three_readers():
     Ws = [synth.q4_0_weight(4010 + i, N, K) for i, N in enumerate(shapes)]
     n0 = qk.launch_count()
     outs, _ = run_mmq(qs, d, 112, T, [(W, N, K) for W, N in zip(Ws, shapes)])
-    # weight packing launched one kernel per projection; the contraction itself is one launch
-    assert qk.launch_count() - n0 == len(shapes) + 1
+    # weight packing launched one kernel per projection; the contraction is two launches
+    # (the dequantised image, then one GEMM for the three readers)
+    assert qk.launch_count() - n0 == len(shapes) + 2
     qsh = host(qs).view(np.int8).reshape(T, -1)
     dh = host(d).view(np.uint16).reshape(T, -1)
     for i, (W, N, yg) in enumerate(zip(Ws, shapes, outs)):
