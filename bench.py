@@ -65,20 +65,21 @@ QUANT_BIG_BYTES = T * K_BIG * 4 + IMG_BIG
 
 def recorded_traffic():
     """DRAM bytes per launch of the roofline kernel from the committed ncu summary,
-    or None when the kernel sources changed since that capture."""
-    import glob
+    or None when the sources that build that kernel changed since the capture."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "mmvq_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
-    csrc = os.path.join(ROOT, "quantized_activation_q4_gb300", "csrc")
     h = hashlib.sha256()
-    for q in sorted(glob.glob(os.path.join(csrc, "*.cu"))) + sorted(glob.glob(os.path.join(csrc, "*.cuh"))):
+    for rel in rec.get("sources", []):
+        q = os.path.join(ROOT, rel)
+        if not os.path.exists(q):
+            return None
         with open(q, "rb") as f:
             h.update(os.path.basename(q).encode() + f.read())
-    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec.get("csrc_sha256") else None
+    return rec["dram_bytes_per_launch"] if rec.get("sources") and h.hexdigest() == rec.get("sources_sha256") else None
 
 
 def measured_peaks() -> dict:

@@ -16,12 +16,17 @@
 // Two kernels per call:
 //   dequant_b: the image -> B, [T][K] binary16 in the caller's workspace,
 //     once per call (it is read by every 128-row weight tile).
-//   mmq_tc: one CTA per (projection, 128-row weight tile, 256-token tile).
+//   mmq_tc: persistent, one CTA per SM, tiles of (projection, 128-row weight
+//     tile, 256-token tile) taken round-robin, tokens fastest so that the CTAs
+//     running at one time share a few weight row tiles through L2.
 //     warp 0: TMA -- the B tiles (2D tensor copies, 128-byte swizzle) and the
-//             packed weight units (bulk copies) into shared-memory rings;
+//             packed weight units (bulk copies) into shared-memory rings, with
+//             L2 prefetches of the units a few ahead;
 //     warps 2-5: turn each unit's nibbles into the swizzled f16 A tile;
-//     warp 1: allocates tensor memory and issues the MMAs (one thread), then
-//             warps 2-5 read the 128 x 256 f32 accumulator and store C.
+//     warp 1: allocates tensor memory (two 256-column accumulators) and
+//             issues the MMAs (one thread);
+//     warps 6-9: read a finished accumulator and store C while the MMAs of
+//             the next tile run into the other one.
 // Within a 32-block the K positions follow the order in which a packed
 // weight word converts (see a_word); dequant_b writes B in the same order.
 
@@ -38,10 +43,13 @@ constexpr int TM = 128;              // weight rows per CTA (MMA M)
 constexpr int TN = 256;              // tokens per CTA (MMA N)
 constexpr int KC = 64;               // K elements per stage (one 128-byte swizzle row of f16)
 constexpr int NS = 4;                // stages
-constexpr int NU = 2;                // packed-unit staging slots (a unit = 2 stages)
+constexpr int NU = 3;                // packed-unit staging slots (a unit = 2 stages)
+constexpr int PF = 6;                // units prefetched into L2 ahead of the one being loaded
 constexpr int A_TILE = TM * KC * 2;  // 16 KB
 constexpr int B_TILE = TN * KC * 2;  // 32 KB
-constexpr int THREADS = 6 * 32;
+constexpr int EPI0 = 6;              // first epilogue warp
+constexpr int THREADS = 10 * 32;
+constexpr uint32_t TMEM_COLS = 2 * TN;   // two accumulators
 constexpr uint32_t SPIN_LIMIT = 1u << 16;
 constexpr uint32_t SUSPEND_NS = 20000;
 
@@ -50,8 +58,10 @@ constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NS * A_TILE;
 constexpr int OFF_U = OFF_B + NS * B_TILE;
 constexpr int OFF_BAR = OFF_U + NU * Q4_UNIT_BYTES;
-constexpr int N_BARS = 3 * NS + 2 * NU + 1;
+// full_a[NS] full_b[NS] empty[NS] ufull[NU] uempty[NU] acc_full[2] acc_empty[2]
+constexpr int N_BARS = 3 * NS + 2 * NU + 4;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + slack to align the base to 1024
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 // instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 256, M = 128
 constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
@@ -62,13 +72,27 @@ struct MmqProj {
     const uint8_t *w;
     float *y;
     int64_t y_stride;
-    int N, K, chunks, row_tiles, tiles_begin;
+    int N, K, chunks, row_tiles, rt_begin;   // rt_begin: first global row tile
 };
 struct MmqArgs {
     CUtensorMap bmap;    // B [T][K] f16, box 64 x 256, 128-byte swizzle
-    int T, n_proj;
+    int T, n_proj, tok_tiles, tiles;
     MmqProj p[MAX_PROJ];
 };
+struct Tile {
+    int j, rt, tok0, nkc;
+};
+__device__ __forceinline__ Tile tile_of(const MmqArgs &a, int tau) {
+    Tile t;
+    const int r = tau / a.tok_tiles;
+    t.tok0 = (tau - r * a.tok_tiles) * TN;
+    int j = 0;
+    while (j + 1 < a.n_proj && r >= a.p[j + 1].rt_begin) j++;
+    t.j = j;
+    t.rt = r - a.p[j].rt_begin;
+    t.nkc = (a.p[j].K + KC - 1) / KC;
+    return t;
+}
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -101,6 +125,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar)
                  : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t mbar) {
     asm volatile(
@@ -177,15 +204,12 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t full_a = sbase + OFF_BAR, full_b = full_a + NS * 8, empty = full_b + NS * 8;
-    const uint32_t ufull = empty + NS * 8, uempty = ufull + NU * 8, done = uempty + NU * 8;
+    const uint32_t ufull = empty + NS * 8, uempty = ufull + NU * 8, acc_full = uempty + NU * 8,
+                   acc_empty = acc_full + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + N_BARS * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int j = 0;
-    while (j + 1 < a.n_proj && (int)blockIdx.x >= a.p[j + 1].tiles_begin) j++;
-    const MmqProj &P = a.p[j];
-    const int rt = blockIdx.x - P.tiles_begin, tok0 = blockIdx.y * TN;
-    const int nkc = (P.K + KC - 1) / KC;
+    const int G = gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; s++) {
@@ -197,12 +221,15 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
             mbar_init(ufull + 8 * u, 1);
             mbar_init(uempty + 8 * u, 128);
         }
-        mbar_init(done, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(acc_full + 8 * b, 1);      // the MMA commit after a tile's last stage
+            mbar_init(acc_empty + 8 * b, 128);   // the four epilogue warps
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {   // tensor memory: 256 columns x 128 lanes of f32 for the accumulator
+    if (warp == 1) {   // tensor memory: 2 x 256 columns x 128 lanes of f32
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(TN)
+                     "r"(TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -215,72 +242,128 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
 
     if (warp == 0) {   // ---------------- producer
         if (lane == 0) {
-            const uint8_t *units = P.w + (int64_t)rt * P.chunks * Q4_UNIT_BYTES;
-            for (int kc = 0; kc < nkc; kc++) {
-                const int s = kc % NS;
-                if ((kc & 1) == 0) {   // a packed unit covers two stages
-                    const int u = kc >> 1, us = u % NU;
-                    if (u >= NU && !mbar_wait(uempty + 8 * us, ((u / NU) - 1) & 1u)) break;
-                    mbar_expect_tx(ufull + 8 * us, Q4_UNIT_BYTES);
-                    bulk_g2s(sbase + OFF_U + us * Q4_UNIT_BYTES, units + (int64_t)u * Q4_UNIT_BYTES, Q4_UNIT_BYTES,
-                             ufull + 8 * us);
+            uint32_t g = 0, gu = 0;   // stages and units issued by this CTA
+            bool ok = true;
+            {   // L2 prefetch of the first tile's leading units
+                const Tile t = tile_of(a, blockIdx.x < a.tiles ? blockIdx.x : 0);
+                const MmqProj &P = a.p[t.j];
+                const uint8_t *units = P.w + (int64_t)t.rt * P.chunks * Q4_UNIT_BYTES;
+                for (int u = 0; u < PF && u < P.chunks && (int)blockIdx.x < a.tiles; u++)
+                    prefetch_l2(units + (int64_t)u * Q4_UNIT_BYTES, Q4_UNIT_BYTES);
+            }
+            for (int tau = blockIdx.x; tau < a.tiles && ok; tau += G) {
+                const Tile t = tile_of(a, tau);
+                const MmqProj &P = a.p[t.j];
+                const uint8_t *units = P.w + (int64_t)t.rt * P.chunks * Q4_UNIT_BYTES;
+                for (int kc = 0; kc < t.nkc; kc++, g++) {
+                    const uint32_t s = g % NS;
+                    if ((kc & 1) == 0) {   // a packed unit covers two stages
+                        const int u = kc >> 1;
+                        const uint32_t us = gu % NU;
+                        if (gu >= NU && !mbar_wait(uempty + 8 * us, ((gu / NU) - 1) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(ufull + 8 * us, Q4_UNIT_BYTES);
+                        bulk_g2s(sbase + OFF_U + us * Q4_UNIT_BYTES, units + (int64_t)u * Q4_UNIT_BYTES,
+                                 Q4_UNIT_BYTES, ufull + 8 * us);
+                        gu++;
+                        // keep the unit PF ahead (in this tile or the next one) on its way into L2
+                        if (u + PF < P.chunks) {
+                            prefetch_l2(units + (int64_t)(u + PF) * Q4_UNIT_BYTES, Q4_UNIT_BYTES);
+                        } else if (tau + G < a.tiles) {
+                            const Tile n = tile_of(a, tau + G);
+                            const MmqProj &Q = a.p[n.j];
+                            const int un = u + PF - P.chunks;
+                            if (un < Q.chunks)
+                                prefetch_l2(Q.w + ((int64_t)n.rt * Q.chunks + un) * Q4_UNIT_BYTES, Q4_UNIT_BYTES);
+                        }
+                    }
+                    if (g >= NS && !mbar_wait(empty + 8 * s, ((g / NS) - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_b + 8 * s, B_TILE);
+                    tma_2d(sbase + OFF_B + s * B_TILE, &a.bmap, kc * KC, t.tok0, full_b + 8 * s);
                 }
-                if (kc >= NS && !mbar_wait(empty + 8 * s, ((kc / NS) - 1) & 1u)) break;
-                mbar_expect_tx(full_b + 8 * s, B_TILE);
-                tma_2d(sbase + OFF_B + s * B_TILE, &a.bmap, kc * KC, tok0, full_b + 8 * s);
             }
         }
     } else if (warp == 1) {   // ---------------- MMA issue (one thread)
         if (lane == 0) {
-            for (int kc = 0; kc < nkc; kc++) {
-                const int s = kc % NS;
-                const uint32_t par = (kc / NS) & 1u;
-                if (!mbar_wait(full_a + 8 * s, par) || !mbar_wait(full_b + 8 * s, par)) break;
+            uint32_t g = 0;
+            int i = 0;
+            bool ok = true;
+            for (int tau = blockIdx.x; tau < a.tiles && ok; tau += G, i++) {
+                const Tile t = tile_of(a, tau);
+                const uint32_t ab = i & 1, acc = tmem + ab * TN;
+                if (i >= 2 && !mbar_wait(acc_empty + 8 * ab, ((i >> 1) - 1) & 1u)) break;
                 tc_fence_after();
-                const uint32_t at = sbase + OFF_A + s * A_TILE, bt = sbase + OFF_B + s * B_TILE;
+                for (int kc = 0; kc < t.nkc; kc++, g++) {
+                    const uint32_t s = g % NS, par = (g / NS) & 1u;
+                    if (!mbar_wait(full_a + 8 * s, par) || !mbar_wait(full_b + 8 * s, par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t at = sbase + OFF_A + s * A_TILE, bt = sbase + OFF_B + s * B_TILE;
 #pragma unroll
-                for (int ks = 0; ks < KC / 16; ks++)   // 16 f16 = 32 bytes along K per MMA
-                    tc_mma(tmem, sdesc(at + 32 * ks), sdesc(bt + 32 * ks), (kc | ks) != 0);
-                tc_commit(empty + 8 * s);   // frees the stage once these MMAs are done
+                    for (int ks = 0; ks < KC / 16; ks++)   // 16 f16 = 32 bytes along K per MMA
+                        tc_mma(acc, sdesc(at + 32 * ks), sdesc(bt + 32 * ks), (kc | ks) != 0);
+                    tc_commit(empty + 8 * s);   // frees the stage once these MMAs are done
+                }
+                if (ok) tc_commit(acc_full + 8 * ab);   // the accumulator is final once its MMAs are done
             }
-            tc_commit(done);                // the accumulator is final once every MMA issued is done
         }
-    } else {   // ---------------- warps 2..5: A conversion, then the epilogue
+    } else if (warp < EPI0) {   // ---------------- warps 2..5: A conversion
         // Tile row n: in the packed unit, row 32 k4 + {g, g+8, 16+g, 24+g}[r] of region k4, lane
         // group g, word slot r; its scale is half h8 of word g*8.. of row group rr (rows 16rr+g, +8).
         const int n = threadIdx.x - 64;
-        const int g = n & 7, r = (n >> 3) & 3, k4 = n >> 5, rr = n >> 4, h8 = (n >> 3) & 1;
+        const int g8 = n & 7, r = (n >> 3) & 3, k4 = n >> 5, rr = n >> 4, h8 = (n >> 3) & 1;
+        uint32_t g = 0, gu = 0;
         bool ok = true;
-        for (int kc = 0; kc < nkc; kc++) {
-            const int s = kc % NS, u = kc >> 1, us = u % NU, h = kc & 1;
-            if (h == 0) ok = mbar_wait(ufull + 8 * us, (u / NU) & 1u);
-            if (ok && kc >= NS) ok = mbar_wait(empty + 8 * s, ((kc / NS) - 1) & 1u);
-            if (!ok) break;
-            const uint8_t *unit = smem + OFF_U + us * Q4_UNIT_BYTES;
-            uint8_t *arow = smem + OFF_A + s * A_TILE + n * 128;
+        for (int tau = blockIdx.x; tau < a.tiles && ok; tau += G) {
+            const Tile t = tile_of(a, tau);
+            for (int kc = 0; kc < t.nkc; kc++, g++) {
+                const uint32_t s = g % NS, us = gu % NU;
+                const int h = kc & 1;
+                if (h == 0) ok = mbar_wait(ufull + 8 * us, (gu / NU) & 1u);
+                if (ok && g >= NS) ok = mbar_wait(empty + 8 * s, ((g / NS) - 1) & 1u);
+                if (!ok) break;
+                const uint8_t *unit = smem + OFF_U + us * Q4_UNIT_BYTES;
+                uint8_t *arow = smem + OFF_A + s * A_TILE + n * 128;
 #pragma unroll
-            for (int q = 0; q < 2; q++) {
-                const int jb = 2 * h + q;
-                const uint32_t sc = *reinterpret_cast<const uint32_t *>(unit + 8192 + jb * 256 + g * 32 + rr * 4);
-                const __half dh = __ushort_as_half((uint16_t)(h8 ? sc >> 16 : sc & 0xFFFFu));
-                const __half2 dw = __halves2half2(dh, dh);
+                for (int q = 0; q < 2; q++) {
+                    const int jb = 2 * h + q;
+                    const uint32_t sc =
+                        *reinterpret_cast<const uint32_t *>(unit + 8192 + jb * 256 + g8 * 32 + rr * 4);
+                    const __half dh = __ushort_as_half((uint16_t)(h8 ? sc >> 16 : sc & 0xFFFFu));
+                    const __half2 dw = __halves2half2(dh, dh);
 #pragma unroll
-                for (int t = 0; t < 4; t++) {
-                    const uint32_t w =
-                        *reinterpret_cast<const uint32_t *>(unit + jb * 2048 + k4 * 512 + (g * 4 + t) * 16 + r * 4);
-                    const int chunk = q * 4 + t;   // 16-byte chunk of the 128-byte row, 128-byte swizzle
-                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ (n & 7)) * 16)) = a_word(w, dw);
+                    for (int tw = 0; tw < 4; tw++) {
+                        const uint32_t w = *reinterpret_cast<const uint32_t *>(unit + jb * 2048 + k4 * 512 +
+                                                                               (g8 * 4 + tw) * 16 + r * 4);
+                        const int chunk = q * 4 + tw;   // 16-byte chunk of the 128-byte row, 128-byte swizzle
+                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (n & 7)) * 16)) = a_word(w, dw);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor core
+                mbar_arrive(full_a + 8 * s);
+                if (h == 1 || kc == t.nkc - 1) {
+                    mbar_arrive(uempty + 8 * us);
+                    gu++;
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor core
-            mbar_arrive(full_a + 8 * s);
-            if (h == 1 || kc == nkc - 1) mbar_arrive(uempty + 8 * us);
         }
-        // epilogue: accumulator lane = tile row, column = token
-        const bool fin = mbar_wait(done, 0);
-        tc_fence_after();
-        const int quad = warp & 3, row = rt * TM + quad * 32 + lane;
-        if (fin) {
+    } else {   // ---------------- warps 6..9: epilogue (accumulator lane = tile row, column = token)
+        const int quad = warp & 3;
+        int i = 0;
+        for (int tau = blockIdx.x; tau < a.tiles; tau += G, i++) {
+            const Tile t = tile_of(a, tau);
+            const MmqProj &P = a.p[t.j];
+            const uint32_t ab = i & 1;
+            if (!mbar_wait(acc_full + 8 * ab, (i >> 1) & 1u)) break;
+            tc_fence_after();
+            const int row = t.rt * TM + quad * 32 + lane;
 #pragma unroll 1
             for (int c0 = 0; c0 < TN; c0 += 32) {
                 uint32_t v[32];
@@ -292,23 +375,26 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                       "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
                       "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
                       "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                    : "r"(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0));
+                    : "r"(tmem + ((uint32_t)(quad * 32) << 16) + ab * TN + (uint32_t)c0));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 if (row < P.N) {
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        const int t = tok0 + c0 + i;
-                        if (t < a.T) P.y[(int64_t)t * P.y_stride + row] = __uint_as_float(v[i]);
+                    for (int k = 0; k < 32; k++) {
+                        const int tok = t.tok0 + c0 + k;
+                        if (tok < a.T) P.y[(int64_t)tok * P.y_stride + row] = __uint_as_float(v[k]);
                     }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(acc_empty + 8 * ab);
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TN) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                     : "memory");
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -342,7 +428,7 @@ qk_status launch_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, in
     MmqArgs a = {};
     a.T = T;
     a.n_proj = n_proj;
-    int tiles = 0, kmax = 0;
+    int rtiles = 0, kmax = 0;
     for (int j = 0; j < n_proj; j++) {
         MmqProj &p = a.p[j];
         p.w = static_cast<const uint8_t *>(projs[j].w);
@@ -352,8 +438,8 @@ qk_status launch_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, in
         p.K = (int)projs[j].K;
         p.chunks = (int)ceil_div(p.K, UNIT_COLS);
         p.row_tiles = (int)ceil_div(p.N, UNIT_ROWS);
-        p.tiles_begin = tiles;
-        tiles += p.row_tiles;
+        p.rt_begin = rtiles;
+        rtiles += p.row_tiles;
         kmax = p.K > kmax ? p.K : kmax;
     }
     if (!ws || ws_bytes < (size_t)mmq_workspace_bytes(T, kmax))
@@ -380,8 +466,10 @@ qk_status launch_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, in
         if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmq: shared memory attribute: %s", cudaGetErrorString(e));
         configured = true;
     }
-    dim3 grid((unsigned)tiles, (unsigned)ceil_div(T, TN));
-    return launch_pdl("mmq", mmq_tc_kernel, grid, dim3(THREADS), (size_t)SMEM_BYTES, s, a);
+    a.tok_tiles = (int)ceil_div(T, TN);
+    a.tiles = rtiles * a.tok_tiles;
+    const int grid = a.tiles < sm_count() ? a.tiles : sm_count();
+    return launch_pdl("mmq", mmq_tc_kernel, dim3((unsigned)grid), dim3(THREADS), (size_t)SMEM_BYTES, s, a);
 }
 
 }  // namespace qk

@@ -984,6 +984,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ s
     }
 }
 
+}  // namespace
+
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -994,6 +996,8 @@ int sm_count() {
     }
     return n;
 }
+
+namespace {
 
 template <int WT>
 size_t sk_smem() {

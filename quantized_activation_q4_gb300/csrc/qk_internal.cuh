@@ -77,6 +77,9 @@ inline int64_t packed_bytes(int wtype, int64_t N, int64_t K) {
     return ceil_div(N, UNIT_ROWS) * ceil_div(K, UNIT_COLS) * unit_bytes(wtype);
 }
 
+// Streaming multiprocessors of the current device (cached after the first call).
+int sm_count();
+
 // Reads and clears the device-side fault word (bit 0: a bounded mbarrier
 // wait gave up). Synchronous.
 qk_status read_device_faults(uint32_t *faults);
