@@ -17,15 +17,18 @@
 //   dequant_b: the image -> B, [T][K] binary16 in the caller's workspace,
 //     once per call (it is read by every 128-row weight tile).
 //   mmq_tc: persistent, one CTA per SM, tiles of (projection, 128-row weight
-//     tile, 256-token tile) taken round-robin, tokens fastest so that the CTAs
+//     tile, 192-token tile) taken round-robin, tokens fastest so that the CTAs
 //     running at one time share a few weight row tiles through L2.
 //     warp 0: TMA -- the B tiles (2D tensor copies, 128-byte swizzle) and the
 //             packed weight units (bulk copies) into shared-memory rings, with
 //             L2 prefetches of the units a few ahead;
-//     warps 2-5: turn each unit's nibbles into the swizzled f16 A tile;
-//     warp 1: allocates tensor memory (two 256-column accumulators) and
-//             issues the MMAs (one thread);
-//     warps 6-9: read a finished accumulator and store C while the MMAs of
+//     warps 2-9: turn each unit's nibbles into f16 A stages held in tensor
+//             memory (tcgen05.st; two warps per 32-lane quarter, one 32-block
+//             each), so the MMAs read A from tensor memory and only B from
+//             shared memory;
+//     warp 1: allocates tensor memory (two 192-column accumulators and four
+//             32-column A stages) and issues the MMAs (one thread);
+//     warps 10-13: read a finished accumulator and store C while the MMAs of
 //             the next tile run into the other one.
 // Within a 32-block the K positions follow the order in which a packed
 // weight word converts (see a_word); dequant_b writes B in the same order.
@@ -40,22 +43,23 @@ namespace {
 
 constexpr int MAX_PROJ = 8;
 constexpr int TM = 128;              // weight rows per CTA (MMA M)
-constexpr int TN = 256;              // tokens per CTA (MMA N)
+constexpr int TN = 192;              // tokens per CTA (MMA N)
 constexpr int KC = 64;               // K elements per stage (one 128-byte swizzle row of f16)
-constexpr int NS = 4;                // stages
+constexpr int NS = 4;                // stages (A in tensor memory, B in shared memory)
 constexpr int NU = 3;                // packed-unit staging slots (a unit = 2 stages)
 constexpr int PF = 6;                // units prefetched into L2 ahead of the one being loaded
-constexpr int A_TILE = TM * KC * 2;  // 16 KB
-constexpr int B_TILE = TN * KC * 2;  // 32 KB
-constexpr int EPI0 = 6;              // first epilogue warp
-constexpr int THREADS = 10 * 32;
-constexpr uint32_t TMEM_COLS = 2 * TN;   // two accumulators
+constexpr int B_TILE = TN * KC * 2;  // 24 KB
+constexpr uint32_t A_COLS = KC / 2;  // tensor-memory columns of one A stage (two f16 per column)
+constexpr int EPI0 = 10;             // first epilogue warp
+constexpr int THREADS = 14 * 32;
+constexpr uint32_t A_TMEM = 2 * TN;       // A stages follow the two accumulators
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(A_TMEM + NS * A_COLS <= TMEM_COLS, "tensor memory");
 constexpr uint32_t SPIN_LIMIT = 1u << 16;
 constexpr uint32_t SUSPEND_NS = 20000;
 
-// shared memory: [A tiles][B tiles][units][barriers][tensor-memory address]
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + NS * A_TILE;
+// shared memory: [B tiles][units][barriers][tensor-memory address]
+constexpr int OFF_B = 0;
 constexpr int OFF_U = OFF_B + NS * B_TILE;
 constexpr int OFF_BAR = OFF_U + NU * Q4_UNIT_BYTES;
 // full_a[NS] full_b[NS] empty[NS] ufull[NU] uempty[NU] acc_full[2] acc_empty[2]
@@ -63,7 +67,7 @@ constexpr int N_BARS = 3 * NS + 2 * NU + 4;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + slack to align the base to 1024
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
-// instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 256, M = 128
+// instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 192, M = 128
 constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
 
 __device__ unsigned int g_mmq_faults = 0;
@@ -75,7 +79,7 @@ struct MmqProj {
     int N, K, chunks, row_tiles, rt_begin;   // rt_begin: first global row tile
 };
 struct MmqArgs {
-    CUtensorMap bmap;    // B [T][K] f16, box 64 x 256, 128-byte swizzle
+    CUtensorMap bmap;    // B [T][K] f16, box 64 x 192, 128-byte swizzle
     int T, n_proj, tok_tiles, tiles;
     MmqProj p[MAX_PROJ];
 };
@@ -140,11 +144,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
     return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
            (2ull << 61);
 }
-__device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+// D (tensor memory) (+)= A (tensor memory) x B (shared memory)
+__device__ __forceinline__ void tc_mma(uint32_t tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
-        "l"(a), "l"(b), "r"(IDESC), "r"(accumulate)
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem),
+        "r"(a_tmem), "l"(b), "r"(IDESC), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint32_t mbar) {
@@ -213,13 +218,13 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; s++) {
-            mbar_init(full_a + 8 * s, 128);   // the four converter warps
+            mbar_init(full_a + 8 * s, 256);   // the eight converter warps
             mbar_init(full_b + 8 * s, 1);     // the producer, with the bytes
             mbar_init(empty + 8 * s, 1);      // the MMA commit
         }
         for (int u = 0; u < NU; u++) {
             mbar_init(ufull + 8 * u, 1);
-            mbar_init(uempty + 8 * u, 128);
+            mbar_init(uempty + 8 * u, 256);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(acc_full + 8 * b, 1);      // the MMA commit after a tile's last stage
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {   // tensor memory: 2 x 256 columns x 128 lanes of f32
+    if (warp == 1) {   // tensor memory: accumulators (2 x 192 columns) and A stages (4 x 32 columns)
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
                      : "memory");
@@ -305,20 +310,22 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t at = sbase + OFF_A + s * A_TILE, bt = sbase + OFF_B + s * B_TILE;
+                    const uint32_t at = tmem + A_TMEM + s * A_COLS, bt = sbase + OFF_B + s * B_TILE;
 #pragma unroll
-                    for (int ks = 0; ks < KC / 16; ks++)   // 16 f16 = 32 bytes along K per MMA
-                        tc_mma(acc, sdesc(at + 32 * ks), sdesc(bt + 32 * ks), (kc | ks) != 0);
+                    for (int ks = 0; ks < KC / 16; ks++)   // K = 16 per MMA: 8 A columns, 32 B bytes
+                        tc_mma(acc, at + 8 * ks, sdesc(bt + 32 * ks), (kc | ks) != 0);
                     tc_commit(empty + 8 * s);   // frees the stage once these MMAs are done
                 }
                 if (ok) tc_commit(acc_full + 8 * ab);   // the accumulator is final once its MMAs are done
             }
         }
-    } else if (warp < EPI0) {   // ---------------- warps 2..5: A conversion
-        // Tile row n: in the packed unit, row 32 k4 + {g, g+8, 16+g, 24+g}[r] of region k4, lane
-        // group g, word slot r; its scale is half h8 of word g*8.. of row group rr (rows 16rr+g, +8).
-        const int n = threadIdx.x - 64;
+    } else if (warp < EPI0) {   // ---------------- warps 2..9: A conversion into tensor memory
+        // A warp may only touch tensor-memory lanes 32 (warp % 4) .. +31, so tile row n = 32 (warp % 4) + lane.
+        // In the packed unit, row n is row {g, g+8, 16+g, 24+g}[r] of region k4, lane group g, word
+        // slot r; its scale is half h8 of word g*8.. of row group rr (rows 16rr+g, +8).
+        const int quad = warp & 3, n = 32 * quad + lane, qb = (warp - 2) >> 2;   // qb: block of the stage
         const int g8 = n & 7, r = (n >> 3) & 3, k4 = n >> 5, rr = n >> 4, h8 = (n >> 3) & 1;
+        const uint32_t arow = tmem + ((uint32_t)(32 * quad) << 16) + A_TMEM;
         uint32_t g = 0, gu = 0;
         bool ok = true;
         for (int tau = blockIdx.x; tau < a.tiles && ok; tau += G) {
@@ -329,11 +336,11 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                 if (h == 0) ok = mbar_wait(ufull + 8 * us, (gu / NU) & 1u);
                 if (ok && g >= NS) ok = mbar_wait(empty + 8 * s, ((g / NS) - 1) & 1u);
                 if (!ok) break;
+                tc_fence_after();
                 const uint8_t *unit = smem + OFF_U + us * Q4_UNIT_BYTES;
-                uint8_t *arow = smem + OFF_A + s * A_TILE + n * 128;
-#pragma unroll
-                for (int q = 0; q < 2; q++) {
-                    const int jb = 2 * h + q;
+                uint32_t v[16];   // column c: K positions 2c, 2c+1 of this block (a_word order)
+                {
+                    const int jb = 2 * h + qb;
                     const uint32_t sc =
                         *reinterpret_cast<const uint32_t *>(unit + 8192 + jb * 256 + g8 * 32 + rr * 4);
                     const __half dh = __ushort_as_half((uint16_t)(h8 ? sc >> 16 : sc & 0xFFFFu));
@@ -342,11 +349,21 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                     for (int tw = 0; tw < 4; tw++) {
                         const uint32_t w = *reinterpret_cast<const uint32_t *>(unit + jb * 2048 + k4 * 512 +
                                                                                (g8 * 4 + tw) * 16 + r * 4);
-                        const int chunk = q * 4 + tw;   // 16-byte chunk of the 128-byte row, 128-byte swizzle
-                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (n & 7)) * 16)) = a_word(w, dw);
+                        const uint4 x = a_word(w, dw);
+                        v[4 * tw + 0] = x.x;
+                        v[4 * tw + 1] = x.y;
+                        v[4 * tw + 2] = x.z;
+                        v[4 * tw + 3] = x.w;
                     }
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor core
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+                    "%15,%16};" ::"r"(arow + s * A_COLS + 16 * qb),
+                    "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+                    "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                    : "memory");
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
                 mbar_arrive(full_a + 8 * s);
                 if (h == 1 || kc == t.nkc - 1) {
                     mbar_arrive(uempty + 8 * us);
@@ -354,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                 }
             }
         }
-    } else {   // ---------------- warps 6..9: epilogue (accumulator lane = tile row, column = token)
+    } else {   // ---------------- warps 10..13: epilogue (accumulator lane = tile row, column = token)
         const int quad = warp & 3;
         int i = 0;
         for (int tau = blockIdx.x; tau < a.tiles; tau += G, i++) {
