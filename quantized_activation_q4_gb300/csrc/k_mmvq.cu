@@ -783,20 +783,27 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------- routed path
-// One CTA per (projection, expert, 128-row tile); experts with no planned pair
-// return at once and read no weights. A live tile streams its 128x128 units
-// with TMA bulk copies into a small ring (a producer warp), and 8 consumer
-// warps take the blocks: warp w does block w & 3 of the units with index
-// = w >> 2 mod 2, for all 128 rows and up to 8 planned pairs at a time (more
-// pairs re-run the pass; the weights then come from L2). The warps' partial
-// sums are added in fixed warp order, so a row's bits depend neither on the
-// other rows routed with it nor on the live count.
+// Persistent CTAs over equal work items: (live expert, pass of up to 8 of its
+// planned pairs, projection, 128-row tile). Every CTA first lists the experts
+// with planned pairs in ascending order, with the prefix of their pass counts
+// (the same lists in every CTA), so experts without pairs form no item and
+// none of their weights is read, the grid is sized once for the resident CTAs
+// whatever the live count, and round-robin over items of one size balances the
+// CTAs. A CTA streams its items' 128x128 units with TMA bulk copies into a
+// small ring (a producer warp), and RW consumer warps take the blocks: warp w
+// does block w & 3 of the units with index = w >> 2 mod RW/4, for all 128 rows
+// and the item's pairs. An item takes a whole number of RW/4 ring positions (a
+// dummy position completes its slot without a copy), so unit u of an item
+// always meets the same warps. The warps' partial sums are added in fixed warp
+// order, so a row's bits depend neither on the other rows routed with it, nor
+// on the live count, nor on the CTA.
 constexpr int RW = 8;
 constexpr int ID_PAR = RW / 4;   // units in work at once
 constexpr int ID_THREADS = (RW + 1) * 32;
+constexpr int ID_MAX_E = 1024;
 
 template <int WT> struct IdLayout;
-// Slot s is reused by unit s + SLOTS, which must belong to the same warps
+// Slot s is reused by position s + SLOTS, which must belong to the same warps
 // (units in work at once divide SLOTS): a waiter two phases ahead would see
 // the barrier's parity alias and pass early.
 template <> struct IdLayout<QK_W_Q4_0> { static constexpr int SLOTS = 6; };
@@ -808,12 +815,12 @@ struct IdProj {
     const uint8_t *w;
     float *y;
     int64_t expert_bytes;
-    int N, K, chunks, row_tiles, tiles_begin;
+    int N, K, chunks, row_tiles, tiles_begin;   // tiles_begin: first tile of this projection within an expert
 };
 struct IdArgs {
     const uint8_t *img;
     int64_t img_row_bytes;
-    int rows, k, n_proj;
+    int rows, k, n_proj, E, tiles_per_expert;
     const int32_t *counts, *offsets, *items;
     IdProj p[MAX_PROJ];
 };
@@ -821,36 +828,49 @@ struct IdArgs {
 template <int WT>
 size_t id_smem() {
     return (size_t)IdLayout<WT>::SLOTS * Layout<WT>::UNIT + (size_t)RW * VALS * sizeof(float) +
-           2 * IdLayout<WT>::SLOTS * sizeof(uint64_t);
+           2 * IdLayout<WT>::SLOTS * sizeof(uint64_t) + (2 * ID_MAX_E + 1) * sizeof(int32_t);
 }
 
 __device__ __forceinline__ void id_consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(RW * 32) : "memory");
 }
 
+struct IdItem {
+    int e, pass, j, rt;
+};
+// Item it = (global pass index) * tiles_per_expert + tile; pass_pre[l] is the
+// first global pass index of live expert l (pass_pre[n_live] = all passes).
+__device__ __forceinline__ IdItem id_item(const IdArgs &a, const int32_t *live_e, const int32_t *pass_pre,
+                                          int n_live, int it) {
+    IdItem r;
+    const int gp = it / a.tiles_per_expert, q = it - gp * a.tiles_per_expert;
+    int lo = 0, hi = n_live - 1;   // the last l with pass_pre[l] <= gp
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pass_pre[mid] <= gp) lo = mid;
+        else hi = mid - 1;
+    }
+    int j = 0;
+    while (j + 1 < a.n_proj && q >= a.p[j + 1].tiles_begin) j++;
+    r.e = live_e[lo];
+    r.pass = gp - pass_pre[lo];
+    r.j = j;
+    r.rt = q - a.p[j].tiles_begin;
+    return r;
+}
+
 template <int WT>
-__global__ void __launch_bounds__(ID_THREADS) mmvq_id_kernel(const __grid_constant__ IdArgs a) {
+__global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_constant__ IdArgs a) {
     using L = Layout<WT>;
     constexpr int SLOTS = IdLayout<WT>::SLOTS;
     extern __shared__ __align__(128) uint8_t smem[];
     float *red = reinterpret_cast<float *>(smem + SLOTS * L::UNIT);   // [RW][VALS]
     uint64_t *full = reinterpret_cast<uint64_t *>(red + RW * VALS);
     uint64_t *empty = full + SLOTS;
-    __shared__ int tok_img[8], tok_out[8];
-    pdl_trigger();
-    pdl_wait();   // counts, offsets and items come from the plan kernel
-    const int tile = blockIdx.x;
-    int j = 0;
-    while (j + 1 < a.n_proj && tile >= a.p[j + 1].tiles_begin) j++;
-    const IdProj &P = a.p[j];
-    const int local = tile - P.tiles_begin;
-    const int e = local / P.row_tiles, rt = local % P.row_tiles;
-    const int n_items = __ldg(a.counts + e);
-    if (n_items <= 0) return;   // no planned pair: no weights read
-    const int item0 = __ldg(a.offsets + e);
-    const uint8_t *wbase = P.w + (int64_t)e * P.expert_bytes + (int64_t)rt * P.chunks * L::UNIT;
+    int32_t *live_e = reinterpret_cast<int32_t *>(empty + SLOTS);   // [ID_MAX_E]
+    int32_t *pass_pre = live_e + ID_MAX_E;                            // [ID_MAX_E + 1]
+    __shared__ int tok_img[8], tok_out[8], w_live[RW + 1], w_pass[RW + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t4 = lane & 3, g = lane >> 2;
-    const int Kb = P.K / QB, chunks = P.chunks, passes = (n_items + 7) / 8;
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; s++) {
             mbar_init(smem_addr(full + s), 1);
@@ -858,19 +878,90 @@ __global__ void __launch_bounds__(ID_THREADS) mmvq_id_kernel(const __grid_consta
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    pdl_trigger();
+    pdl_wait();   // counts, offsets and items come from the plan kernel
+    // The experts with planned pairs, ascending, and the prefix of their pass counts. Warp w
+    // takes a contiguous run of 32-expert chunks: it counts its run, the runs are prefixed over
+    // warps, and the run is walked again to write its entries.
+    const int nch = (a.E + 31) / 32, cpw = (nch + RW) / (RW + 1);
+    const int c_begin = warp * cpw, c_end = min(nch, c_begin + cpw);
+    const unsigned lt = (1u << lane) - 1u;
+    auto expert_at = [&](int c, int &e, int &passes) {
+        e = 32 * c + lane;
+        const int cnt = e < a.E ? __ldg(a.counts + e) : 0;
+        passes = cnt > 0 ? (cnt + 7) / 8 : 0;
+    };
+    {
+        int nl = 0, np = 0;
+        for (int c = c_begin; c < c_end; c++) {
+            int e, ps;
+            expert_at(c, e, ps);
+            nl += __popc(__ballot_sync(0xffffffffu, ps > 0));
+            np += (int)__reduce_add_sync(0xffffffffu, (unsigned)ps);
+        }
+        if (lane == 0) {
+            w_live[warp] = nl;
+            w_pass[warp] = np;
+        }
+    }
     __syncthreads();
+    {
+        int bl = 0, bp = 0;
+        for (int w = 0; w < warp; w++) {
+            bl += w_live[w];
+            bp += w_pass[w];
+        }
+        for (int c = c_begin; c < c_end; c++) {
+            int e, ps;
+            expert_at(c, e, ps);
+            const unsigned m = __ballot_sync(0xffffffffu, ps > 0);
+            int incl = ps;   // inclusive scan of the pass counts over the lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (ps > 0) {
+                const int l = bl + __popc(m & lt);
+                live_e[l] = e;
+                pass_pre[l] = bp + incl - ps;
+            }
+            bl += __popc(m);
+            bp += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (warp == RW && lane == 0) pass_pre[bl] = bp;   // the last warp's run ends the list
+    }
+    __syncthreads();
+    int n_live = 0;
+    for (int w = 0; w <= RW; w++) n_live += w_live[w];
+    const int n_work = (n_live > 0 ? pass_pre[n_live] : 0) * a.tiles_per_expert, G = gridDim.x;
     const uint32_t ring = smem_addr(smem);
 
     if (warp == RW) {   // ---------------- producer
         if (lane == 0) {
             const uint64_t pol = evict_first_policy();
-            for (int s = 0; s < passes * chunks; s++) {
-                const int slot = s % SLOTS;
-                const uint32_t n = (uint32_t)s / SLOTS;
-                if (n > 0 && !mbar_wait(smem_addr(empty + slot), (n - 1) & 1u)) break;
-                mbar_expect_tx(smem_addr(full + slot), L::UNIT);
-                bulk_g2s(ring + (uint32_t)slot * L::UNIT, wbase + (int64_t)(s % chunks) * L::UNIT, L::UNIT,
-                         smem_addr(full + slot), pol);
+            uint32_t pos = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_work && ok; it += G) {
+                const IdItem w = id_item(a, live_e, pass_pre, n_live, it);
+                const IdProj &P = a.p[w.j];
+                const int pp = (P.chunks + ID_PAR - 1) / ID_PAR * ID_PAR;
+                const uint8_t *wbase = P.w + (int64_t)w.e * P.expert_bytes + (int64_t)w.rt * P.chunks * L::UNIT;
+                for (int u = 0; u < pp && ok; u++, pos++) {
+                    const int slot = pos % SLOTS;
+                    const uint32_t n = pos / SLOTS;
+                    if (n > 0 && !mbar_wait(smem_addr(empty + slot), (n - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (u < P.chunks) {
+                        mbar_expect_tx(smem_addr(full + slot), L::UNIT);
+                        bulk_g2s(ring + (uint32_t)slot * L::UNIT, wbase + (int64_t)u * L::UNIT, L::UNIT,
+                                 smem_addr(full + slot), pol);
+                    } else {
+                        mbar_arrive(smem_addr(full + slot));   // dummy position: completes the phase
+                    }
+                }
             }
         }
         return;
@@ -879,58 +970,70 @@ __global__ void __launch_bounds__(ID_THREADS) mmvq_id_kernel(const __grid_consta
     // ---------------- consumers
     bool ok = true;
     const int jb = warp & 3, par = warp >> 2;
-    for (int pass = 0; pass < passes; pass++) {
-        if (threadIdx.x < 8) {
-            const int idx = pass * 8 + threadIdx.x;
-            int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
-            if (p < 0 || p / a.k >= a.rows) p = -1;   // not a pair of this bucket: skip
-            tok_img[threadIdx.x] = p >= 0 ? p / a.k : -1;
-            tok_out[threadIdx.x] = p;
-        }
-        id_consumers_sync();
-        const int rB = tok_img[g], rS0 = tok_img[2 * t4], rS1 = tok_img[2 * t4 + 1];
-        const uint8_t *imgB = rB >= 0 ? a.img + (int64_t)rB * a.img_row_bytes : nullptr;
-        const uint8_t *imgS0 = rS0 >= 0 ? a.img + (int64_t)rS0 * a.img_row_bytes : nullptr;
-        const uint8_t *imgS1 = rS1 >= 0 ? a.img + (int64_t)rS1 * a.img_row_bytes : nullptr;
-        float acc[UNIT_GROUPS][4];
-#pragma unroll
-        for (int r = 0; r < UNIT_GROUPS; r++)
-#pragma unroll
-            for (int i = 0; i < 4; i++) acc[r][i] = 0.0f;
-        // this warp's units: u = par mod ID_PAR; the image words one unit ahead
-        int u = par;
-        Raw next = {0u, 0u, 0u, 0u};
-        if (u < chunks && 4 * u + jb < Kb) next = load_raw(imgB, imgS0, imgS1, 4 * u + jb, t4);
-        for (; u < chunks; u += ID_PAR) {
-            const Raw cur = next;
-            if (u + ID_PAR < chunks && 4 * (u + ID_PAR) + jb < Kb)
-                next = load_raw(imgB, imgS0, imgS1, 4 * (u + ID_PAR) + jb, t4);
-            const int s = pass * chunks + u, slot = s % SLOTS;
-            if (ok) ok = mbar_wait(smem_addr(full + slot), ((uint32_t)s / SLOTS) & 1u);
-            if (ok && 4 * u + jb < Kb) {
-                BSide bs;
-                bside<WT>(cur, bs);
-                const uint32_t ub = ring + (uint32_t)slot * L::UNIT;
-                block_rows<WT, true>(nullptr, ub + jb * L::BLOCK, nullptr, ub + L::SCALES + jb * 256, lane, bs, acc);
+    uint32_t pos0 = 0;   // ring position of the current pass's first unit
+    for (int it = blockIdx.x; it < n_work; it += G) {
+        const IdItem w = id_item(a, live_e, pass_pre, n_live, it);
+        const IdProj &P = a.p[w.j];
+        const int n_items = __ldg(a.counts + w.e), item0 = __ldg(a.offsets + w.e);
+        const int Kb = P.K / QB, chunks = P.chunks;
+        const int pp = (chunks + ID_PAR - 1) / ID_PAR * ID_PAR;
+        {
+            const int pass = w.pass;
+            if (threadIdx.x < 8) {
+                const int idx = pass * 8 + threadIdx.x;
+                int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
+                if (p < 0 || p / a.k >= a.rows) p = -1;   // not a pair of this bucket: skip
+                tok_img[threadIdx.x] = p >= 0 ? p / a.k : -1;
+                tok_out[threadIdx.x] = p;
             }
-            mbar_arrive(smem_addr(empty + slot));   // after this thread's shared loads
+            id_consumers_sync();
+            const int rB = tok_img[g], rS0 = tok_img[2 * t4], rS1 = tok_img[2 * t4 + 1];
+            const uint8_t *imgB = rB >= 0 ? a.img + (int64_t)rB * a.img_row_bytes : nullptr;
+            const uint8_t *imgS0 = rS0 >= 0 ? a.img + (int64_t)rS0 * a.img_row_bytes : nullptr;
+            const uint8_t *imgS1 = rS1 >= 0 ? a.img + (int64_t)rS1 * a.img_row_bytes : nullptr;
+            float acc[UNIT_GROUPS][4];
+#pragma unroll
+            for (int r = 0; r < UNIT_GROUPS; r++)
+#pragma unroll
+                for (int i = 0; i < 4; i++) acc[r][i] = 0.0f;
+            // this warp's units: u = par mod ID_PAR; the image words one unit ahead
+            int u = par;
+            Raw next = {0u, 0u, 0u, 0u};
+            if (u < chunks && 4 * u + jb < Kb) next = load_raw(imgB, imgS0, imgS1, 4 * u + jb, t4);
+            for (; u < pp; u += ID_PAR) {
+                const Raw cur = next;
+                if (u + ID_PAR < chunks && 4 * (u + ID_PAR) + jb < Kb)
+                    next = load_raw(imgB, imgS0, imgS1, 4 * (u + ID_PAR) + jb, t4);
+                const uint32_t pos = pos0 + u;
+                const int slot = pos % SLOTS;
+                if (ok) ok = mbar_wait(smem_addr(full + slot), (pos / SLOTS) & 1u);
+                if (ok && u < chunks && 4 * u + jb < Kb) {
+                    BSide bs;
+                    bside<WT>(cur, bs);
+                    const uint32_t ub = ring + (uint32_t)slot * L::UNIT;
+                    block_rows<WT, true>(nullptr, ub + jb * L::BLOCK, nullptr, ub + L::SCALES + jb * 256, lane, bs,
+                                         acc);
+                }
+                mbar_arrive(smem_addr(empty + slot));   // after this thread's shared loads
+            }
+#pragma unroll
+            for (int r = 0; r < UNIT_GROUPS; r++)
+#pragma unroll
+                for (int i = 0; i < 4; i++) red[warp * VALS + (r * 4 + i) * 32 + lane] = acc[r][i];
+            id_consumers_sync();
+            for (int t = threadIdx.x; t < VALS; t += RW * 32) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int ww = 0; ww < RW; ww++) sum += red[ww * VALS + t];
+                int row, slot;
+                val_pos(t, row, slot);
+                row += w.rt * UNIT_ROWS;
+                const int orow = tok_out[slot];
+                if (row < P.N && orow >= 0) P.y[(int64_t)orow * P.N + row] = sum;
+            }
+            id_consumers_sync();   // tok_* and red are reused by the next item
         }
-#pragma unroll
-        for (int r = 0; r < UNIT_GROUPS; r++)
-#pragma unroll
-            for (int i = 0; i < 4; i++) red[warp * VALS + (r * 4 + i) * 32 + lane] = acc[r][i];
-        id_consumers_sync();
-        for (int t = threadIdx.x; t < VALS; t += RW * 32) {
-            float sum = 0.0f;
-#pragma unroll
-            for (int w = 0; w < RW; w++) sum += red[w * VALS + t];
-            int row, slot;
-            val_pos(t, row, slot);
-            row += rt * UNIT_ROWS;
-            const int orow = tok_out[slot];
-            if (row < P.N && orow >= 0) P.y[(int64_t)orow * P.N + row] = sum;
-        }
-        id_consumers_sync();   // tok_* and red are reused by the next pass
+        pos0 += pp;
     }
 }
 
@@ -1102,6 +1205,7 @@ qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k
     a.rows = rows;
     a.k = k;
     a.n_proj = n_proj;
+    a.E = (int)projs[0].n_experts;
     a.counts = counts;
     a.offsets = offsets;
     a.items = items;
@@ -1116,26 +1220,25 @@ qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k
         d.chunks = (int)ceil_div(d.K, UNIT_COLS);
         d.row_tiles = (int)ceil_div(d.N, UNIT_ROWS);
         d.tiles_begin = tiles;
-        tiles += d.row_tiles * projs[j].n_experts;
+        tiles += d.row_tiles;
     }
-    if (projs[0].wtype == QK_W_Q4_0) {
-        static bool configured = false;
-        if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(mmvq_id_kernel<QK_W_Q4_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)id_smem<QK_W_Q4_0>());
-            if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq_id: shared memory attribute: %s", cudaGetErrorString(e));
-            configured = true;
-        }
-        return launch_pdl("mmvq_id", mmvq_id_kernel<QK_W_Q4_0>, dim3(tiles), dim3(ID_THREADS), id_smem<QK_W_Q4_0>(), s, a);
+    a.tiles_per_expert = tiles;
+    if (a.E > ID_MAX_E) return fail(QK_ERR_UNSUPPORTED, "mmvq_id: n_experts=%d > %d", a.E, ID_MAX_E);
+    const bool q4 = projs[0].wtype == QK_W_Q4_0;
+    auto kernel = q4 ? mmvq_id_kernel<QK_W_Q4_0> : mmvq_id_kernel<QK_W_Q8_0>;
+    const size_t smem = q4 ? id_smem<QK_W_Q4_0>() : id_smem<QK_W_Q8_0>();
+    static int per_sm[2] = {0, 0};   // resident CTAs per SM, after the shared-memory attribute
+    int &occ = per_sm[q4 ? 0 : 1];
+    if (occ == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, ID_THREADS, smem);
+        if (e != cudaSuccess || occ < 1)
+            return fail(QK_ERR_CUDA, "mmvq_id: kernel configuration: %s", cudaGetErrorString(e));
     }
-    static bool configured8 = false;
-    if (!configured8) {
-        cudaError_t e = cudaFuncSetAttribute(mmvq_id_kernel<QK_W_Q8_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)id_smem<QK_W_Q8_0>());
-        if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq_id: shared memory attribute: %s", cudaGetErrorString(e));
-        configured8 = true;
-    }
-    return launch_pdl("mmvq_id", mmvq_id_kernel<QK_W_Q8_0>, dim3(tiles), dim3(ID_THREADS), id_smem<QK_W_Q8_0>(), s, a);
+    const int64_t work_max = (int64_t)a.E * tiles;
+    const int64_t resident = (int64_t)occ * sm_count();
+    const int G = (int)(work_max < resident ? work_max : resident);
+    return launch_pdl("mmvq_id", kernel, dim3((unsigned)G), dim3(ID_THREADS), smem, s, a);
 }
 
 }  // namespace qk
