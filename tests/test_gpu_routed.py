@@ -188,3 +188,41 @@ def test_captured_bucket_replay_with_poisoned_padding(moe, bucket, lives):
         assert np.array_equal(y[:live].view(np.uint32), host(ref["y"]).view(np.uint32))
         assert np.array_equal(yg[:live * TOPK].view(np.uint32), host(ref["yg"]).view(np.uint32))
         assert np.array_equal(yu[:live * TOPK].view(np.uint32), host(ref["yu"]).view(np.uint32))
+
+
+@pytest.mark.parametrize("wtype", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("n_exp,k", [(1, 1), (37, 4), (300, 4)])
+def test_routed_widths_passes_and_ragged_tiles(wtype, n_exp, k):
+    """Expert counts that are not a multiple of 32 and above one 32-expert run per warp, experts with
+    more than 8 pairs (several passes), an odd number of 128-column chunks, ragged row tiles and two
+    projections of different widths: outputs within the exact-path NMSE of the oracle, every planned
+    pair written, every unplanned pair left as it was."""
+    import torch
+    rows, live, Kp = 48, 45, 384                      # 3 column chunks
+    Ns = (200, 64)                                    # 2 row tiles (ragged) and 1
+    g = synth.rng(9400 + n_exp + k)
+    hot = max(1, min(5, n_exp))                       # half the pairs go to a few experts (> 8 pairs each)
+    ids_h = np.where(g.random((rows, k)) < 0.5, g.integers(0, hot, size=(rows, k)),
+                     g.integers(0, n_exp, size=(rows, k))).astype(np.int32)
+    x = synth.activations(9401 + n_exp, rows, Kp)
+    img_h = O.quantize_q8_1(x, row_blocks=Kp // 32)
+    counts = torch.zeros((n_exp,), dtype=torch.int32, device="cuda")
+    offsets = torch.zeros((n_exp + 1,), dtype=torch.int32, device="cuda")
+    items = torch.zeros((rows * k,), dtype=torch.int32, device="cuda")
+    qk.qk_moe_plan(dev(ids_h), rows, k, n_exp, counts, offsets, items, live_ptr(live))
+    rc, ro, rit = O.moe_plan(ids_h, n_exp, live=live)
+    assert np.array_equal(host(counts), rc) and rc.max() > 8
+    gen = synth.q4_0_weight if wtype == "q4_0" else synth.q8_0_weight
+    Ws = [[gen(9500 + 1000 * j + e, N, Kp) for e in range(n_exp)] for j, N in enumerate(Ns)]
+    bufs = [pack_experts(Ws[j], wtype, N, Kp) for j, N in enumerate(Ns)]
+    ys = [torch.full((rows * k, N), float(SENTINEL), dtype=torch.float32, device="cuda") for N in Ns]
+    projs = [qk.make_proj_id(wtype, n_exp, bufs[j], N, Kp, ys[j]) for j, N in enumerate(Ns)]
+    qk.qk_mmvq_id(dev(img_h.reshape(-1)), Kp // 32, rows, k, projs, counts, offsets, items)
+    assert qk.qk_device_faults() == 0
+    planned = np.zeros(rows * k, dtype=bool)
+    planned[rit] = True
+    for j, N in enumerate(Ns):
+        got = host(ys[j])
+        ref = O.proj_id_q8_1(wtype, np.concatenate(Ws[j], axis=0), n_exp, N, Kp, img_h, Kp // 32, ids_h, rit)
+        assert O.nmse(got[planned], ref[planned]) <= 1e-10
+        assert np.all(got[~planned] == SENTINEL)
