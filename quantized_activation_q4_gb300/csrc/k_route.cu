@@ -16,6 +16,19 @@ constexpr int MAX_E_PER_LANE = 8;   // E <= 256
 // larger first, equal logits to the lower expert index (exact f32 compares,
 // so ids are reproducible bit for bit). Weights are the softmax probabilities
 // of the chosen experts.
+//
+// Each pick is two warp reductions: the largest key, then the lowest expert
+// index holding it. A logit's key is its bit pattern mapped so that unsigned
+// order is float order (negative: all bits flipped; positive: sign bit set),
+// after adding +0 so that -0 and +0 share a key, as they compare equal.
+__device__ __forceinline__ unsigned order_key(float v) {
+    const unsigned u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int rows, int E,
                                                    int k, int32_t *__restrict__ ids,
                                                    float *__restrict__ wts, const int32_t *live) {
@@ -26,13 +39,14 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     if (r >= live_rows(live, rows)) return;   // warp-uniform
     const float *l = logits + (int64_t)r * E;
     float v[MAX_E_PER_LANE];
-    int n = 0;
+    unsigned key[MAX_E_PER_LANE];
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < MAX_E_PER_LANE; i++) {
         const int e = lane + 32 * i;
         v[i] = e < E ? __ldg(l + e) : -INFINITY;
-        if (e < E) { mx = fmaxf(mx, v[i]); n++; }
+        key[i] = e < E ? order_key(v[i]) : 0u;   // 0: below every logit, never picked
+        if (e < E) mx = fmaxf(mx, v[i]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
@@ -43,34 +57,27 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(FULL, z, o);
 
-    unsigned taken = 0;   // bit i: expert lane + 32 i already chosen
     for (int s = 0; s < k; s++) {
-        float bv = -INFINITY;
+        unsigned bk = 0u;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < MAX_E_PER_LANE; i++) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi) || bi == 0x7fffffff)) {
-                bv = v[i];
-                bi = e;
+        for (int i = 0; i < MAX_E_PER_LANE; i++)   // ascending expert index: strict > keeps the lowest on ties
+            if (key[i] > bk) {
+                bk = key[i];
+                bi = lane + 32 * i;
             }
-        }
+        const unsigned mk = __reduce_max_sync(FULL, bk);
+        const int idx = (int)__reduce_min_sync(FULL, bk == mk && bk != 0u ? (unsigned)bi : 0x7fffffffu);
+        if ((idx & 31) == lane) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(FULL, bv, o);
-            const int oi = __shfl_xor_sync(FULL, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-                bv = ov;
-                bi = oi;
-            }
+            for (int i = 0; i < MAX_E_PER_LANE; i++)
+                if (i == (idx >> 5)) key[i] = 0u;   // taken
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
         if (lane == 0) {
-            ids[(int64_t)r * k + s] = bi;
-            wts[(int64_t)r * k + s] = expf(bv - mx) / z;
+            ids[(int64_t)r * k + s] = idx;
+            wts[(int64_t)r * k + s] = expf(key_value(mk) - mx) / z;
         }
     }
-    (void)n;
 }
 
 // ---------------------------------------------------------------- plan
