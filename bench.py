@@ -428,7 +428,31 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
     out["c1_control"] = {"fused_us": round(us_f, 3), "unfused_us": round(us_c, 3),
                          "kernels_fused": ["rmsnorm_q8_1", "mmvq(q,k,v)"],
                          "kernels_unfused": ["rmsnorm_q8_1", "quantize_q8_1", "mmvq(q,k,v)"]}
-    del qkv_w
+    # ---- config 1 per kernel (cold: rotating weights) and warm (one weight set, resident in L2)
+    x2 = dev(synth.activations(102, T, K_BIG))
+    img2 = torch.empty((IMG_BIG,), dtype=torch.uint8, device="cuda")
+    big_w = [packed(650 + r, N_BIG, K_BIG) for r in range(max(2, -(-3 * l2 // W_BIG)))]
+    big_y = torch.empty((T, N_BIG), dtype=torch.float32, device="cuda")
+    pb = lambda r: [qk.make_proj("q4_0", big_w[r], N_BIG, K_BIG, big_y, N_BIG)]
+    wsb_n = qk.qk_mmvq_workspace_bytes(pb(0))
+    wsb = torch.zeros((wsb_n,), dtype=torch.uint8, device="cuda")
+    rms = lambda: qk.qk_rmsnorm_q8_1(x, T, D_ATTN, D_ATTN, "mul", w, None, 1.0, 1e-6, y, D_ATTN, img, D_ATTN // 32)
+    quant = lambda: qk.qk_quantize_q8_1(x2, T, K_BIG, K_BIG, img2, K_BIG // 32)
+    mq = lambda r: qk.qk_mmvq(img, D_ATTN // 32, T, pr(r), ws1, ws1_n)
+    mb = lambda r: qk.qk_mmvq(img2, K_BIG // 32, T, pb(r), wsb, wsb_n)
+    rms()
+    quant()
+    Rb = len(big_w)
+    k_us = {"rmsnorm_q8_1": _graph_us(torch, stream, [rms] * R1, 10),
+            "mmvq_qkv_cold": _graph_us(torch, stream, [lambda r=r: mq(r) for r in range(R1)], 10),
+            "mmvq_qkv_warm": _graph_us(torch, stream, [lambda: mq(0)] * R1, 10),
+            "quantize_q8_1": _graph_us(torch, stream, [quant] * Rb, 10),
+            "mmvq_8192_cold": _graph_us(torch, stream, [lambda r=r: mb(r) for r in range(Rb)], 10),
+            "mmvq_8192_warm": _graph_us(torch, stream, [lambda: mb(0)] * Rb, 10)}
+    out["c1_kernels"] = {k: round(v, 3) for k, v in k_us.items()}
+    out["c1_kernels"]["note"] = ("each kernel alone, back-to-back in one graph; cold = weights rotate over "
+                                 "replicas > 3x L2, warm = one weight set re-read from L2")
+    del qkv_w, big_w
 
     # ---- config 2: SwiGLU (packed [8, 37888]) -> image -> down 18944 -> 3584
     NF, DM = 18944, 3584
@@ -492,9 +516,22 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
         us_3 = _graph_us(torch, stream, [lambda r=r: routed(r) for r in range(R3)], 10)
         touched = int((counts > 0).sum().item())
         wb = touched * 2 * per
+        per_kernel = {
+            "rmsnorm_q8_1": _graph_us(torch, stream, [lambda: qk.qk_rmsnorm_q8_1(
+                xr, bucket, DR, DR, "mul", wr, None, 1.0, 1e-6, yr, DR, rimg, DR // 32, d_live_rows=lv)] * 16, 10),
+            "topk_route": _graph_us(torch, stream, [lambda: qk.qk_topk_route(
+                logits, bucket, E, KTOP, ids, wts, d_live_rows=lv)] * 16, 10),
+            "moe_plan": _graph_us(torch, stream, [lambda: qk.qk_moe_plan(
+                ids, bucket, KTOP, E, counts, offsets, items, d_live_rows=lv)] * 16, 10),
+            "mmvq_id": _graph_us(torch, stream, [lambda r=r: qk.qk_mmvq_id(
+                rimg, DR // 32, bucket, KTOP, [qk.make_proj_id("q4_0", E, experts[r][pj], NE, DR, ys[pj])
+                                               for pj in range(2)], counts, offsets, items)
+                for r in list(range(R3)) * 8], 10)}
         c3[f"live{live}_bucket{bucket}"] = {"us": round(us_3, 3), "distinct_experts": touched, "weight_bytes": wb,
                                             "weight_gbs": gb(wb, us_3),
-                                            "kernels": ["rmsnorm_q8_1", "topk_route", "moe_plan", "mmvq_id(gate,up)"]}
+                                            "kernels": ["rmsnorm_q8_1", "topk_route", "moe_plan", "mmvq_id(gate,up)"],
+                                            "per_kernel_us": {k: round(v, 3) for k, v in per_kernel.items()},
+                                            "mmvq_id_gbs": gb(wb, per_kernel["mmvq_id"])}
     out["c3_routed"] = c3
     del experts
 
@@ -584,7 +621,30 @@ def cpu_baseline(big_rows: int = 2048, budget_s: float = 10.0) -> dict:
     return {"value": round(wbytes / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"full q/k/v component + {big_rows} of 8192 rows of the K8192 matvec per step "
                       f"({wbytes / 1e6:.1f} MB of weights), {reps} steps, single thread",
-            "seconds_per_sample_step": round(dt, 3)}
+            "seconds_per_sample_step": round(dt, 3), "c4_prefill": cpu_prefill_sample()}
+
+
+def cpu_prefill_sample(cols: int = 64) -> dict:
+    """The oracle's quantised-path prefill contraction (config 4) on a bounded sample:
+    all 3325 tokens of the Q8_0 image against `cols` output columns of the q weight
+    (3584 x 3584), single thread; the per-layer time is an extrapolation by ops."""
+    from oracle import oracle as O
+    from quantized_activation_q4_gb300 import synth
+    TP, DP = 3325, 3584
+    x = synth.activations(130, TP, DP)
+    qs, dh = O.quantize_q8_0(x)
+    W = synth.q4_0_weight(800, DP, DP)
+    rows = np.arange(TP)
+    cs = np.arange(cols)
+    O.proj_q8_0_sampled("q4_0", W, DP, DP, qs, dh, DP // 32, rows[:8], cs)   # build + warm
+    t0 = time.perf_counter()
+    O.proj_q8_0_sampled("q4_0", W, DP, DP, qs, dh, DP // 32, rows, cs)
+    dt = time.perf_counter() - t0
+    ops = 2 * TP * cols * DP
+    layer_ops = 2 * TP * DP * (3584 + 512 + 512 + 2 * 18944)
+    return {"gop_per_s": round(ops / dt / 1e9, 3), "cores": 1, "kind": "oracle",
+            "sample": f"{TP} tokens x {cols} of 3584 q columns, K=3584 ({ops / 1e9:.2f} GOP, {dt:.2f} s)",
+            "layer_seconds_extrapolated": round(layer_ops / (ops / dt), 1)}
 
 
 def run_reference(args, rank: int) -> dict | None:

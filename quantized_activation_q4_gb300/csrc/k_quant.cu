@@ -88,13 +88,15 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
     pdl_trigger();
     pdl_wait();
     const int t = blockIdx.y;
-    if (t >= live_rows(live, T)) return;
     const int lane = threadIdx.x & 31, j8 = lane & 7;
     const int64_t b = (int64_t)blockIdx.x * 32 + (threadIdx.x >> 5) * 4 + (lane >> 3);
     const bool in_row = b < row_blocks;          // whole 8-lane group agrees
     const int64_t col = b * QB + 4 * j8;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
+    // the row's values are loaded together with the live count (row t < T is in the caller's
+    // buffer even when it is padding), so the two global reads overlap
     if (in_row && col < K) load4(x + t * x_stride + col, (int)(K - col < 4 ? K - col : 4), v);
+    if (t >= live_rows(live, T)) return;
     uint32_t codes;
     int sum;
     const float d = q8_block(v, &codes, &sum);  // all lanes take part in the shuffles
@@ -121,21 +123,23 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
     pdl_trigger();
     pdl_wait();
     const int t = blockIdx.x;
-    if (t >= live_rows(live, T)) return;
     const float *xr = x + t * x_stride;
     const int tid = threadIdx.x, lane = tid & 31, j8 = lane & 7;
 
+    // the row is loaded together with the live count (row t < T is in the caller's buffer
+    // even when it is padding), so the two global reads overlap
     float v[RMS_ITEMS][4];
-    float ss = 0.0f;
 #pragma unroll
     for (int it = 0; it < RMS_ITEMS; it++) {
         const int c = 4 * tid + 4 * RMS_THREADS * it;
         v[it][0] = v[it][1] = v[it][2] = v[it][3] = 0.0f;
-        if (c < K) {
-            load4(xr + c, 4, v[it]);
-            ss += v[it][0] * v[it][0] + v[it][1] * v[it][1] + v[it][2] * v[it][2] + v[it][3] * v[it][3];
-        }
+        if (c < K) load4(xr + c, 4, v[it]);
     }
+    if (t >= live_rows(live, T)) return;
+    float ss = 0.0f;
+#pragma unroll
+    for (int it = 0; it < RMS_ITEMS; it++)
+        ss += v[it][0] * v[it][0] + v[it][1] * v[it][1] + v[it][2] * v[it][2] + v[it][3] * v[it][3];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
     __shared__ float red[RMS_THREADS / 32];
@@ -203,7 +207,6 @@ __global__ void __launch_bounds__(256) glu_q8_1_kernel(
     pdl_trigger();
     pdl_wait();
     const int t = blockIdx.y;
-    if (t >= live_rows(live, T)) return;
     const int tid = threadIdx.x, j8 = tid & 7;
     const int c = blockIdx.x * 1024 + 4 * tid;
     const float *g, *u;
@@ -218,11 +221,16 @@ __global__ void __launch_bounds__(256) glu_q8_1_kernel(
         g = u + N;
     }
     const bool ok = c < N;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    // the inputs are loaded together with the live count (row t < T is in the caller's
+    // buffers even when it is padding), so the global reads overlap
+    float gv[4] = {0.f, 0.f, 0.f, 0.f}, uv[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
-        float gv[4], uv[4];
         load4(g + c, 4, gv);
         load4(u + c, 4, uv);
+    }
+    if (t >= live_rows(live, T)) return;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
 #pragma unroll
         for (int i = 0; i < 4; i++) v[i] = glu_act(kind, gv[i]) * uv[i];
         store4(out + t * out_stride + c, v);

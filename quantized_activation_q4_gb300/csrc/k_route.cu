@@ -36,15 +36,22 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (r >= live_rows(live, rows)) return;   // warp-uniform
+    if (r >= rows) return;   // warp-uniform
+    // the row's logits are loaded together with the live count (row r < rows is in the
+    // caller's buffer even when it is padding), so the two global reads overlap
     const float *l = logits + (int64_t)r * E;
     float v[MAX_E_PER_LANE];
+#pragma unroll
+    for (int i = 0; i < MAX_E_PER_LANE; i++) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldg(l + e) : -INFINITY;
+    }
+    if (r >= live_rows(live, rows)) return;   // warp-uniform
     unsigned key[MAX_E_PER_LANE];
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < MAX_E_PER_LANE; i++) {
         const int e = lane + 32 * i;
-        v[i] = e < E ? __ldg(l + e) : -INFINITY;
         key[i] = e < E ? order_key(v[i]) : 0u;   // 0: below every logit, never picked
         if (e < E) mx = fmaxf(mx, v[i]);
     }
