@@ -30,8 +30,9 @@
 //             32-column A stages) and issues the MMAs (one thread);
 //     warps 10-13: read a finished accumulator and store C while the MMAs of
 //             the next tile run into the other one.
-// Within a 32-block the K positions follow the order in which a packed
-// weight word converts (see a_word); dequant_b writes B in the same order.
+// Within a 32-block the K positions follow the order in which the converters
+// store a packed weight word (column 2t+p: elements 4t+p and 4t+p+2; column
+// 8+2t+p: elements 16+4t+p and 18+4t+p); dequant_b writes B in the same order.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -46,8 +47,8 @@ constexpr int TM = 128;              // weight rows per CTA (MMA M)
 constexpr int TN = 192;              // tokens per CTA (MMA N)
 constexpr int KC = 64;               // K elements per stage (one 128-byte swizzle row of f16)
 constexpr int NS = 4;                // stages (A in tensor memory, B in shared memory)
-constexpr int NU = 3;                // packed-unit staging slots (a unit = 2 stages)
-constexpr int PF = 6;                // units prefetched into L2 ahead of the one being loaded
+constexpr int NU = 6;                // packed-unit staging slots (a unit = 2 stages)
+constexpr int PF = 10;               // units prefetched into L2 ahead of the one being loaded
 constexpr int B_TILE = TN * KC * 2;  // 24 KB
 constexpr uint32_t A_COLS = KC / 2;  // tensor-memory columns of one A stage (two f16 per column)
 constexpr int EPI0 = 10;             // first epilogue warp
@@ -184,8 +185,9 @@ __device__ __forceinline__ uint32_t b_pair(uint32_t v, int k0, int k1, float da)
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-// One thread per (token, block, word): 8 codes -> 16 bytes of f16 q * d_a in
-// the K order of a_word.
+// One thread per (token, block, word w): 8 codes -> f16 q * d_a at columns
+// 2w, 2w+1 (low word) and 8+2w, 9+2w (high word) of the block, the K order of
+// the A stages.
 __global__ void __launch_bounds__(256) dequant_b_kernel(const int8_t *__restrict__ qs, const uint16_t *__restrict__ d,
                                                         int64_t row_blocks, int T, int kb, __half *__restrict__ B) {
     pdl_trigger();
@@ -199,8 +201,9 @@ __global__ void __launch_bounds__(256) dequant_b_kernel(const int8_t *__restrict
     const uint32_t lo = __ldg(reinterpret_cast<const unsigned int *>(src + 4 * w));
     const uint32_t hi = __ldg(reinterpret_cast<const unsigned int *>(src + 16 + 4 * w));
     const float da = __half2float(__ushort_as_half(__ldg(d + (int64_t)t * row_blocks + b)));
-    const uint4 out = make_uint4(b_pair(lo, 0, 2, da), b_pair(lo, 1, 3, da), b_pair(hi, 0, 2, da), b_pair(hi, 1, 3, da));
-    *reinterpret_cast<uint4 *>(B + ((int64_t)t * kb + b) * QB + 8 * w) = out;
+    __half *dst = B + ((int64_t)t * kb + b) * QB;
+    *reinterpret_cast<uint2 *>(dst + 4 * w) = make_uint2(b_pair(lo, 0, 2, da), b_pair(lo, 1, 3, da));
+    *reinterpret_cast<uint2 *>(dst + 16 + 4 * w) = make_uint2(b_pair(hi, 0, 2, da), b_pair(hi, 1, 3, da));
 }
 
 // ------------------------------------------------------------------ the GEMM
@@ -320,11 +323,9 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
             }
         }
     } else if (warp < EPI0) {   // ---------------- warps 2..9: A conversion into tensor memory
-        // A warp may only touch tensor-memory lanes 32 (warp % 4) .. +31, so tile row n = 32 (warp % 4) + lane.
-        // In the packed unit, row n is row {g, g+8, 16+g, 24+g}[r] of region k4, lane group g, word
-        // slot r; its scale is half h8 of word g*8.. of row group rr (rows 16rr+g, +8).
-        const int quad = warp & 3, n = 32 * quad + lane, qb = (warp - 2) >> 2;   // qb: block of the stage
-        const int g8 = n & 7, r = (n >> 3) & 3, k4 = n >> 5, rr = n >> 4, h8 = (n >> 3) & 1;
+        // A warp may only touch tensor-memory lanes 32 (warp % 4) .. +31: its rows are tile rows
+        // 32 (warp % 4) .. +31, region warp % 4 of the packed unit, and tensor-memory lane = tile row.
+        const int quad = warp & 3, qb = (warp - 2) >> 2;   // qb: the stage's block this warp converts
         const uint32_t arow = tmem + ((uint32_t)(32 * quad) << 16) + A_TMEM;
         uint32_t g = 0, gu = 0;
         bool ok = true;
@@ -338,30 +339,28 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                 if (!ok) break;
                 tc_fence_after();
                 const uint8_t *unit = smem + OFF_U + us * Q4_UNIT_BYTES;
-                uint32_t v[16];   // column c: K positions 2c, 2c+1 of this block (a_word order)
                 {
-                    const int jb = 2 * h + qb;
-                    const uint32_t sc =
-                        *reinterpret_cast<const uint32_t *>(unit + 8192 + jb * 256 + g8 * 32 + rr * 4);
-                    const __half dh = __ushort_as_half((uint16_t)(h8 ? sc >> 16 : sc & 0xFFFFu));
-                    const __half2 dw = __halves2half2(dh, dh);
-#pragma unroll
-                    for (int tw = 0; tw < 4; tw++) {
-                        const uint32_t w = *reinterpret_cast<const uint32_t *>(unit + jb * 2048 + k4 * 512 +
-                                                                               (g8 * 4 + tw) * 16 + r * 4);
-                        const uint4 x = a_word(w, dw);
-                        v[4 * tw + 0] = x.x;
-                        v[4 * tw + 1] = x.y;
-                        v[4 * tw + 2] = x.z;
-                        v[4 * tw + 3] = x.w;
-                    }
+                    // Lane (g, t) loads word t of rows g, g+8, 16+g, 24+g of the warp's 32 rows (one
+                    // conflict-free 16-byte load) and stores them with the 16x256b shape: registers 0,1
+                    // go to lane g and 2,3 to lane g+8 at columns 2t, 2t+1, registers 4..7 the same way
+                    // at columns 8+2t, 9+2t; a second store does lanes 16+g and 24+g. So column 2t+p of a
+                    // block holds elements (4t+p, 4t+p+2) and column 8+2t+p holds (16+4t+p, 18+4t+p).
+                    const int jb = 2 * h + qb, gq = lane >> 2;
+                    const uint4 wv = *reinterpret_cast<const uint4 *>(unit + jb * 2048 + quad * 512 + lane * 16);
+                    const uint2 sc = *reinterpret_cast<const uint2 *>(unit + 8192 + jb * 256 + gq * 32 + quad * 8);
+                    const __half2 s01 = *reinterpret_cast<const __half2 *>(&sc.x), s23 = *reinterpret_cast<const __half2 *>(&sc.y);
+                    const uint4 a0 = a_word(wv.x, __low2half2(s01)), a1 = a_word(wv.y, __high2half2(s01));
+                    const uint4 a2 = a_word(wv.z, __low2half2(s23)), a3 = a_word(wv.w, __high2half2(s23));
+                    const uint32_t base = arow + s * A_COLS + 16 * qb;
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(base),
+                        "r"(a0.x), "r"(a0.y), "r"(a1.x), "r"(a1.y), "r"(a0.z), "r"(a0.w), "r"(a1.z), "r"(a1.w)
+                        : "memory");
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(base + (16u << 16)),
+                        "r"(a2.x), "r"(a2.y), "r"(a3.x), "r"(a3.y), "r"(a2.z), "r"(a2.w), "r"(a3.z), "r"(a3.w)
+                        : "memory");
                 }
-                asm volatile(
-                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-                    "%15,%16};" ::"r"(arow + s * A_COLS + 16 * qb),
-                    "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-                    "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-                    : "memory");
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 mbar_arrive(full_a + 8 * s);
