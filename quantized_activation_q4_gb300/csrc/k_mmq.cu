@@ -17,7 +17,7 @@
 //   dequant_b: the image -> B, [T][K] binary16 in the caller's workspace,
 //     once per call (it is read by every 128-row weight tile).
 //   mmq_tc: persistent, one CTA per SM, tiles of (projection, 128-row weight
-//     tile, 192-token tile) taken round-robin, tokens fastest so that the CTAs
+//     tile, 208-token tile) taken round-robin, tokens fastest so that the CTAs
 //     running at one time share a few weight row tiles through L2.
 //     warp 0: TMA -- the B tiles (2D tensor copies, 128-byte swizzle) and the
 //             packed weight units (bulk copies) into shared-memory rings, with
@@ -26,7 +26,7 @@
 //             memory (tcgen05.st; two warps per 32-lane quarter, one 32-block
 //             each), so the MMAs read A from tensor memory and only B from
 //             shared memory;
-//     warp 1: allocates tensor memory (two 192-column accumulators and four
+//     warp 1: allocates tensor memory (two 208-column accumulators and three
 //             32-column A stages) and issues the MMAs (one thread);
 //     warps 10-13: read a finished accumulator and store C while the MMAs of
 //             the next tile run into the other one.
@@ -44,12 +44,12 @@ namespace {
 
 constexpr int MAX_PROJ = 8;
 constexpr int TM = 128;              // weight rows per CTA (MMA M)
-constexpr int TN = 192;              // tokens per CTA (MMA N)
+constexpr int TN = 208;              // tokens per CTA (MMA N; 3325 tokens = 16 tiles)
 constexpr int KC = 64;               // K elements per stage (one 128-byte swizzle row of f16)
-constexpr int NS = 4;                // stages (A in tensor memory, B in shared memory)
+constexpr int NS = 3;                // stages (A in tensor memory, B in shared memory)
 constexpr int NU = 6;                // packed-unit staging slots (a unit = 2 stages)
 constexpr int PF = 10;               // units prefetched into L2 ahead of the one being loaded
-constexpr int B_TILE = TN * KC * 2;  // 24 KB
+constexpr int B_TILE = TN * KC * 2;  // 26 KB
 constexpr uint32_t A_COLS = KC / 2;  // tensor-memory columns of one A stage (two f16 per column)
 constexpr int EPI0 = 10;             // first epilogue warp
 constexpr int THREADS = 14 * 32;
@@ -68,7 +68,7 @@ constexpr int N_BARS = 3 * NS + 2 * NU + 4;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + slack to align the base to 1024
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
-// instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 192, M = 128
+// instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 208, M = 128
 constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
 
 __device__ unsigned int g_mmq_faults = 0;
@@ -80,7 +80,7 @@ struct MmqProj {
     int N, K, chunks, row_tiles, rt_begin;   // rt_begin: first global row tile
 };
 struct MmqArgs {
-    CUtensorMap bmap;    // B [T][K] f16, box 64 x 192, 128-byte swizzle
+    CUtensorMap bmap;    // B [T][K] f16, box 64 x 208, 128-byte swizzle
     int T, n_proj, tok_tiles, tiles;
     MmqProj p[MAX_PROJ];
 };
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {   // tensor memory: accumulators (2 x 192 columns) and A stages (4 x 32 columns)
+    if (warp == 1) {   // tensor memory: accumulators (2 x 208 columns) and A stages (3 x 32 columns)
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
                      : "memory");
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
             tc_fence_after();
             const int row = t.rt * TM + quad * 32 + lane;
 #pragma unroll 1
-            for (int c0 = 0; c0 < TN; c0 += 32) {
+            for (int c0 = 0; c0 < TN; c0 += 32) {   // the last load runs past TN: those columns are not stored
                 uint32_t v[32];
                 asm volatile(
                     "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
 #pragma unroll
                     for (int k = 0; k < 32; k++) {
                         const int tok = t.tok0 + c0 + k;
-                        if (tok < a.T) P.y[(int64_t)tok * P.y_stride + row] = __uint_as_float(v[k]);
+                        if (c0 + k < TN && tok < a.T) P.y[(int64_t)tok * P.y_stride + row] = __uint_as_float(v[k]);
                     }
                 }
             }
