@@ -279,36 +279,87 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         ms_per_step = float(t.item())
 
     # ---------------------------------------------------------------- e2e through the C ABI, host buffers
-    xh = torch.empty((T, D_ATTN), dtype=torch.float32).pin_memory()
-    x2h = torch.empty((T, K_BIG), dtype=torch.float32).pin_memory()
-    xh.copy_(torch.from_numpy(synth.activations(100, T, D_ATTN)))
-    x2h.copy_(torch.from_numpy(synth.activations(102, T, K_BIG)))
-    outh = {name: torch.empty((T, N), dtype=torch.float32).pin_memory() for name, N in QKV}
-    bigh = torch.empty((T, N_BIG), dtype=torch.float32).pin_memory()
-    h2d = xh.numel() * 4 + x2h.numel() * 4
-    d2h = sum(v.numel() * 4 for v in outh.values()) + bigh.numel() * 4
+    # Every step copies its inputs (x and x2, as column ranges of one [8][3584 + 8192] buffer) in from
+    # pinned host memory, runs the four kernels and copies all four outputs (column ranges of one
+    # [8][4608 + 8192] buffer: q, k, v, then the 8192-wide matvec) back: one copy each way. Each step
+    # (copies and launches) is one CUDA graph, as a serving loop would replay it; two device buffer
+    # sets alternate, and the input copy of the next step runs on a second stream, so it overlaps
+    # the kernels of the step before.
+    NB = 2
+    XW, YW = D_ATTN + K_BIG, sum(N for _, N in QKV) + N_BIG
+    sets = [{"xin": torch.empty((T, XW), dtype=torch.float32, device="cuda"), "y": torch.empty_like(y),
+             "img": torch.empty_like(img), "img2": torch.empty_like(img2),
+             "yout": torch.empty((T, YW), dtype=torch.float32, device="cuda")} for _ in range(NB)]
+    xinh = torch.empty((T, XW), dtype=torch.float32).pin_memory()
+    xinh[:, :D_ATTN].copy_(torch.from_numpy(synth.activations(100, T, D_ATTN)))
+    xinh[:, D_ATTN:].copy_(torch.from_numpy(synth.activations(102, T, K_BIG)))
+    youth = [torch.empty((T, YW), dtype=torch.float32).pin_memory() for _ in range(NB)]
+    h2d = xinh.numel() * 4
+    d2h = youth[0].numel() * 4
+    side = torch.cuda.Stream()
+    col0 = [0]
+    for _, N in QKV:
+        col0.append(col0[-1] + N)
 
-    def e2e_step(i):
-        r = i % R
-        x.copy_(xh, non_blocking=True)
-        x2.copy_(x2h, non_blocking=True)
-        step_graphs[r].replay()
-        for name, _ in QKV:
-            outh[name].copy_(outs[name], non_blocking=True)
-        bigh.copy_(out_big, non_blocking=True)
+    def e2e_step(r, b):
+        """The step on set b: its kernels on the main stream while the side stream copies the next
+        step's inputs into set 1 - b and the previous step's outputs out of set 1 - b (a two-deep
+        software pipeline); the side stream joins before the step ends."""
+        sb, nb = sets[b], sets[1 - b]
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            youth[1 - b].copy_(nb["yout"], non_blocking=True)
+            nb["xin"].copy_(xinh, non_blocking=True)
+        xs, x2s, yo = sb["xin"][:, :D_ATTN], sb["xin"][:, D_ATTN:], sb["yout"]
+        qk.qk_rmsnorm_q8_1(xs, T, D_ATTN, XW, "mul", w, None, 1.0, 1e-6, sb["y"], D_ATTN, sb["img"], D_ATTN // 32)
+        qk.qk_mmvq(sb["img"], D_ATTN // 32, T,
+                   [qk.make_proj("q4_0", reps[r]["qkv"][i], N, D_ATTN, yo[:, col0[i]:col0[i] + N], YW)
+                    for i, (name, N) in enumerate(QKV)], ws_a, ws_a_n)
+        qk.qk_quantize_q8_1(x2s, T, K_BIG, XW, sb["img2"], K_BIG // 32)
+        qk.qk_mmvq(sb["img2"], K_BIG // 32, T,
+                   [qk.make_proj("q4_0", reps[r]["big"], N_BIG, K_BIG, yo[:, col0[-1]:], YW)], ws_m, ws_m_n)
+        stream.wait_stream(side)
 
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            e2e_step(i)
+        for b in range(NB):
+            sets[b]["xin"].copy_(xinh, non_blocking=True)
+            e2e_step(0, b)
+    torch.cuda.synchronize()
+    e2e_graphs = {}
+    for r in range(R):
+        for b in range(NB):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                e2e_step(r, b)
+            e2e_graphs[(r, b)] = g
+
+    def e2e_run(n, start):
+        """n steps: the first step's input copy, n step graphs, the last step's output copy (so
+        n + 1 copies each way are timed for n steps)."""
+        sets[start % NB]["xin"].copy_(xinh, non_blocking=True)
+        for i in range(start, start + n):
+            e2e_graphs[(i % R, i % NB)].replay()
+        last = (start + n - 1) % NB
+        youth[last].copy_(sets[last]["yout"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_run(args.warmup, 0)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(2e6 + 100_000 * K))   # hold the stream while the host enqueues
         e0.record(stream)
-        for i in range(K):
-            e2e_step(i)
+        e2e_run(K, args.warmup)
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K
+    # the last step's outputs, as copied to the host, against the same step run by the device-timed path
+    r_last = (args.warmup + K - 1) % R
+    with torch.cuda.stream(stream):
+        step_graphs[r_last].replay()
+    torch.cuda.synchronize()
+    ref = torch.cat([outs[name] for name, _ in QKV] + [out_big], dim=1).cpu()
+    e2e_match = bool(torch.equal(youth[(args.warmup + K - 1) % NB], ref))
 
     peaks = measured_peaks()
     hbm = peaks["hbm_gbs"]
@@ -355,7 +406,13 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                      "traffic_source": "profiles/mmvq_q4_0_8192x8192_t8.md (ncu, one launch; null if the "
                                        "kernel sources changed since)"},
         "e2e": {"value": round(W_STEP / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 5),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "outputs_match_device_path": e2e_match,
+                "schedule": "every step copies x and x2 in from pinned host memory (one copy: column ranges of one "
+                            "buffer) and its 4 outputs back (one copy: column ranges of one buffer); one CUDA graph "
+                            "per step, two device buffer sets, a two-deep pipeline: while a step's kernels run, a "
+                            "second stream copies the next step's inputs in and the previous step's outputs out; "
+                            "n + 1 copies each way are timed for n steps"},
         "gpu_launches": launches,
         "clocks": clocks,
     }

@@ -232,8 +232,8 @@ qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_
         Span sw = span(p.w, (size_t)packed_bytes(p.wtype, p.N, p.K));
         REQUIRE(!overlap(sy, si) && !overlap(sy, sw), QK_ERR_ALIAS, "projection %d: y overlaps img or w", j);
         for (int i = 0; i < j; i++) {
-            Span so = span(projs[i].y, rows_span(T, projs[i].y_stride * 4, projs[i].N * 4));
-            REQUIRE(!overlap(sy, so), QK_ERR_ALIAS, "outputs of projections %d and %d overlap", i, j);
+            REQUIRE(!rows_overlap(projs[i].y, projs[i].y_stride * 4, projs[i].N * 4, p.y, p.y_stride * 4, p.N * 4, T),
+                    QK_ERR_ALIAS, "outputs of projections %d and %d overlap", i, j);
         }
     }
     REQUIRE(ws && aligned(ws, 16), QK_ERR_WORKSPACE, "workspace null or not 16-byte aligned");
@@ -354,8 +354,8 @@ qk_status qk_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int64_
         REQUIRE(!overlap(sy, sq) && !overlap(sy, sd) && !overlap(sy, span(p.w, (size_t)packed_bytes(p.wtype, p.N, p.K))),
                 QK_ERR_ALIAS, "projection %d: y overlaps an input", j);
         for (int i = 0; i < j; i++)
-            REQUIRE(!overlap(sy, span(projs[i].y, rows_span(T, projs[i].y_stride * 4, projs[i].N * 4))), QK_ERR_ALIAS,
-                    "outputs of projections %d and %d overlap", i, j);
+            REQUIRE(!rows_overlap(projs[i].y, projs[i].y_stride * 4, projs[i].N * 4, p.y, p.y_stride * 4, p.N * 4, T),
+                    QK_ERR_ALIAS, "outputs of projections %d and %d overlap", i, j);
     }
     const size_t need = qk_mmq_workspace_bytes(T, n_proj, projs);
     REQUIRE(ws && aligned(ws, 128), QK_ERR_WORKSPACE, "workspace null or not 128-byte aligned");

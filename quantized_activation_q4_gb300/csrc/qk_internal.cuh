@@ -29,6 +29,18 @@ inline size_t rows_span(int64_t rows, int64_t pitch_bytes, int64_t row_bytes) {
     return rows <= 0 ? 0 : (size_t)((rows - 1) * pitch_bytes + row_bytes);
 }
 
+// Whether two row sets (`rows` rows of la / lb bytes at pitches pa / pb) share a byte. Row sets
+// with one pitch whose column windows are disjoint within the pitch (the q, k and v outputs as
+// column ranges of one fused [T][N_q + N_k + N_v] buffer) do not overlap; any other pair whose
+// byte ranges meet counts as overlapping.
+inline bool rows_overlap(const void *a, int64_t pa, int64_t la, const void *b, int64_t pb, int64_t lb, int64_t rows) {
+    if (!overlap(span(a, rows_span(rows, pa, la)), span(b, rows_span(rows, pb, lb)))) return false;
+    if (rows <= 1 || pa != pb || la > pa || lb > pb) return true;
+    const int64_t diff = (int64_t)(reinterpret_cast<uintptr_t>(b) - reinterpret_cast<uintptr_t>(a));
+    const int64_t d = ((diff % pa) + pa) % pa;   // b's column offset within a's row period
+    return !(d >= la && d + lb <= pa);
+}
+
 // ------------------------------------------------------------- device side
 constexpr int QB = 32;           // elements per quant block
 constexpr int Q8_1_BYTES = 36;   // half d, half s, 32 codes

@@ -74,6 +74,14 @@ def test_projection_checks(lib):
     assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, P(WS), 1 << 20, None) == 1       # misaligned weights
     arr = (qk.qk_proj * 2)(good, qk.qk_proj(0, 0, W, 64, 256, Y + 128, 64))
     assert lib.qk_mmvq(P(IMG), 8, 8, 2, arr, None, P(WS), 1 << 20, None) == 3       # overlapping outputs
+    # column windows of one fused [T][64 + 32] output buffer: accepted (then the tiny workspace is refused)
+    fused = (qk.qk_proj * 2)(qk.qk_proj(0, 0, W, 64, 256, Y, 96), qk.qk_proj(0, 0, W, 32, 256, Y + 256, 96))
+    assert lib.qk_mmvq(P(IMG), 8, 8, 2, fused, None, P(WS), 16, None) == 4
+    # windows that share a column, or rows that wrap into the next row's window: refused
+    clash = (qk.qk_proj * 2)(qk.qk_proj(0, 0, W, 64, 256, Y, 96), qk.qk_proj(0, 0, W, 32, 256, Y + 252, 96))
+    assert lib.qk_mmvq(P(IMG), 8, 8, 2, clash, None, P(WS), 16, None) == 3
+    wrap = (qk.qk_proj * 2)(qk.qk_proj(0, 0, W, 64, 256, Y, 96), qk.qk_proj(0, 0, W, 64, 256, Y + 256, 96))
+    assert lib.qk_mmvq(P(IMG), 8, 8, 2, wrap, None, P(WS), 16, None) == 3
     arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W, 64, 256, IMG + 4, 64))
     assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, P(WS), 1 << 20, None) == 3       # output over the image
     arr = (qk.qk_proj * 1)(good)
