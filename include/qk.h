@@ -236,7 +236,9 @@ typedef struct qk_proj {
  *   Q8_0: y += d_w * d_a * D,              D = sum w_i * q_i
  *   img  [T][img_row_blocks] Q8_1; every projection's K <= 32*img_row_blocks
  *   T    1..8 image rows (tokens); rows >= *d_live_rows are not written
- *   projs host array of n_proj (1..8) descriptors; outputs must not overlap
+ *   projs host array of n_proj (1..8) descriptors; outputs must not share a
+ *        byte. Outputs with one y_stride may be disjoint column windows of
+ *        one buffer (q, k and v as columns of a fused [T][Nq+Nk+Nv] output).
  *   ws   device workspace of at least qk_mmvq_workspace_bytes(n_proj, projs)
  *        bytes, 16-byte aligned, ZEROED ONCE before its first use (e.g. by
  *        cudaMemset). It holds completion counters, which every call returns
@@ -354,7 +356,9 @@ QK_API qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t row
  * sections 1 and 5: the q/k/v and gate/up GEMMs that share one quantised A).
  *   qs [T][row_blocks*32] int8 and d [T][row_blocks] half: qk_quantize_q8_0
  *   C[t][n] = sum_b d_w[n][b] * d_a[t][b] * sum_{i in b} w_i * q_i
- *   (Q4_0: w_i = nibble - 8) written to projs[j].y ([T][y_stride] F32)
+ *   (Q4_0: w_i = nibble - 8) written to projs[j].y ([T][y_stride] F32);
+ *   outputs must not share a byte (disjoint column windows of one buffer
+ *   with one y_stride are allowed, as for qk_mmvq)
  * Runs on the tensor cores with binary16 operands (nibble - 8) * d_w and
  * q * d_a, each rounded once, accumulated in binary32: within about 2^-11
  * relative per product of the exact block form (NMSE ~1e-7).
