@@ -111,34 +111,42 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
 
 // ---------------------------------------------------------------- RMS producer
 // One CTA of 1024 threads per row; the row stays in registers between the
-// sum of squares and the output (thread i holds columns 4i + 4096*it, up to
-// RMS_ITEMS float4, so K <= 32768).
+// sum of squares and the output (thread i holds columns 4i + 4096*it for
+// it < ITEMS, ITEMS = 1, 2, 4 or 8 by K, so K <= 32768). With ITEMS <= 2 the
+// weight and bias are loaded together with the row, before the reduction.
 constexpr int RMS_THREADS = 1024;
 constexpr int RMS_ITEMS = 8;
 
+template <int ITEMS>
 __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
     const float *__restrict__ x, int K, int64_t x_stride, int kind, const float *__restrict__ w,
     const float *__restrict__ bias, float scale, float eps, float *__restrict__ y, int64_t y_stride,
     uint8_t *__restrict__ img, int64_t row_blocks, int T, const int32_t *live) {
+    constexpr bool EARLY = ITEMS <= 2;   // registers for the weight and bias next to the row
     pdl_trigger();
     pdl_wait();
     const int t = blockIdx.x;
     const float *xr = x + t * x_stride;
     const int tid = threadIdx.x, lane = tid & 31, j8 = lane & 7;
+    const bool use_w = kind == QK_NORM_MUL || kind == QK_NORM_MUL_ADD, use_b = kind == QK_NORM_MUL_ADD;
 
-    // the row is loaded together with the live count (row t < T is in the caller's buffer
-    // even when it is padding), so the two global reads overlap
-    float v[RMS_ITEMS][4];
+    // the row (and with EARLY its weight and bias) is loaded together with the live count (row
+    // t < T is in the caller's buffer even when it is padding), so the global reads overlap
+    float v[ITEMS][4], wv[EARLY ? ITEMS : 1][4], bv[EARLY ? ITEMS : 1][4];
 #pragma unroll
-    for (int it = 0; it < RMS_ITEMS; it++) {
+    for (int it = 0; it < ITEMS; it++) {
         const int c = 4 * tid + 4 * RMS_THREADS * it;
         v[it][0] = v[it][1] = v[it][2] = v[it][3] = 0.0f;
-        if (c < K) load4(xr + c, 4, v[it]);
+        if (c < K) {
+            load4(xr + c, 4, v[it]);
+            if (EARLY && use_w) load4(w + c, 4, wv[EARLY ? it : 0]);
+            if (EARLY && use_b) load4(bias + c, 4, bv[EARLY ? it : 0]);
+        }
     }
     if (t >= live_rows(live, T)) return;
     float ss = 0.0f;
 #pragma unroll
-    for (int it = 0; it < RMS_ITEMS; it++)
+    for (int it = 0; it < ITEMS; it++)
         ss += v[it][0] * v[it][0] + v[it][1] * v[it][1] + v[it][2] * v[it][2] + v[it][3] * v[it][3];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
@@ -157,20 +165,26 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
     float *yr = y + t * y_stride;
     uint8_t *ir = img + t * row_blocks * Q8_1_BYTES;
 #pragma unroll
-    for (int it = 0; it < RMS_ITEMS; it++) {
+    for (int it = 0; it < ITEMS; it++) {
         if (4 * RMS_THREADS * it >= K) break;               // uniform: no warp has columns left
         const int c = 4 * tid + 4 * RMS_THREADS * it;
         const bool ok = c < K;                               // K % 32 == 0: whole 8-lane groups agree
         float o[4] = {0.f, 0.f, 0.f, 0.f};
         if (ok) {
-            float wv[4], bv[4];
-            if (kind == QK_NORM_MUL || kind == QK_NORM_MUL_ADD) load4(w + c, 4, wv);
-            if (kind == QK_NORM_MUL_ADD) load4(bias + c, 4, bv);
+            float wl[4], bl[4];
+            const float *wq = wl, *bq = bl;
+            if (EARLY) {
+                wq = wv[EARLY ? it : 0];
+                bq = bv[EARLY ? it : 0];
+            } else {
+                if (use_w) load4(w + c, 4, wl);
+                if (use_b) load4(bias + c, 4, bl);
+            }
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 float q = v[it][i] * r;
-                if (kind == QK_NORM_MUL) q = q * wv[i];
-                else if (kind == QK_NORM_MUL_ADD) q = q * wv[i] + bv[i];
+                if (kind == QK_NORM_MUL) q = q * wq[i];
+                else if (kind == QK_NORM_MUL_ADD) q = q * wq[i] + bq[i];
                 else if (kind == QK_NORM_SCALE) q = q * scale;
                 o[i] = q;
             }
@@ -272,8 +286,13 @@ qk_status launch_rmsnorm_q8_1(const float *x, int T, int K, int64_t x_stride, in
                               int64_t y_stride, uint8_t *img, int64_t row_blocks,
                               const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
-    return launch_pdl("rmsnorm_q8_1", rmsnorm_q8_1_kernel, dim3((unsigned)T), dim3(RMS_THREADS), 0, s, x, K,
-                      x_stride, kind, w, b, scale, eps, y, y_stride, img, row_blocks, T, live);
+    const int per = 4 * RMS_THREADS;   // columns per item
+    auto kernel = K <= per ? rmsnorm_q8_1_kernel<1>
+                  : K <= 2 * per ? rmsnorm_q8_1_kernel<2>
+                  : K <= 4 * per ? rmsnorm_q8_1_kernel<4>
+                                 : rmsnorm_q8_1_kernel<RMS_ITEMS>;
+    return launch_pdl("rmsnorm_q8_1", kernel, dim3((unsigned)T), dim3(RMS_THREADS), 0, s, x, K, x_stride, kind, w, b,
+                      scale, eps, y, y_stride, img, row_blocks, T, live);
 }
 
 qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride, const float *b,
