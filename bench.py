@@ -82,6 +82,22 @@ def recorded_traffic():
     return rec["dram_bytes_per_launch"] if rec.get("sources") and h.hexdigest() == rec.get("sources_sha256") else None
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over the ranks (each rank a replica; the job's time is its slowest)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_step: int, ms_per_step: float) -> float:
+    """Whole-job weight-stream GB/s: every rank streams its own replica's bytes each step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -273,10 +289,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         raise RuntimeError(f"device fault word {faults:#x} after the timed region")
     ms_per_step = e_s0.elapsed_time(e_s1) / K
     comp_us = {name: e_c[name][0].elapsed_time(e_c[name][1]) * 1e3 / (KC * R) for name in comp_graphs}
-    if world > 1:
-        t = torch.tensor([ms_per_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(ms_per_step, world, "cuda")
 
     # ---------------------------------------------------------------- e2e through the C ABI, host buffers
     # Every step copies its inputs (x and x2, as column ranges of one [8][3584 + 8192] buffer) in from
@@ -352,7 +365,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         e2e_run(K, args.warmup)
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, "cuda")
     # the last step's outputs, as copied to the host, against the same step run by the device-timed path
     r_last = (args.warmup + K - 1) % R
     with torch.cuda.stream(stream):
@@ -365,7 +378,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     hbm = peaks["hbm_gbs"]
     us_a, us_b, us_m = comp_us["a"], comp_us["b"], comp_us["m"]
     achieved = MMVQ_BIG_BYTES / (us_m * 1e-6) / 1e9
-    value = world * W_STEP / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(world, W_STEP, ms_per_step)
     clocks = clk.summary()
     others = None if args.no_other_configs else other_configs(qk, synth, torch, dev, hbm, l2)
     if rank != 0:
@@ -405,7 +418,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                      "algorithmic_bytes_per_launch": MMVQ_BIG_BYTES, "traffic": recorded_traffic(),
                      "traffic_source": "profiles/mmvq_q4_0_8192x8192_t8.md (ncu, one launch; null if the "
                                        "kernel sources changed since)"},
-        "e2e": {"value": round(W_STEP / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 5),
+        "e2e": {"value": round(job_gbs(world, W_STEP, e2e_ms), 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "outputs_match_device_path": e2e_match,
                 "schedule": "every step copies x and x2 in from pinned host memory (one copy: column ranges of one "
