@@ -117,6 +117,14 @@ QK_API uint64_t qk_launch_count(void);
  */
 QK_API qk_status qk_device_faults(uint32_t *faults);
 
+/*
+ * Failure-path self-test: launches one CTA whose bounded wait on a
+ * shared-memory barrier that nothing completes runs out (about a second at
+ * most), sets bit 0 of the fault word and returns. The device stays usable;
+ * read the word with qk_device_faults. For tests of the timeout path.
+ */
+QK_API qk_status qk_selftest_wait_timeout(qk_stream stream);
+
 /* ------------------------------------------------------------ the image */
 
 /*

@@ -59,6 +59,7 @@ _SIGS = {
     "qk_weight_packed_bytes": ([C.c_int, I64, I64], SZ),
     "qk_weight_pack": ([C.c_int, P, I64, I64, P, SZ, P], C.c_int),
     "qk_device_faults": ([C.POINTER(C.c_uint32)], C.c_int),
+    "qk_selftest_wait_timeout": ([C.c_void_p], C.c_int),
     "qk_mmvq_workspace_bytes": ([I32, C.POINTER(qk_proj)], SZ),
     "qk_mmvq": ([P, I64, I64, I32, C.POINTER(qk_proj), P, P, SZ, P], C.c_int),
     "qk_mmvq_static_ws": ([P, I64, I64, I32, C.POINTER(qk_proj), P, P], C.c_int),
@@ -195,6 +196,10 @@ def qk_mmvq_static_ws(img, img_row_blocks, T, projs, d_live_rows=None, stream=No
     arr = (qk_proj * len(projs))(*projs)
     _check("qk_mmvq_static_ws", load().qk_mmvq_static_ws(_ptr(img), img_row_blocks, T, len(projs), arr,
                                                          _ptr(d_live_rows), _stream(stream)))
+
+
+def qk_selftest_wait_timeout(stream=None):
+    _check("qk_selftest_wait_timeout", load().qk_selftest_wait_timeout(_stream(stream)))
 
 
 def qk_device_faults() -> int:

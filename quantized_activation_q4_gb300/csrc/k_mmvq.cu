@@ -1037,6 +1037,21 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
     }
 }
 
+// ---------------------------------------------------------------- wait self-test
+// One warp waits, with the bounded wait every kernel here uses, on a
+// shared-memory barrier that nothing completes: the wait runs out (about a
+// second at most), sets bit 0 of the fault word and the kernel returns, so the
+// failure path can be checked on a device without faulting it.
+__global__ void __launch_bounds__(32) wait_selftest_kernel() {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) mbar_wait(smem_addr(&bar), 0u);   // no thread ever arrives
+}
+
 // ---------------------------------------------------------------- weight pack
 // One CTA of 256 threads per 128x128 unit. Canonical blocks are only 2-byte
 // aligned, so they are read byte by byte.
@@ -1121,6 +1136,12 @@ int64_t mmvq_workspace_bytes(int n_proj, const qk_proj *projs) {
     }
     const int64_t G = U < sm_count() ? U : sm_count();
     return G * 2 * VALS * (int64_t)sizeof(float) + R * (int64_t)sizeof(unsigned int);
+}
+
+qk_status launch_wait_selftest(cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>();
+    count_launch();
+    return check_launch("wait_selftest");
 }
 
 qk_status read_device_faults(uint32_t *faults) {

@@ -214,6 +214,8 @@ qk_status qk_device_faults(uint32_t *faults) {
     return st;
 }
 
+qk_status qk_selftest_wait_timeout(qk_stream stream) { return launch_wait_selftest((cudaStream_t)stream); }
+
 qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_proj, const qk_proj *projs,
                   const int32_t *d_live_rows, void *ws, size_t ws_bytes, qk_stream stream) {
     REQUIRE(img && projs, QK_ERR_ARG, "null pointer");

@@ -95,6 +95,8 @@ int sm_count();
 // Reads and clears the device-side fault word (bit 0: a bounded mbarrier
 // wait gave up). Synchronous.
 qk_status read_device_faults(uint32_t *faults);
+// One CTA whose bounded wait runs out and sets bit 0 of the fault word.
+qk_status launch_wait_selftest(cudaStream_t s);
 
 // Launch with programmatic stream serialization (see pdl_trigger/pdl_wait).
 template <typename... KArgs, typename... Args>
