@@ -694,26 +694,39 @@ def cpu_baseline(big_rows: int = 2048, budget_s: float = 10.0) -> dict:
             "seconds_per_sample_step": round(dt, 3), "c4_prefill": cpu_prefill_sample()}
 
 
-def cpu_prefill_sample(cols: int = 64) -> dict:
-    """The oracle's quantised-path prefill contraction (config 4) on a bounded sample:
-    all 3325 tokens of the Q8_0 image against `cols` output columns of the q weight
-    (3584 x 3584), single thread; the per-layer time is an extrapolation by ops."""
+def _prefill_cols(args):
+    """One worker's share of the prefill oracle sample: its columns of the q weight for all tokens."""
+    cols, TP, DP = args
+    sys.path.insert(0, ROOT)
     from oracle import oracle as O
     from quantized_activation_q4_gb300 import synth
-    TP, DP = 3325, 3584
     x = synth.activations(130, TP, DP)
     qs, dh = O.quantize_q8_0(x)
     W = synth.q4_0_weight(800, DP, DP)
-    rows = np.arange(TP)
-    cs = np.arange(cols)
-    O.proj_q8_0_sampled("q4_0", W, DP, DP, qs, dh, DP // 32, rows[:8], cs)   # build + warm
     t0 = time.perf_counter()
-    O.proj_q8_0_sampled("q4_0", W, DP, DP, qs, dh, DP // 32, rows, cs)
-    dt = time.perf_counter() - t0
-    ops = 2 * TP * cols * DP
+    O.proj_q8_0_sampled("q4_0", W, DP, DP, qs, dh, DP // 32, np.arange(TP), np.asarray(cols))
+    return time.perf_counter() - t0
+
+
+def cpu_prefill_sample(cols_per_core: int = 16) -> dict:
+    """The oracle's quantised-path prefill contraction (config 4) on a bounded sample, on all host
+    cores (one spawned process per core, each computing all 3325 tokens for its own columns of the
+    q weight, 3584 x 3584); the per-layer time is an extrapolation by ops."""
+    import multiprocessing as mp
+    TP, DP = 3325, 3584
+    cores = max(1, min(os.cpu_count() or 1, 64))
+    jobs = [(list(range(c * cols_per_core, (c + 1) * cols_per_core)), TP, DP) for c in range(cores)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.map(_prefill_cols, jobs[:cores])          # build + warm every worker
+        t0 = time.perf_counter()
+        pool.map(_prefill_cols, jobs)
+        dt = time.perf_counter() - t0
+    ops = 2 * TP * cols_per_core * cores * DP
     layer_ops = 2 * TP * DP * (3584 + 512 + 512 + 2 * 18944)
-    return {"gop_per_s": round(ops / dt / 1e9, 3), "cores": 1, "kind": "oracle",
-            "sample": f"{TP} tokens x {cols} of 3584 q columns, K=3584 ({ops / 1e9:.2f} GOP, {dt:.2f} s)",
+    return {"gop_per_s": round(ops / dt / 1e9, 3), "cores": cores, "kind": "oracle",
+            "sample": f"{TP} tokens x {cols_per_core * cores} of 3584 q columns, K=3584, {cores} processes "
+                      f"({ops / 1e9:.2f} GOP, {dt:.2f} s)",
             "layer_seconds_extrapolated": round(layer_ops / (ops / dt), 1)}
 
 
