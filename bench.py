@@ -597,7 +597,15 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
                 rimg, DR // 32, bucket, KTOP, [qk.make_proj_id("q4_0", E, experts[r][pj], NE, DR, ys[pj])
                                                for pj in range(2)], counts, offsets, items)
                 for r in list(range(R3)) * 8], 10)}
-        c3[f"live{live}_bucket{bucket}"] = {"us": round(us_3, 3), "distinct_experts": touched, "weight_bytes": wb,
+        def routed_fused(r):   # the same chain with top-k and plan in one launch (qk_route_plan)
+            qk.qk_rmsnorm_q8_1(xr, bucket, DR, DR, "mul", wr, None, 1.0, 1e-6, yr, DR, rimg, DR // 32, d_live_rows=lv)
+            qk.qk_route_plan(logits, bucket, E, KTOP, ids, wts, counts, offsets, items, d_live_rows=lv)
+            qk.qk_mmvq_id(rimg, DR // 32, bucket, KTOP, [qk.make_proj_id("q4_0", E, experts[r][pj], NE, DR, ys[pj])
+                                                          for pj in range(2)], counts, offsets, items)
+
+        us_3f = _graph_us(torch, stream, [lambda r=r: routed_fused(r) for r in range(R3)], 10)
+        c3[f"live{live}_bucket{bucket}"] = {"us": round(us_3, 3), "us_route_plan_one_launch": round(us_3f, 3),
+                                            "distinct_experts": touched, "weight_bytes": wb,
                                             "weight_gbs": gb(wb, us_3),
                                             "kernels": ["rmsnorm_q8_1", "topk_route", "moe_plan", "mmvq_id(gate,up)"],
                                             "per_kernel_us": {k: round(v, 3) for k, v in per_kernel.items()},

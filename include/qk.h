@@ -329,6 +329,17 @@ QK_API qk_status qk_moe_plan(const int32_t *ids, int64_t rows, int32_t k, int32_
                       int32_t *counts, int32_t *offsets, int32_t *items,
                       const int32_t *d_live_rows, qk_stream stream);
 
+/*
+ * qk_route_plan -- qk_topk_route then qk_moe_plan, in one launch when the
+ * bucket has at most 32 rows (one CTA: a warp per row, then the plan), else
+ * as the two launches. Outputs (ids, wts, counts, offsets, items) are the
+ * same bytes as the two calls'; arguments and limits as theirs (E <= 256).
+ * Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED, QK_ERR_ALIAS.
+ */
+QK_API qk_status qk_route_plan(const float *logits, int64_t rows, int32_t E, int32_t k, int32_t *ids,
+                               float *wts, int32_t *counts, int32_t *offsets, int32_t *items,
+                               const int32_t *d_live_rows, qk_stream stream);
+
 /* One routed projection: E experts' packed weights back to back. */
 typedef struct qk_proj_id {
     int32_t wtype;          /* qk_wtype */

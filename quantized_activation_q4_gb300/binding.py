@@ -65,6 +65,7 @@ _SIGS = {
     "qk_mmvq_static_ws": ([P, I64, I64, I32, C.POINTER(qk_proj), P, P], C.c_int),
     "qk_topk_route": ([P, I64, I32, I32, P, P, P, P], C.c_int),
     "qk_moe_plan": ([P, I64, I32, I32, P, P, P, P, P], C.c_int),
+    "qk_route_plan": ([P, I64, I32, I32, P, P, P, P, P, P, P], C.c_int),
     "qk_mmvq_id": ([P, I64, I64, I32, I32, C.POINTER(qk_proj_id), P, P, P, P], C.c_int),
     "qk_mmq_workspace_bytes": ([I64, I32, C.POINTER(qk_proj)], C.c_size_t),
     "qk_mmq": ([P, P, I64, I64, I32, C.POINTER(qk_proj), P, C.c_size_t, P], C.c_int),
@@ -234,3 +235,8 @@ def qk_topk_route(logits, rows, E, k, ids, wts, d_live_rows=None, stream=None):
 def qk_moe_plan(ids, rows, k, E, counts, offsets, items, d_live_rows=None, stream=None):
     _check("qk_moe_plan", load().qk_moe_plan(_ptr(ids), rows, k, E, _ptr(counts), _ptr(offsets), _ptr(items),
                                              _ptr(d_live_rows), _stream(stream)))
+
+
+def qk_route_plan(logits, rows, E, k, ids, wts, counts, offsets, items, d_live_rows=None, stream=None):
+    _check("qk_route_plan", load().qk_route_plan(_ptr(logits), rows, E, k, _ptr(ids), _ptr(wts), _ptr(counts),
+                                                 _ptr(offsets), _ptr(items), _ptr(d_live_rows), _stream(stream)))

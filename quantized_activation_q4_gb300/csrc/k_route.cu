@@ -10,6 +10,7 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int MAX_E_PER_LANE = 8;   // E <= 256
+constexpr int ROUTE_PLAN_MAX_ROWS = 32;   // fused top-k + plan: one row per warp of one CTA
 
 // ---------------------------------------------------------------- top-k
 // One warp per row; lane l holds experts l, l+32, ... Ranking by logit,
@@ -29,24 +30,9 @@ __device__ __forceinline__ float key_value(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int rows, int E,
-                                                   int k, int32_t *__restrict__ ids,
-                                                   float *__restrict__ wts, const int32_t *live) {
-    pdl_trigger();
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (r >= rows) return;   // warp-uniform
-    // the row's logits are loaded together with the live count (row r < rows is in the
-    // caller's buffer even when it is padding), so the two global reads overlap
-    const float *l = logits + (int64_t)r * E;
-    float v[MAX_E_PER_LANE];
-#pragma unroll
-    for (int i = 0; i < MAX_E_PER_LANE; i++) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? __ldg(l + e) : -INFINITY;
-    }
-    if (r >= live_rows(live, rows)) return;   // warp-uniform
+// Top-k of row r (one warp): the logits are already in v (lane l: experts l, l+32, ...).
+__device__ __forceinline__ void topk_row(const float v[MAX_E_PER_LANE], int r, int E, int k, int lane,
+                                         int32_t *__restrict__ ids, float *__restrict__ wts) {
     unsigned key[MAX_E_PER_LANE];
     float mx = -INFINITY;
 #pragma unroll
@@ -87,6 +73,32 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     }
 }
 
+__device__ __forceinline__ void load_logits(const float *__restrict__ logits, int r, int E, int lane,
+                                            float v[MAX_E_PER_LANE]) {
+    const float *l = logits + (int64_t)r * E;
+#pragma unroll
+    for (int i = 0; i < MAX_E_PER_LANE; i++) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldg(l + e) : -INFINITY;
+    }
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int rows, int E,
+                                                   int k, int32_t *__restrict__ ids,
+                                                   float *__restrict__ wts, const int32_t *live) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= rows) return;   // warp-uniform
+    // the row's logits are loaded together with the live count (row r < rows is in the
+    // caller's buffer even when it is padding), so the two global reads overlap
+    float v[MAX_E_PER_LANE];
+    load_logits(logits, r, E, lane, v);
+    if (r >= live_rows(live, rows)) return;   // warp-uniform
+    topk_row(v, r, E, k, lane, ids, wts);
+}
+
 // ---------------------------------------------------------------- plan
 // One CTA of 1024 threads (32 warps) for any width. Warp w owns a contiguous
 // segment of the live pairs. Pass 1 counts each segment per expert (warp
@@ -95,18 +107,14 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 // segment in order and scatters, so each expert's items come out in
 // ascending pair order (a stable counting sort). Pairs naming an expert
 // outside [0, E) are left out of the plan.
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ ids, int rows, int k,
-                                                    int E, int32_t *__restrict__ counts,
-                                                    int32_t *__restrict__ offsets,
-                                                    int32_t *__restrict__ items, const int32_t *live) {
-    extern __shared__ int32_t sm[];
+// The plan of the first npairs pairs of ids, by one CTA of 1024 threads (ids read with plain
+// loads: in the fused launch this CTA wrote them). sm: 32 * E + E + 1 ints of dynamic shared memory.
+__device__ __forceinline__ void plan_body(const int32_t *ids, int npairs, int E, int32_t *__restrict__ counts,
+                                          int32_t *__restrict__ offsets, int32_t *__restrict__ items,
+                                          int32_t *sm, int32_t *wsum) {
     int32_t *seg = sm;                 // [32][E] per-warp counts, then per-warp bases
     int32_t *off = sm + 32 * E;        // [E + 1]
-    __shared__ int32_t wsum[32];
-    pdl_trigger();
-    pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int npairs = live_rows(live, rows) * k;
     const int per = (npairs + 31) / 32;
     const int p_begin = warp * per, p_end = min(npairs, p_begin + per);
     const unsigned lt = (1u << lane) - 1u;
@@ -116,7 +124,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
 
     for (int p0 = p_begin; p0 < p_end; p0 += 32) {
         const int p = p0 + lane;
-        const int e = p < p_end ? __ldg(ids + p) : -1;
+        const int e = p < p_end ? ids[p] : -1;
         const bool ok = e >= 0 && e < E;
         const unsigned m = __match_any_sync(FULL, ok ? e : -1);
         if (ok && (m & lt) == 0) seg[warp * E + e] += __popc(m);
@@ -166,7 +174,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
 
     for (int p0 = p_begin; p0 < p_end; p0 += 32) {
         const int p = p0 + lane;
-        const int e = p < p_end ? __ldg(ids + p) : -1;
+        const int e = p < p_end ? ids[p] : -1;
         const bool ok = e >= 0 && e < E;
         const unsigned m = __match_any_sync(FULL, ok ? e : -1);
         if (ok) {
@@ -179,6 +187,37 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
     }
 }
 
+
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ ids, int rows, int k,
+                                                    int E, int32_t *__restrict__ counts,
+                                                    int32_t *__restrict__ offsets,
+                                                    int32_t *__restrict__ items, const int32_t *live) {
+    extern __shared__ int32_t sm[];
+    __shared__ int32_t wsum[32];
+    pdl_trigger();
+    pdl_wait();
+    plan_body(ids, live_rows(live, rows) * k, E, counts, offsets, items, sm, wsum);
+}
+
+// Top-k and plan in one CTA of 1024 threads for buckets of up to 32 rows (one row per warp):
+// the same ids, weights and plan as the two launches, one launch boundary fewer on the path.
+__global__ void __launch_bounds__(1024) route_plan_kernel(const float *__restrict__ logits, int rows, int E, int k,
+                                                          int32_t *ids, float *__restrict__ wts,
+                                                          int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                                          int32_t *__restrict__ items, const int32_t *live) {
+    extern __shared__ int32_t sm[];
+    __shared__ int32_t wsum[32];
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, r = threadIdx.x >> 5;
+    float v[MAX_E_PER_LANE];
+    if (r < rows) load_logits(logits, r, E, lane, v);
+    const int n_live = live_rows(live, rows);
+    if (r < n_live) topk_row(v, r, E, k, lane, ids, wts);
+    __syncthreads();   // this CTA's ids are visible to all its threads
+    plan_body(ids, n_live * k, E, counts, offsets, items, sm, wsum);
+}
+
 }  // namespace
 
 qk_status launch_topk_route(const float *logits, int rows, int E, int k, int32_t *ids, float *wts,
@@ -186,6 +225,22 @@ qk_status launch_topk_route(const float *logits, int rows, int E, int k, int32_t
     if (rows == 0) return QK_OK;
     return launch_pdl("topk_route", topk_kernel, dim3((unsigned)ceil_div(rows, 8)), dim3(256), 0, s, logits, rows,
                       E, k, ids, wts, live);
+}
+
+qk_status launch_route_plan(const float *logits, int rows, int E, int k, int32_t *ids, float *wts, int32_t *counts,
+                            int32_t *offsets, int32_t *items, const int32_t *live, cudaStream_t s) {
+    if (rows > ROUTE_PLAN_MAX_ROWS) {   // one row per warp in one CTA: larger buckets use the two launches
+        qk_status st = launch_topk_route(logits, rows, E, k, ids, wts, live, s);
+        return st != QK_OK ? st : launch_moe_plan(ids, rows, k, E, counts, offsets, items, live, s);
+    }
+    const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
+    static int configured = 0;
+    if (smem > 48 * 1024 && configured < (int)smem) {
+        cudaFuncSetAttribute(route_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        configured = (int)smem;
+    }
+    return launch_pdl("route_plan", route_plan_kernel, dim3(1), dim3(1024), smem, s, logits, rows, E, k, ids, wts,
+                      counts, offsets, items, live);
 }
 
 qk_status launch_moe_plan(const int32_t *ids, int rows, int k, int E, int32_t *counts,

@@ -331,6 +331,27 @@ qk_status qk_moe_plan(const int32_t *ids, int64_t rows, int32_t k, int32_t E, in
     return launch_moe_plan(ids, (int)rows, k, E, counts, offsets, items, d_live_rows, (cudaStream_t)stream);
 }
 
+qk_status qk_route_plan(const float *logits, int64_t rows, int32_t E, int32_t k, int32_t *ids, float *wts,
+                        int32_t *counts, int32_t *offsets, int32_t *items, const int32_t *d_live_rows,
+                        qk_stream stream) {
+    REQUIRE(logits && ids && wts && counts && offsets && items, QK_ERR_ARG, "null pointer");
+    REQUIRE(rows >= 0 && rows <= (1 << 24) && E >= 1 && k >= 1, QK_ERR_ARG, "rows, E or k out of range");
+    REQUIRE(E <= 256 && k <= 32 && k <= E, QK_ERR_UNSUPPORTED, "E=%d k=%d (need E <= 256, k <= min(32, E))", E, k);
+    Span sl = span(logits, (size_t)(rows * E * 4));
+    Span si = span(ids, (size_t)(rows * k * 4));
+    Span sw = span(wts, (size_t)(rows * k * 4));
+    Span sc = span(counts, (size_t)E * 4), so = span(offsets, (size_t)(E + 1) * 4);
+    Span sit = span(items, (size_t)(rows * k * 4));
+    const Span outs[5] = {si, sw, sc, so, sit};
+    for (int a = 0; a < 5; a++) {
+        REQUIRE(!overlap(outs[a], sl), QK_ERR_ALIAS, "an output overlaps logits");
+        for (int b = 0; b < a; b++) REQUIRE(!overlap(outs[a], outs[b]), QK_ERR_ALIAS, "outputs overlap each other");
+    }
+    if (rows == 0) return QK_OK;
+    return launch_route_plan(logits, (int)rows, E, k, ids, wts, counts, offsets, items, d_live_rows,
+                             (cudaStream_t)stream);
+}
+
 // ------------------------------------------------------------------ prefill
 size_t qk_mmq_workspace_bytes(int64_t T, int32_t n_proj, const qk_proj *projs) {
     if (T < 1 || n_proj < 1 || n_proj > 8 || !projs) return 0;

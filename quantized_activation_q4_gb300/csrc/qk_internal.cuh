@@ -144,6 +144,9 @@ qk_status launch_topk_route(const float *logits, int rows, int E, int k, int32_t
                             float *wts, const int32_t *live, cudaStream_t s);
 qk_status launch_moe_plan(const int32_t *ids, int rows, int k, int E, int32_t *counts,
                           int32_t *offsets, int32_t *items, const int32_t *live, cudaStream_t s);
+// Top-k then plan in one launch (buckets of up to 32 rows; larger ones take the two launches).
+qk_status launch_route_plan(const float *logits, int rows, int E, int k, int32_t *ids, float *wts, int32_t *counts,
+                            int32_t *offsets, int32_t *items, const int32_t *live, cudaStream_t s);
 qk_status launch_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int T, int n_proj,
                      const qk_proj *projs, void *ws, size_t ws_bytes, cudaStream_t s);
 int64_t mmq_workspace_bytes(int64_t T, int64_t kmax);

@@ -226,3 +226,33 @@ def test_routed_widths_passes_and_ragged_tiles(wtype, n_exp, k):
         ref = O.proj_id_q8_1(wtype, np.concatenate(Ws[j], axis=0), n_exp, N, Kp, img_h, Kp // 32, ids_h, rit)
         assert O.nmse(got[planned], ref[planned]) <= 1e-10
         assert np.all(got[~planned] == SENTINEL)
+
+
+@pytest.mark.parametrize("rows,live,E_,k", [(16, 1, 128, 8), (16, 9, 128, 8), (32, 17, 128, 8), (32, 32, 256, 8),
+                                            (16, 0, 128, 8), (8, 5, 37, 4), (128, 113, 128, 8)])
+def test_route_plan_one_launch_equals_the_two_calls(rows, live, E_, k):
+    """qk_route_plan (one CTA up to 32 rows, else the two launches) writes the same bytes as
+    qk_topk_route followed by qk_moe_plan, and both match the oracle."""
+    import torch
+    logits = synth.poison_rows(synth.router_logits(9600 + rows + live, rows, E_), live)
+    stale = synth.stale_ids(9601, rows, k, E_)
+    l_d = dev(logits)
+
+    def fresh():
+        return (dev(stale.copy()), torch.full((rows, k), float("nan"), dtype=torch.float32, device="cuda"),
+                torch.full((E_,), -7, dtype=torch.int32, device="cuda"),
+                torch.full((E_ + 1,), -7, dtype=torch.int32, device="cuda"),
+                torch.full((rows * k,), -7, dtype=torch.int32, device="cuda"))
+
+    a = fresh()
+    qk.qk_topk_route(l_d, rows, E_, k, a[0], a[1], live_ptr(live))
+    qk.qk_moe_plan(a[0], rows, k, E_, a[2], a[3], a[4], live_ptr(live))
+    b = fresh()
+    qk.qk_route_plan(l_d, rows, E_, k, b[0], b[1], b[2], b[3], b[4], live_ptr(live))
+    ha, hb = [host(t) for t in a], [host(t) for t in b]
+    for x, y in zip(ha, hb):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    ri, rw = O.topk_route(logits[:live], k)
+    assert np.array_equal(hb[0][:live], ri)
+    rc, ro, rit = O.moe_plan(hb[0], E_, live=live)
+    assert np.array_equal(hb[2], rc) and np.array_equal(hb[3], ro) and np.array_equal(hb[4][:live * k], rit)
