@@ -290,11 +290,32 @@ __device__ __forceinline__ void dot_q8(uint4 v, const BSide &s, float d[4]) {
 }
 
 __device__ __forceinline__ void scale_epilogue(const float dv[4], uint32_t dw2, const BSide &s, float acc[4]) {
-    const float2 dw = __half22float2(as_h2(dw2));   // (row g, row g+8)
-    acc[0] = fmaf(dw.x, fmaf(s.da0, dv[0], s.ns0), acc[0]);
-    acc[1] = fmaf(dw.x, fmaf(s.da1, dv[1], s.ns1), acc[1]);
-    acc[2] = fmaf(dw.y, fmaf(s.da0, dv[2], s.ns0), acc[2]);
-    acc[3] = fmaf(dw.y, fmaf(s.da1, dv[3], s.ns1), acc[3]);
+    // acc[i] += dw_row * (d_a * D + ns), the token pair's operations two at a time (fma.rn.f32x2:
+    // the same correctly rounded fma per lane as fmaf, in half the issue slots)
+    asm("{\n"
+        ".reg .b16 hx, hy;\n"
+        ".reg .f32 wx, wy;\n"
+        ".reg .b64 DA, NS, D01, D23, T01, T23, WX, WY, A01, A23;\n"
+        "mov.b32 {hx, hy}, %10;\n"
+        "cvt.f32.f16 wx, hx;\n"
+        "cvt.f32.f16 wy, hy;\n"
+        "mov.b64 DA, {%6, %7};\n"
+        "mov.b64 NS, {%8, %9};\n"
+        "mov.b64 D01, {%4, %5};\n"
+        "mov.b64 D23, {%11, %12};\n"
+        "fma.rn.f32x2 T01, DA, D01, NS;\n"
+        "fma.rn.f32x2 T23, DA, D23, NS;\n"
+        "mov.b64 WX, {wx, wx};\n"
+        "mov.b64 WY, {wy, wy};\n"
+        "mov.b64 A01, {%0, %1};\n"
+        "mov.b64 A23, {%2, %3};\n"
+        "fma.rn.f32x2 A01, WX, T01, A01;\n"
+        "fma.rn.f32x2 A23, WY, T23, A23;\n"
+        "mov.b64 {%0, %1}, A01;\n"
+        "mov.b64 {%2, %3}, A23;\n"
+        "}\n"
+        : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
+        : "f"(dv[0]), "f"(dv[1]), "f"(s.da0), "f"(s.da1), "f"(s.ns0), "f"(s.ns1), "r"(dw2), "f"(dv[2]), "f"(dv[3]));
 }
 
 // All 8 row groups of one block, from shared memory (SMEM, 32-bit shared
