@@ -23,15 +23,19 @@
 //
 // Ordinary path: one persistent CTA per SM. A producer warp streams 128x128
 // weight units with TMA bulk copies (cp.async.bulk, L2 evict-first) into a
-// ring of shared-memory slots guarded by full/empty mbarriers; 15 consumer
-// warps take the units' 32-column blocks round-robin (block j of the CTA's
-// range goes to warp j mod 15), each computing all 128 rows x 8 tokens of its
-// block. Work is split by equal bytes over the CTAs (stream-K): a row tile
-// cut between CTAs leaves partial sums in a small caller workspace (written
-// when the CTA has finished its whole range, so no consumer waits on global
-// memory mid-stream), and the last CTA to publish its part (atomic counter,
-// reset after use) adds the parts in CTA order. All sums run in a fixed order, so results do not depend on
-// timing or on the live-row count.
+// ring of shared-memory slots guarded by full/empty mbarriers; 16 consumer
+// warps form four unit phases (the CTA's units with index = phase mod 4), and
+// in a phase warp p does rows 32p..32p+31 of all four blocks of the unit after
+// the phase's four warps have each turned one block's image words into a
+// shared activation record. Work is split by equal bytes over the CTAs
+// (stream-K): a row tile cut between CTAs is finished by its owner (the CTA
+// holding its first unit), which adds the other CTAs' parts from a small
+// caller workspace in CTA order; if they are late, the owner publishes its
+// part too and the last contributor adds them, in the same order. All sums run
+// in a fixed order, so results do not depend on timing or on the live-row
+// count.
+//
+// Routed path: see mmvq_id_kernel.
 
 #include <cstdlib>
 #include <mutex>
