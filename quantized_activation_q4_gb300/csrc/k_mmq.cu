@@ -17,7 +17,7 @@
 //   dequant_b: the image -> B, [T][K] binary16 in the caller's workspace,
 //     once per call (it is read by every 128-row weight tile).
 //   mmq_tc: persistent, one CTA per SM, tiles of (projection, 128-row weight
-//     tile, 208-token tile) taken round-robin, tokens fastest so that the CTAs
+//     tile, 256-token tile) taken round-robin, tokens fastest so that the CTAs
 //     running at one time share a few weight row tiles through L2.
 //     warp 0: TMA -- the B tiles (2D tensor copies, 128-byte swizzle) and the
 //             packed weight units (bulk copies) into shared-memory rings, with
@@ -26,10 +26,13 @@
 //             memory (tcgen05.st; two warps per 32-lane quarter, one 32-block
 //             each), so the MMAs read A from tensor memory and only B from
 //             shared memory;
-//     warp 1: allocates tensor memory (two 208-column accumulators and three
+//     warp 1: allocates tensor memory (one 256-column accumulator and five
 //             32-column A stages) and issues the MMAs (one thread);
-//     warps 10-13: read a finished accumulator and store C while the MMAs of
-//             the next tile run into the other one.
+//     warps 10-17: read the finished accumulator (two 64-column loads per
+//             warp), release it to the next tile's MMAs as soon as the loads
+//             are done, then store C. (Two 208-column accumulators leave room
+//             for only three A stages; five stages at 256 tokens measured 11%
+//             faster on the gate/up launch.)
 // Within a 32-block the K positions follow the order in which the converters
 // store a packed weight word (column 2t+p: elements 4t+p and 4t+p+2; column
 // 8+2t+p: elements 16+4t+p and 18+4t+p); dequant_b writes B in the same order.
@@ -44,16 +47,16 @@ namespace {
 
 constexpr int MAX_PROJ = 8;
 constexpr int TM = 128;              // weight rows per CTA (MMA M)
-constexpr int TN = 208;              // tokens per CTA (MMA N; 3325 tokens = 16 tiles)
+constexpr int TN = 256;              // tokens per CTA (MMA N; 3325 tokens = 13 tiles)
 constexpr int KC = 64;               // K elements per stage (one 128-byte swizzle row of f16)
-constexpr int NS = 3;                // stages (A in tensor memory, B in shared memory)
+constexpr int NS = 5;                // stages (A in tensor memory, B in shared memory)
 constexpr int NU = 6;                // packed-unit staging slots (a unit = 2 stages)
 constexpr int PF = 10;               // units prefetched into L2 ahead of the one being loaded
-constexpr int B_TILE = TN * KC * 2;  // 26 KB
+constexpr int B_TILE = TN * KC * 2;  // 32 KB
 constexpr uint32_t A_COLS = KC / 2;  // tensor-memory columns of one A stage (two f16 per column)
-constexpr int EPI0 = 10;             // first epilogue warp
-constexpr int THREADS = 14 * 32;
-constexpr uint32_t A_TMEM = 2 * TN;       // A stages follow the two accumulators
+constexpr int EPI0 = 10;             // first epilogue warp (8 epilogue warps)
+constexpr int THREADS = 18 * 32;
+constexpr uint32_t A_TMEM = TN;           // A stages follow the accumulator
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(A_TMEM + NS * A_COLS <= TMEM_COLS, "tensor memory");
 constexpr uint32_t SPIN_LIMIT = 1u << 16;
@@ -63,12 +66,12 @@ constexpr uint32_t SUSPEND_NS = 20000;
 constexpr int OFF_B = 0;
 constexpr int OFF_U = OFF_B + NS * B_TILE;
 constexpr int OFF_BAR = OFF_U + NU * Q4_UNIT_BYTES;
-// full_a[NS] full_b[NS] empty[NS] ufull[NU] uempty[NU] acc_full[2] acc_empty[2]
-constexpr int N_BARS = 3 * NS + 2 * NU + 4;
+// full_a[NS] full_b[NS] empty[NS] ufull[NU] uempty[NU] acc_full acc_empty
+constexpr int N_BARS = 3 * NS + 2 * NU + 2;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + slack to align the base to 1024
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
-// instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 208, M = 128
+// instruction descriptor: f32 accumulator, f16 A and B, both K-major, N = 256, M = 128
 constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
 
 __device__ unsigned int g_mmq_faults = 0;
@@ -80,7 +83,7 @@ struct MmqProj {
     int N, K, chunks, row_tiles, rt_begin;   // rt_begin: first global row tile
 };
 struct MmqArgs {
-    CUtensorMap bmap;    // B [T][K] f16, box 64 x 208, 128-byte swizzle
+    CUtensorMap bmap;    // B [T][K] f16, box 64 x 256, 128-byte swizzle
     int T, n_proj, tok_tiles, tiles;
     MmqProj p[MAX_PROJ];
 };
@@ -213,7 +216,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
     const uint32_t sbase = smem_u32(smem);
     const uint32_t full_a = sbase + OFF_BAR, full_b = full_a + NS * 8, empty = full_b + NS * 8;
     const uint32_t ufull = empty + NS * 8, uempty = ufull + NU * 8, acc_full = uempty + NU * 8,
-                   acc_empty = acc_full + 16;
+                   acc_empty = acc_full + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + N_BARS * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -229,13 +232,11 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
             mbar_init(ufull + 8 * u, 1);
             mbar_init(uempty + 8 * u, 256);
         }
-        for (int b = 0; b < 2; b++) {
-            mbar_init(acc_full + 8 * b, 1);      // the MMA commit after a tile's last stage
-            mbar_init(acc_empty + 8 * b, 128);   // the four epilogue warps
-        }
+        mbar_init(acc_full, 1);      // the MMA commit after a tile's last stage
+        mbar_init(acc_empty, 256);   // the eight epilogue warps, once they have read it
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {   // tensor memory: accumulators (2 x 208 columns) and A stages (3 x 32 columns)
+    if (warp == 1) {   // tensor memory: the accumulator (256 columns) and A stages (5 x 32 columns)
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
                      : "memory");
@@ -303,8 +304,8 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
             bool ok = true;
             for (int tau = blockIdx.x; tau < a.tiles && ok; tau += G, i++) {
                 const Tile t = tile_of(a, tau);
-                const uint32_t ab = i & 1, acc = tmem + ab * TN;
-                if (i >= 2 && !mbar_wait(acc_empty + 8 * ab, ((i >> 1) - 1) & 1u)) break;
+                const uint32_t acc = tmem;
+                if (i >= 1 && !mbar_wait(acc_empty, (i - 1) & 1u)) break;
                 tc_fence_after();
                 for (int kc = 0; kc < t.nkc; kc++, g++) {
                     const uint32_t s = g % NS, par = (g / NS) & 1u;
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                         tc_mma(acc, at + 8 * ks, sdesc(bt + 32 * ks), (kc | ks) != 0);
                     tc_commit(empty + 8 * s);   // frees the stage once these MMAs are done
                 }
-                if (ok) tc_commit(acc_full + 8 * ab);   // the accumulator is final once its MMAs are done
+                if (ok) tc_commit(acc_full);   // the accumulator is final once its MMAs are done
             }
         }
     } else if (warp < EPI0) {   // ---------------- warps 2..9: A conversion into tensor memory
@@ -370,39 +371,48 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                 }
             }
         }
-    } else {   // ---------------- warps 10..13: epilogue (accumulator lane = tile row, column = token)
-        const int quad = warp & 3;
+    } else {   // ---------------- warps 10..17: epilogue (accumulator lane = tile row, column = token)
+        // warp w reads lanes 32 (w % 4).. of columns 128 ((w - 10) / 4) ..+127, releases the
+        // accumulator as soon as its last load is done, then stores the last chunk
+        const int quad = warp & 3, c_half = ((warp - EPI0) >> 2) * (TN / 2);
         int i = 0;
         for (int tau = blockIdx.x; tau < a.tiles; tau += G, i++) {
             const Tile t = tile_of(a, tau);
             const MmqProj &P = a.p[t.j];
-            const uint32_t ab = i & 1;
-            if (!mbar_wait(acc_full + 8 * ab, (i >> 1) & 1u)) break;
+            if (!mbar_wait(acc_full, i & 1u)) break;
             tc_fence_after();
             const int row = t.rt * TM + quad * 32 + lane;
 #pragma unroll 1
-            for (int c0 = 0; c0 < TN; c0 += 32) {   // the last load runs past TN: those columns are not stored
-                uint32_t v[32];
+            for (int c0 = c_half; c0 < c_half + TN / 2; c0 += 64) {
+                uint32_t v[64];
                 asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                    "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
+                    "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63},"
+                    " [%64];"
                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
                       "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
                       "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
                       "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-                      "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                    : "r"(tmem + ((uint32_t)(quad * 32) << 16) + ab * TN + (uint32_t)c0));
+                      "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]),
+                      "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]),
+                      "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]),
+                      "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]),
+                      "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+                    : "r"(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (c0 + 64 >= c_half + TN / 2) {   // last chunk read: the MMAs of the next tile may start
+                    tc_fence_before();
+                    mbar_arrive(acc_empty);
+                }
                 if (row < P.N) {
 #pragma unroll
-                    for (int k = 0; k < 32; k++) {
+                    for (int k = 0; k < 64; k++) {
                         const int tok = t.tok0 + c0 + k;
-                        if (c0 + k < TN && tok < a.T) P.y[(int64_t)tok * P.y_stride + row] = __uint_as_float(v[k]);
+                        if (tok < a.T) P.y[(int64_t)tok * P.y_stride + row] = __uint_as_float(v[k]);
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(acc_empty + 8 * ab);
         }
     }
     tc_fence_before();
