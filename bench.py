@@ -650,6 +650,36 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
     if os.path.exists(pk):
         with open(pk) as f:
             peak_t = json.load(f).get("bf16_tflops")
+    # the layer with RMSNorm*w producers: fused (RMS emits the Q8_0 planes) vs a separate quantize
+    wn = dev(synth.norm_weight(132, DP))
+    ya = torch.empty((TP, DP), dtype=torch.float32, device="cuda")
+    yb = torch.empty_like(ya)
+    scratch = torch.empty((TP * rb * 36,), dtype=torch.uint8, device="cuda")
+
+    def layer_fused(r):
+        qk.qk_rmsnorm_q8_0(xa, TP, DP, DP, "mul", wn, None, 1.0, 1e-6, ya, DP, qa, da, rb)
+        mmq(qa, da, mk(r, (0, 1, 2)))
+        qk.qk_rmsnorm_q8_0(xb, TP, DP, DP, "mul", wn, None, 1.0, 1e-6, yb, DP, qb, db, rb)
+        mmq(qb, db, mk(r, (3, 4)))
+
+    def layer_unfused(r):   # RMS writes y (its Q8_1 image ignored), then the standalone Q8_0 pass re-reads y
+        qk.qk_rmsnorm_q8_1(xa, TP, DP, DP, "mul", wn, None, 1.0, 1e-6, ya, DP, scratch, rb)
+        qk.qk_quantize_q8_0(ya, TP, DP, DP, qa, da, rb)
+        mmq(qa, da, mk(r, (0, 1, 2)))
+        qk.qk_rmsnorm_q8_1(xb, TP, DP, DP, "mul", wn, None, 1.0, 1e-6, yb, DP, scratch, rb)
+        qk.qk_quantize_q8_0(yb, TP, DP, DP, qb, db, rb)
+        mmq(qb, db, mk(r, (3, 4)))
+
+    us_4f = _graph_us(torch, stream, [lambda r=r: layer_fused(r) for r in range(R4)], 2)
+    us_4u = _graph_us(torch, stream, [lambda r=r: layer_unfused(r) for r in range(R4)], 2)
+    us_4r = _graph_us(torch, stream, [lambda: qk.qk_rmsnorm_q8_0(xa, TP, DP, DP, "mul", wn, None, 1.0, 1e-6, ya, DP,
+                                                                 qa, da, rb) for _ in range(R4)], 3)
+    out["c4_rms_producer_layer"] = {
+        "fused_us": round(us_4f, 2), "unfused_us": round(us_4u, 2), "rmsnorm_q8_0_us": round(us_4r, 2),
+        "rmsnorm_q8_0_gbs": gb(TP * DP * 4 * 2 + DP * 4 + TP * DP + TP * rb * 2, us_4r),
+        "kernels_fused": ["rmsnorm_q8_0", "mmq(q,k,v)", "rmsnorm_q8_0", "mmq(gate,up)"],
+        "kernels_unfused": ["rmsnorm_q8_1", "quantize_q8_0", "mmq(q,k,v)", "rmsnorm_q8_1", "quantize_q8_0",
+                            "mmq(gate,up)"]}
     out["c4_prefill_layer"] = {
         "us": round(us_4, 2), "quantize_q8_0_us": round(us_4q, 2), "mmq_qkv_us": round(us_4a, 2),
         "mmq_gate_up_us": round(us_4b, 2), "mmq_tflops": round((ops_qkv + ops_gu) / ((us_4a + us_4b) * 1e-6) / 1e12, 1),

@@ -191,6 +191,22 @@ QK_API qk_status qk_rmsnorm_q8_1(const float *x, int64_t T, int64_t K, int64_t x
                           const int32_t *d_live_rows, qk_stream stream);
 
 /*
+ * qk_rmsnorm_q8_0 -- the same RMS producer emitting the prefill Q8_0 planes
+ * that qk_mmq reads (minfer doc 52, "r51" fused RMSNorm -> Q8_0 producer: the
+ * separate quantize pass and its re-read of y go away).
+ *   y   as qk_rmsnorm_q8_1
+ *   qs  [T][row_blocks*32] int8 codes, 16-byte aligned; d [T][row_blocks] half
+ *       scales: bit-identical to qk_quantize_q8_0 applied to the stored y
+ *       (blocks from K/32 up to row_blocks are zero)
+ * Errors: as qk_rmsnorm_q8_1.
+ */
+QK_API qk_status qk_rmsnorm_q8_0(const float *x, int64_t T, int64_t K, int64_t x_stride,
+                                 qk_norm_kind kind, const float *w, const float *b,
+                                 float scale, float eps, float *y, int64_t y_stride,
+                                 int8_t *qs, uint16_t *d, int64_t row_blocks,
+                                 const int32_t *d_live_rows, qk_stream stream);
+
+/*
  * qk_glu_q8_1 -- GLU producer that emits the image (llama.cpp PR #117,
  * Coverage: F32 ReGLU, GeGLU, SwiGLU with separate, packed and packed-swapped
  * inputs and independent source row strides; output width whole Q8_1 blocks).

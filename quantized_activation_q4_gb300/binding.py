@@ -55,6 +55,7 @@ _SIGS = {
     "qk_quantize_q8_1": ([P, I64, I64, I64, P, I64, P, P], C.c_int),
     "qk_quantize_q8_0": ([P, I64, I64, I64, P, P, I64, P, P], C.c_int),
     "qk_rmsnorm_q8_1": ([P, I64, I64, I64, C.c_int, P, P, F32, F32, P, I64, P, I64, P, P], C.c_int),
+    "qk_rmsnorm_q8_0": ([P, I64, I64, I64, C.c_int, P, P, F32, F32, P, I64, P, P, I64, P, P], C.c_int),
     "qk_glu_q8_1": ([C.c_int, C.c_int, P, I64, P, I64, I64, I64, P, I64, P, I64, P, P], C.c_int),
     "qk_weight_packed_bytes": ([C.c_int, I64, I64], SZ),
     "qk_weight_pack": ([C.c_int, P, I64, I64, P, SZ, P], C.c_int),
@@ -147,6 +148,14 @@ def qk_rmsnorm_q8_1(x, T, K, x_stride, kind, w, b, scale, eps, y, y_stride, img,
     _check("qk_rmsnorm_q8_1", load().qk_rmsnorm_q8_1(_ptr(x), T, K, x_stride, kind, _ptr(w), _ptr(b),
                                                      float(scale), float(eps), _ptr(y), y_stride, _ptr(img),
                                                      img_row_blocks, _ptr(d_live_rows), _stream(stream)))
+
+
+def qk_rmsnorm_q8_0(x, T, K, x_stride, kind, w, b, scale, eps, y, y_stride, qs, d, row_blocks,
+                    d_live_rows=None, stream=None):
+    kind = NORM[kind] if isinstance(kind, str) else int(kind)
+    _check("qk_rmsnorm_q8_0", load().qk_rmsnorm_q8_0(_ptr(x), T, K, x_stride, kind, _ptr(w), _ptr(b),
+                                                     float(scale), float(eps), _ptr(y), y_stride, _ptr(qs), _ptr(d),
+                                                     row_blocks, _ptr(d_live_rows), _stream(stream)))
 
 
 def qk_glu_q8_1(kind, layout, a, a_stride, b, b_stride, T, N, out, out_stride, img, img_row_blocks,

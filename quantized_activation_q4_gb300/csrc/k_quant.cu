@@ -117,11 +117,14 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
 constexpr int RMS_THREADS = 1024;
 constexpr int RMS_ITEMS = 8;
 
-template <int ITEMS>
+// Q81: the image is Q8_1 blocks (img); else Q8_0 split planes (qs codes, dh half scales), the
+// prefill layout that qk_mmq reads.
+template <int ITEMS, bool Q81>
 __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
     const float *__restrict__ x, int K, int64_t x_stride, int kind, const float *__restrict__ w,
     const float *__restrict__ bias, float scale, float eps, float *__restrict__ y, int64_t y_stride,
-    uint8_t *__restrict__ img, int64_t row_blocks, int T, const int32_t *live) {
+    uint8_t *__restrict__ img, int8_t *__restrict__ qs, uint16_t *__restrict__ dh, int64_t row_blocks, int T,
+    const int32_t *live) {
     constexpr bool EARLY = ITEMS <= 2;   // registers for the weight and bias next to the row
     pdl_trigger();
     pdl_wait();
@@ -163,7 +166,9 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
     const float r = red[0];
 
     float *yr = y + t * y_stride;
-    uint8_t *ir = img + t * row_blocks * Q8_1_BYTES;
+    uint8_t *ir = Q81 ? img + t * row_blocks * Q8_1_BYTES : nullptr;
+    int8_t *qr = Q81 ? nullptr : qs + t * row_blocks * QB;
+    uint16_t *dr = Q81 ? nullptr : dh + t * row_blocks;
 #pragma unroll
     for (int it = 0; it < ITEMS; it++) {
         if (4 * RMS_THREADS * it >= K) break;               // uniform: no warp has columns left
@@ -193,13 +198,27 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
         uint32_t codes;
         int sum;
         const float d = q8_block(o, &codes, &sum);   // all lanes of the warp take part
-        if (ok) put_q8_1(ir + (int64_t)(c / QB) * Q8_1_BYTES, j8, d, codes, sum);
+        if (ok) {
+            if (Q81) {
+                put_q8_1(ir + (int64_t)(c / QB) * Q8_1_BYTES, j8, d, codes, sum);
+            } else {
+                reinterpret_cast<uint32_t *>(qr + (int64_t)(c / QB) * QB)[j8] = codes;
+                if (j8 == 0) dr[c / QB] = __half_as_ushort(__float2half_rn(d));
+            }
+        }
     }
     // zero blocks of the row padding
     for (int64_t bb = K / QB + tid; bb < row_blocks; bb += RMS_THREADS) {
-        uint32_t *p = reinterpret_cast<uint32_t *>(ir + bb * Q8_1_BYTES);
+        if (Q81) {
+            uint32_t *p = reinterpret_cast<uint32_t *>(ir + bb * Q8_1_BYTES);
 #pragma unroll
-        for (int i = 0; i < 9; i++) p[i] = 0u;
+            for (int i = 0; i < 9; i++) p[i] = 0u;
+        } else {
+            uint32_t *p = reinterpret_cast<uint32_t *>(qr + bb * QB);
+#pragma unroll
+            for (int i = 0; i < 8; i++) p[i] = 0u;
+            dr[bb] = 0;
+        }
     }
 }
 
@@ -281,18 +300,33 @@ qk_status launch_quantize_q8_0(const float *x, int T, int K, int64_t x_stride, i
                       (uint8_t *)nullptr, qs, d, row_blocks, T, live);
 }
 
+template <bool Q81>
+static qk_status launch_rmsnorm(const float *x, int T, int K, int64_t x_stride, int kind, const float *w,
+                                const float *b, float scale, float eps, float *y, int64_t y_stride, uint8_t *img,
+                                int8_t *qs, uint16_t *dh, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
+    if (T == 0) return QK_OK;
+    const int per = 4 * RMS_THREADS;   // columns per item
+    auto kernel = K <= per ? rmsnorm_q8_1_kernel<1, Q81>
+                  : K <= 2 * per ? rmsnorm_q8_1_kernel<2, Q81>
+                  : K <= 4 * per ? rmsnorm_q8_1_kernel<4, Q81>
+                                 : rmsnorm_q8_1_kernel<RMS_ITEMS, Q81>;
+    return launch_pdl(Q81 ? "rmsnorm_q8_1" : "rmsnorm_q8_0", kernel, dim3((unsigned)T), dim3(RMS_THREADS), 0, s, x,
+                      K, x_stride, kind, w, b, scale, eps, y, y_stride, img, qs, dh, row_blocks, T, live);
+}
+
 qk_status launch_rmsnorm_q8_1(const float *x, int T, int K, int64_t x_stride, int kind,
                               const float *w, const float *b, float scale, float eps, float *y,
                               int64_t y_stride, uint8_t *img, int64_t row_blocks,
                               const int32_t *live, cudaStream_t s) {
-    if (T == 0) return QK_OK;
-    const int per = 4 * RMS_THREADS;   // columns per item
-    auto kernel = K <= per ? rmsnorm_q8_1_kernel<1>
-                  : K <= 2 * per ? rmsnorm_q8_1_kernel<2>
-                  : K <= 4 * per ? rmsnorm_q8_1_kernel<4>
-                                 : rmsnorm_q8_1_kernel<RMS_ITEMS>;
-    return launch_pdl("rmsnorm_q8_1", kernel, dim3((unsigned)T), dim3(RMS_THREADS), 0, s, x, K, x_stride, kind, w, b,
-                      scale, eps, y, y_stride, img, row_blocks, T, live);
+    return launch_rmsnorm<true>(x, T, K, x_stride, kind, w, b, scale, eps, y, y_stride, img, nullptr, nullptr,
+                                row_blocks, live, s);
+}
+
+qk_status launch_rmsnorm_q8_0(const float *x, int T, int K, int64_t x_stride, int kind, const float *w,
+                              const float *b, float scale, float eps, float *y, int64_t y_stride, int8_t *qs,
+                              uint16_t *dh, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
+    return launch_rmsnorm<false>(x, T, K, x_stride, kind, w, b, scale, eps, y, y_stride, nullptr, qs, dh,
+                                 row_blocks, live, s);
 }
 
 qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride, const float *b,

@@ -132,6 +132,37 @@ qk_status qk_rmsnorm_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride
                                static_cast<uint8_t *>(img), img_row_blocks, d_live_rows, (cudaStream_t)stream);
 }
 
+qk_status qk_rmsnorm_q8_0(const float *x, int64_t T, int64_t K, int64_t x_stride, qk_norm_kind kind,
+                          const float *w, const float *b, float scale, float eps, float *y, int64_t y_stride,
+                          int8_t *qs, uint16_t *d, int64_t row_blocks, const int32_t *d_live_rows,
+                          qk_stream stream) {
+    qk_status st = check_quant_in(x, T, K, x_stride);
+    if (st != QK_OK) return st;
+    REQUIRE(kind >= QK_NORM_PLAIN && kind <= QK_NORM_SCALE, QK_ERR_ARG, "bad norm kind %d", (int)kind);
+    REQUIRE(K % QB == 0, QK_ERR_SHAPE, "K=%lld is not a whole number of 32-blocks", (long long)K);
+    REQUIRE(K <= 32768, QK_ERR_UNSUPPORTED, "K=%lld > 32768 (a row is kept in registers)", (long long)K);
+    REQUIRE((y && qs && d) || T == 0, QK_ERR_ARG, "y, qs or d is null");
+    const bool need_w = kind == QK_NORM_MUL || kind == QK_NORM_MUL_ADD;
+    REQUIRE(!need_w || w, QK_ERR_ARG, "w is null for a MUL kind");
+    REQUIRE(kind != QK_NORM_MUL_ADD || b, QK_ERR_ARG, "b is null for MUL_ADD");
+    REQUIRE(y_stride >= K, QK_ERR_SHAPE, "y_stride < K");
+    REQUIRE(row_blocks >= K / QB, QK_ERR_SHAPE, "row_blocks < K/32");
+    REQUIRE(aligned(y, 4) && aligned(qs, 16) && aligned(d, 4) && aligned(w, 4) && aligned(b, 4), QK_ERR_ARG,
+            "misaligned pointer (qs must be 16-byte aligned)");
+    Span sx = span(x, rows_span(T, x_stride * 4, K * 4));
+    Span sy = span(y, rows_span(T, y_stride * 4, K * 4));
+    Span sq = span(qs, (size_t)(T * row_blocks * QB)), sd = span(d, (size_t)(T * row_blocks * 2));
+    Span sw = span(need_w ? w : nullptr, need_w ? (size_t)K * 4 : 0);
+    Span sb = span(kind == QK_NORM_MUL_ADD ? b : nullptr, kind == QK_NORM_MUL_ADD ? (size_t)K * 4 : 0);
+    const Span outs[3] = {sy, sq, sd}, ins[3] = {sx, sw, sb};
+    for (int o = 0; o < 3; o++) {
+        for (int i = 0; i < 3; i++) REQUIRE(!overlap(outs[o], ins[i]), QK_ERR_ALIAS, "an output overlaps an input");
+        for (int q = 0; q < o; q++) REQUIRE(!overlap(outs[o], outs[q]), QK_ERR_ALIAS, "outputs overlap each other");
+    }
+    return launch_rmsnorm_q8_0(x, (int)T, (int)K, x_stride, (int)kind, w, b, scale, eps, y, y_stride, qs, d,
+                               row_blocks, d_live_rows, (cudaStream_t)stream);
+}
+
 qk_status qk_glu_q8_1(qk_glu_kind kind, qk_glu_layout layout, const float *a, int64_t a_stride,
                       const float *b, int64_t b_stride, int64_t T, int64_t N, float *out,
                       int64_t out_stride, void *img, int64_t img_row_blocks, const int32_t *d_live_rows,

@@ -128,6 +128,9 @@ qk_status launch_rmsnorm_q8_1(const float *x, int T, int K, int64_t x_stride, in
                               const float *w, const float *b, float scale, float eps, float *y,
                               int64_t y_stride, uint8_t *img, int64_t row_blocks,
                               const int32_t *live, cudaStream_t s);
+qk_status launch_rmsnorm_q8_0(const float *x, int T, int K, int64_t x_stride, int kind, const float *w,
+                              const float *b, float scale, float eps, float *y, int64_t y_stride, int8_t *qs,
+                              uint16_t *dh, int64_t row_blocks, const int32_t *live, cudaStream_t s);
 qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride, const float *b,
                           int64_t b_stride, int T, int N, float *out, int64_t out_stride,
                           uint8_t *img, int64_t row_blocks, const int32_t *live, cudaStream_t s);

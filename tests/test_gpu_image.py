@@ -162,3 +162,34 @@ def test_glu_live_rows():
     og, ig = host(out), host(img).reshape(T, -1)
     assert np.all(np.isnan(og[live:])) and np.all(ig[live:] == 0xA5)
     assert np.array_equal(ig[:live], O.quantize_q8_1(og[:live]))
+
+
+@pytest.mark.parametrize("kind", ["mul", "plain", "mul_add", "scale"])
+@pytest.mark.parametrize("T,K,live", [(5, 3584, None), (3325, 3584, None), (9, 256, 6), (2, 12288, None)])
+def test_rmsnorm_q8_0_planes(kind, T, K, live):
+    """The fused RMS -> Q8_0 producer (prefill): the planes are bit-exact to the oracle's Q8_0
+    quantiser applied to the GPU's own stored y, and y matches the oracle RMS within tolerance."""
+    import torch
+    if T > 64 and kind != "mul":
+        pytest.skip("the full prefill size runs once, with the config's MUL kind")
+    x = synth.activations(2100 + K + T, T, K)
+    if live is not None:
+        x = synth.poison_rows(x, live)
+    w = synth.norm_weight(2101, K)
+    b = synth.activations(2102, 1, K)[0] * np.float32(0.1)
+    rb = K // 32 + 2                                     # with row padding
+    y = torch.full((T, K), float("nan"), dtype=torch.float32, device="cuda")
+    qs = torch.full((T * rb * 32,), 0x5A, dtype=torch.int8, device="cuda")
+    d = torch.full((T * rb,), 0x5A5A, dtype=torch.int16, device="cuda")
+    qk.qk_rmsnorm_q8_0(dev(x), T, K, K, kind, dev(w), dev(b), 0.5, 1e-6, y, K, qs, d, rb,
+                       live_ptr(live) if live is not None else None)
+    n = T if live is None else live
+    yg = host(y)
+    qg = host(qs).reshape(T, rb * 32)
+    dg = host(d).view(np.uint16).reshape(T, rb)
+    rows = np.arange(n) if n <= 64 else np.random.default_rng(5).choice(n, 64, replace=False)
+    yref = O.rmsnorm(x[rows], kind, w=w, b=b, scale=0.5, eps=1e-6)
+    assert np.all(np.abs(yg[rows] - yref) <= _y_tolerance(yref, b if kind == 'mul_add' else None))
+    q_o, d_o = O.quantize_q8_0(yg[:n], row_blocks=rb)
+    assert np.array_equal(qg[:n], q_o) and np.array_equal(dg[:n], d_o)
+    assert np.all(np.isnan(yg[n:])) and np.all(qg[n:] == 0x5A) and np.all(dg[n:] == 0x5A5A)
