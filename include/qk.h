@@ -149,8 +149,9 @@ QK_API qk_status qk_selftest_wait_timeout(qk_stream stream);
  * emission replaces; kept for unfused use and as the fused kernels' control).
  *   x        [T][x_stride] F32, columns 0..K-1 read
  *   img      [T][img_row_blocks] Q8_1 blocks, img_row_blocks >= ceil(K/32)
- * Errors: QK_ERR_ARG (null, T < 0, K < 1), QK_ERR_SHAPE (x_stride < K,
- * img_row_blocks < ceil(K/32)), QK_ERR_ALIAS (img overlaps x).
+ * Errors: QK_ERR_ARG (null, T < 0, K < 1 or K > 2^25, img_row_blocks > 2^20),
+ * QK_ERR_SHAPE (x_stride < K, img_row_blocks < ceil(K/32)), QK_ERR_ALIAS (img
+ * overlaps x).
  */
 QK_API qk_status qk_quantize_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride,
                            void *img, int64_t img_row_blocks,
@@ -214,7 +215,7 @@ QK_API qk_status qk_rmsnorm_q8_0(const float *x, int64_t T, int64_t K, int64_t x
  *   img the Q8_1 image of exactly the stored out values
  *   SEPARATE: g = a + t*a_stride, u = b + t*b_stride
  *   PACKED: g = a + t*a_stride, u = g + N;  PACKED_SWAPPED: u = a + t*a_stride, g = u + N
- * Errors: QK_ERR_ARG, QK_ERR_SHAPE (N % 32 != 0, strides too small),
+ * Errors: QK_ERR_ARG (N > 2^25), QK_ERR_SHAPE (N % 32 != 0, strides too small),
  * QK_ERR_ALIAS (out or img overlapping the inputs or each other).
  */
 QK_API qk_status qk_glu_q8_1(qk_glu_kind kind, qk_glu_layout layout,
@@ -383,6 +384,31 @@ QK_API qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t row
                      int32_t n_proj, const qk_proj_id *projs,
                      const int32_t *counts, const int32_t *offsets, const int32_t *items,
                      qk_stream stream);
+
+/*
+ * qk_mmvq_id_slots -- qk_mmvq_id with one image row per pair: y[p][:] =
+ * W_e * image row p (the per-slot down projection of a routed FFN, whose
+ * input is each pair's own GLU output; TensorFold PR #1047 "Ordinary, K8192
+ * / 32 slots" and "K2560 / 128 slots" components). img has rows * k rows.
+ * Errors: as qk_mmvq_id.
+ */
+QK_API qk_status qk_mmvq_id_slots(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k,
+                                  int32_t n_proj, const qk_proj_id *projs, const int32_t *counts,
+                                  const int32_t *offsets, const int32_t *items, qk_stream stream);
+
+/*
+ * qk_moe_combine -- weighted combine of the routed experts' outputs (the
+ * closing step of the routed FFN; TensorFold PR #1047: live-row aware).
+ *   y[r][n] = sum over s = 0..k-1 (in that order, one binary32 fma each) of
+ *             wts[r*k + s] * expert_out[r*k + s][n],   for rows r < live
+ *   expert_out [rows*k][out_stride] F32, wts [rows][k] F32 (qk_topk_route's),
+ *   y [rows][y_stride] F32; rows >= *d_live_rows are not read or written.
+ *   expert_out and y 16-byte aligned; strides and N multiples of 4; N <= 2^25.
+ * Errors: QK_ERR_ARG, QK_ERR_SHAPE, QK_ERR_ALIAS.
+ */
+QK_API qk_status qk_moe_combine(const float *expert_out, int64_t out_stride, const float *wts, int64_t rows,
+                                int32_t k, int64_t N, float *y, int64_t y_stride, const int32_t *d_live_rows,
+                                qk_stream stream);
 
 /* ---------------------------------------------------------- prefill */
 

@@ -239,6 +239,31 @@ def proj_id_q8_1(wtype: str, W: np.ndarray, E: int, N: int, K: int, img: np.ndar
     return y
 
 
+def proj_id_slots_q8_1(wtype: str, W: np.ndarray, E: int, N: int, K: int, img: np.ndarray, row_blocks: int,
+                       ids: np.ndarray, items: np.ndarray) -> np.ndarray:
+    """Per-slot routed projection (the down projection of a routed FFN; TensorFold
+    PR #1047 "Ordinary, K8192 / 32 slots" and "K2560 / 128 slots" components):
+    pair p = row*k + slot reads image row p, its own GLU output, instead of the
+    token's row. This is the routed projection of the flattened pairs, one slot
+    per row, so it reuses proj_id_q8_1 with ids viewed as [rows*k][1]."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    return proj_id_q8_1(wtype, W, E, N, K, img, row_blocks, ids.reshape(-1, 1), items)
+
+
+def moe_combine(expert_out: np.ndarray, wts: np.ndarray, live: int | None = None) -> np.ndarray:
+    """Weighted combine closing the routed FFN (tf_moe_combine; TensorFold PR #1047,
+    "What this changes": padding rows get no combine), in float64:
+    y[r] = sum over slots s of wts[r, s] * expert_out[r*k + s], for the first
+    `live` rows; the remaining rows are NaN (the caller's buffer is not written)."""
+    wts = np.asarray(wts, dtype=np.float64)
+    rows, k = wts.shape
+    eo = np.asarray(expert_out, dtype=np.float64).reshape(rows, k, -1)
+    live = rows if live is None else live
+    y = np.full((rows, eo.shape[2]), np.nan, dtype=np.float64)
+    y[:live] = np.einsum("rs,rsn->rn", wts[:live], eo[:live])
+    return y
+
+
 # ---------------------------------------------------------------- metrics
 def nmse(a, ref) -> float:
     """Normalised mean squared error sum((a-ref)^2) / sum(ref^2)."""

@@ -68,6 +68,8 @@ _SIGS = {
     "qk_moe_plan": ([P, I64, I32, I32, P, P, P, P, P], C.c_int),
     "qk_route_plan": ([P, I64, I32, I32, P, P, P, P, P, P, P], C.c_int),
     "qk_mmvq_id": ([P, I64, I64, I32, I32, C.POINTER(qk_proj_id), P, P, P, P], C.c_int),
+    "qk_mmvq_id_slots": ([P, I64, I64, I32, I32, C.POINTER(qk_proj_id), P, P, P, P], C.c_int),
+    "qk_moe_combine": ([P, I64, P, I64, I32, I64, P, I64, P, P], C.c_int),
     "qk_mmq_workspace_bytes": ([I64, I32, C.POINTER(qk_proj)], C.c_size_t),
     "qk_mmq": ([P, P, I64, I64, I32, C.POINTER(qk_proj), P, C.c_size_t, P], C.c_int),
 }
@@ -222,6 +224,17 @@ def qk_mmvq_id(img, img_row_blocks, rows, k, projs, counts, offsets, items, stre
     arr = (qk_proj_id * len(projs))(*projs)
     _check("qk_mmvq_id", load().qk_mmvq_id(_ptr(img), img_row_blocks, rows, k, len(projs), arr, _ptr(counts),
                                            _ptr(offsets), _ptr(items), _stream(stream)))
+
+
+def qk_mmvq_id_slots(img, img_row_blocks, rows, k, projs, counts, offsets, items, stream=None):
+    arr = (qk_proj_id * len(projs))(*projs)
+    _check("qk_mmvq_id_slots", load().qk_mmvq_id_slots(_ptr(img), img_row_blocks, rows, k, len(projs), arr,
+                                                       _ptr(counts), _ptr(offsets), _ptr(items), _stream(stream)))
+
+
+def qk_moe_combine(expert_out, out_stride, wts, rows, k, N, y, y_stride, d_live_rows=None, stream=None):
+    _check("qk_moe_combine", load().qk_moe_combine(_ptr(expert_out), out_stride, _ptr(wts), rows, k, N, _ptr(y),
+                                                   y_stride, _ptr(d_live_rows), _stream(stream)))
 
 
 def qk_mmq_workspace_bytes(T, projs) -> int:

@@ -846,6 +846,7 @@ struct IdArgs {
     const uint8_t *img;
     int64_t img_row_bytes;
     int rows, k, n_proj, E, tiles_per_expert;
+    int per_pair;   // the image has a row per pair (row p) rather than per token (row p / k)
     const int32_t *counts, *offsets, *items;
     IdProj p[MAX_PROJ];
 };
@@ -1008,7 +1009,7 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
                 const int idx = pass * 8 + threadIdx.x;
                 int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
                 if (p < 0 || p / a.k >= a.rows) p = -1;   // not a pair of this bucket: skip
-                tok_img[threadIdx.x] = p >= 0 ? p / a.k : -1;
+                tok_img[threadIdx.x] = p >= 0 ? (a.per_pair ? p : p / a.k) : -1;
                 tok_out[threadIdx.x] = p;
             }
             id_consumers_sync();
@@ -1244,9 +1245,10 @@ qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj,
 
 qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k, int n_proj,
                          const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
-                         const int32_t *items, cudaStream_t s) {
+                         const int32_t *items, bool per_pair, cudaStream_t s) {
     IdArgs a = {};
     a.img = img;
+    a.per_pair = per_pair ? 1 : 0;
     a.img_row_bytes = row_blocks * Q8_1_BYTES;
     a.rows = rows;
     a.k = k;

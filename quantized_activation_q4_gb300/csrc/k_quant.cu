@@ -78,8 +78,8 @@ __device__ __forceinline__ void put_q8_1(uint8_t *blk, int j8, float d, uint32_t
 }
 
 // ---------------------------------------------------------------- quantizers
-// grid (ceil(row_blocks/32), T), 256 threads: warp w, lane group m handles
-// block 32*blockIdx.x + 4*w + m of row blockIdx.y.
+// grid (T, ceil(row_blocks/32)), 256 threads: warp w, lane group m handles
+// block 32*blockIdx.y + 4*w + m of row blockIdx.x (rows on x: up to 2^31-1).
 template <bool Q81>
 __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__ x, int K,
                                                        int64_t x_stride, uint8_t *__restrict__ out,
@@ -87,9 +87,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
                                                        int64_t row_blocks, int T, const int32_t *live) {
     pdl_trigger();
     pdl_wait();
-    const int t = blockIdx.y;
+    const int t = blockIdx.x;
     const int lane = threadIdx.x & 31, j8 = lane & 7;
-    const int64_t b = (int64_t)blockIdx.x * 32 + (threadIdx.x >> 5) * 4 + (lane >> 3);
+    const int64_t b = (int64_t)blockIdx.y * 32 + (threadIdx.x >> 5) * 4 + (lane >> 3);
     const bool in_row = b < row_blocks;          // whole 8-lane group agrees
     const int64_t col = b * QB + 4 * j8;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -239,9 +239,9 @@ __global__ void __launch_bounds__(256) glu_q8_1_kernel(
     int64_t row_blocks, int T, const int32_t *live) {
     pdl_trigger();
     pdl_wait();
-    const int t = blockIdx.y;
+    const int t = blockIdx.x;
     const int tid = threadIdx.x, j8 = tid & 7;
-    const int c = blockIdx.x * 1024 + 4 * tid;
+    const int c = blockIdx.y * 1024 + 4 * tid;
     const float *g, *u;
     if (layout == QK_GLU_SEPARATE) {
         g = a + t * a_stride;
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(256) glu_q8_1_kernel(
     const float d = q8_block(v, &codes, &sum);
     uint8_t *ir = img + t * row_blocks * Q8_1_BYTES;
     if (ok) put_q8_1(ir + (int64_t)(c / QB) * Q8_1_BYTES, j8, d, codes, sum);
-    if (blockIdx.x == 0) {  // zero blocks of the row padding
+    if (blockIdx.y == 0) {  // zero blocks of the row padding
         for (int64_t bb = N / QB + tid; bb < row_blocks; bb += 256) {
             uint32_t *p = reinterpret_cast<uint32_t *>(ir + bb * Q8_1_BYTES);
 #pragma unroll
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(256) glu_q8_1_kernel(
 qk_status launch_quantize_q8_1(const float *x, int T, int K, int64_t x_stride, uint8_t *img,
                                int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
-    dim3 grid((unsigned)ceil_div(row_blocks, 32), (unsigned)T);
+    dim3 grid((unsigned)T, (unsigned)ceil_div(row_blocks, 32));
     return launch_pdl("quantize_q8_1", quantize_kernel<true>, grid, dim3(256), 0, s, x, K, x_stride, img,
                       (int8_t *)nullptr, (uint16_t *)nullptr, row_blocks, T, live);
 }
@@ -295,7 +295,7 @@ qk_status launch_quantize_q8_1(const float *x, int T, int K, int64_t x_stride, u
 qk_status launch_quantize_q8_0(const float *x, int T, int K, int64_t x_stride, int8_t *qs,
                                uint16_t *d, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
-    dim3 grid((unsigned)ceil_div(row_blocks, 32), (unsigned)T);
+    dim3 grid((unsigned)T, (unsigned)ceil_div(row_blocks, 32));
     return launch_pdl("quantize_q8_0", quantize_kernel<false>, grid, dim3(256), 0, s, x, K, x_stride,
                       (uint8_t *)nullptr, qs, d, row_blocks, T, live);
 }
@@ -333,7 +333,7 @@ qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride
                           int64_t b_stride, int T, int N, float *out, int64_t out_stride,
                           uint8_t *img, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
-    dim3 grid((unsigned)ceil_div(N, 1024), (unsigned)T);
+    dim3 grid((unsigned)T, (unsigned)ceil_div(N, 1024));
     return launch_pdl("glu_q8_1", glu_q8_1_kernel, grid, dim3(256), 0, s, kind, layout, a, a_stride, b, b_stride,
                       N, out, out_stride, img, row_blocks, T, live);
 }

@@ -218,6 +218,31 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(const float *__restric
     plan_body(ids, n_live * k, E, counts, offsets, items, sm, wsum);
 }
 
+
+// ---------------------------------------------------------------- combine
+// y[r][n] = sum over slots s (ascending) of wts[r][s] * expert_out[r*k + s][n], one binary32 fma
+// per slot, for live rows r. Grid (ceil(N/1024), rows); thread i handles columns 4i..4i+3.
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ eo, int64_t eo_stride,
+                                                      const float *__restrict__ wts, int rows, int k, int N,
+                                                      float *__restrict__ y, int64_t y_stride, const int32_t *live) {
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x;
+    if (r >= live_rows(live, rows)) return;
+    const int c = (blockIdx.y * 256 + threadIdx.x) * 4;
+    if (c >= N) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < k; s++) {
+        const float w = wts[(int64_t)r * k + s];
+        const float4 e = *reinterpret_cast<const float4 *>(eo + ((int64_t)r * k + s) * eo_stride + c);
+        acc.x = fmaf(w, e.x, acc.x);
+        acc.y = fmaf(w, e.y, acc.y);
+        acc.z = fmaf(w, e.z, acc.z);
+        acc.w = fmaf(w, e.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(y + (int64_t)r * y_stride + c) = acc;
+}
+
 }  // namespace
 
 qk_status launch_topk_route(const float *logits, int rows, int E, int k, int32_t *ids, float *wts,
@@ -255,4 +280,10 @@ qk_status launch_moe_plan(const int32_t *ids, int rows, int k, int E, int32_t *c
                       items, live);
 }
 
+qk_status launch_moe_combine(const float *expert_out, int64_t out_stride, const float *wts, int rows, int k, int N,
+                             float *y, int64_t y_stride, const int32_t *live, cudaStream_t s) {
+    dim3 grid((unsigned)rows, (unsigned)ceil_div(N, 1024));   // rows on x: up to 2^31-1 blocks
+    return launch_pdl("moe_combine", combine_kernel, grid, dim3(256), 0, s, expert_out, out_stride, wts, rows, k, N,
+                      y, y_stride, live);
+}
 }  // namespace qk

@@ -67,7 +67,7 @@ uint64_t qk_launch_count(void) { return g_launches.load(std::memory_order_relaxe
 // ------------------------------------------------------------------ image
 static qk_status check_quant_in(const float *x, int64_t T, int64_t K, int64_t x_stride) {
     REQUIRE(T >= 0 && T <= INT32_MAX, QK_ERR_ARG, "T=%lld out of range", (long long)T);
-    REQUIRE(K >= 1 && K <= (1LL << 30), QK_ERR_ARG, "K=%lld out of range", (long long)K);
+    REQUIRE(K >= 1 && K <= (1LL << 25), QK_ERR_ARG, "K=%lld out of range", (long long)K);
     REQUIRE(x || T == 0, QK_ERR_ARG, "x is null");
     REQUIRE(x_stride >= K, QK_ERR_SHAPE, "x_stride=%lld < K=%lld", (long long)x_stride, (long long)K);
     REQUIRE(aligned(x, 4), QK_ERR_ARG, "x not 4-byte aligned");
@@ -82,6 +82,7 @@ qk_status qk_quantize_q8_1(const float *x, int64_t T, int64_t K, int64_t x_strid
     REQUIRE(aligned(img, 4), QK_ERR_ARG, "img not 4-byte aligned");
     REQUIRE(img_row_blocks >= ceil_div(K, QB), QK_ERR_SHAPE, "img_row_blocks=%lld < ceil(K/32)=%lld",
             (long long)img_row_blocks, (long long)ceil_div(K, QB));
+    REQUIRE(img_row_blocks <= (1 << 20), QK_ERR_ARG, "img_row_blocks > 2^20");
     Span sx = span(x, rows_span(T, x_stride * 4, K * 4));
     Span si = span(img, (size_t)(T * img_row_blocks * Q8_1_BYTES));
     REQUIRE(!overlap(sx, si), QK_ERR_ALIAS, "img overlaps x");
@@ -96,6 +97,7 @@ qk_status qk_quantize_q8_0(const float *x, int64_t T, int64_t K, int64_t x_strid
     REQUIRE((qs && d) || T == 0, QK_ERR_ARG, "qs or d is null");
     REQUIRE(aligned(qs, 4) && aligned(d, 2), QK_ERR_ARG, "qs must be 4-byte and d 2-byte aligned");
     REQUIRE(row_blocks >= ceil_div(K, QB), QK_ERR_SHAPE, "row_blocks=%lld < ceil(K/32)", (long long)row_blocks);
+    REQUIRE(row_blocks <= (1 << 20), QK_ERR_ARG, "row_blocks > 2^20");
     Span sx = span(x, rows_span(T, x_stride * 4, K * 4));
     Span sq = span(qs, (size_t)(T * row_blocks * QB));
     Span sd = span(d, (size_t)(T * row_blocks * 2));
@@ -169,7 +171,7 @@ qk_status qk_glu_q8_1(qk_glu_kind kind, qk_glu_layout layout, const float *a, in
                       qk_stream stream) {
     REQUIRE(kind >= QK_GLU_SWIGLU && kind <= QK_GLU_REGLU, QK_ERR_ARG, "bad glu kind %d", (int)kind);
     REQUIRE(layout >= QK_GLU_SEPARATE && layout <= QK_GLU_PACKED_SWAPPED, QK_ERR_ARG, "bad glu layout %d", (int)layout);
-    REQUIRE(T >= 0 && T <= INT32_MAX && N >= 1 && N <= (1LL << 30), QK_ERR_ARG, "T or N out of range");
+    REQUIRE(T >= 0 && T <= INT32_MAX && N >= 1 && N <= (1LL << 25), QK_ERR_ARG, "T or N out of range");
     REQUIRE(N % QB == 0, QK_ERR_SHAPE, "N=%lld is not a whole number of 32-blocks", (long long)N);
     REQUIRE((a && out && img && (layout != QK_GLU_SEPARATE || b)) || T == 0, QK_ERR_ARG, "null pointer");
     const int64_t a_row = layout == QK_GLU_SEPARATE ? N : 2 * N;
@@ -299,15 +301,15 @@ qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_
     return QK_OK;
 }
 
-qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k, int32_t n_proj,
-                     const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
-                     const int32_t *items, qk_stream stream) {
+static qk_status mmvq_id_common(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k, int32_t n_proj,
+                                const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
+                                const int32_t *items, bool per_pair, qk_stream stream) {
     REQUIRE(img && projs && counts && offsets && items, QK_ERR_ARG, "null pointer");
     REQUIRE(aligned(img, 4), QK_ERR_ARG, "img not 4-byte aligned");
     REQUIRE(rows >= 1 && rows <= (1 << 24) && k >= 1 && k <= 64 && img_row_blocks >= 1, QK_ERR_ARG,
             "rows, k or img_row_blocks out of range");
     REQUIRE(n_proj >= 1 && n_proj <= 8, QK_ERR_UNSUPPORTED, "n_proj=%d not in 1..8", (int)n_proj);
-    Span si = span(img, (size_t)(rows * img_row_blocks * Q8_1_BYTES));
+    Span si = span(img, (size_t)((per_pair ? rows * k : rows) * img_row_blocks * Q8_1_BYTES));
     for (int j = 0; j < n_proj; j++) {
         const qk_proj_id &p = projs[j];
         qk_status st = check_proj_common(p.wtype, p.w, p.N, p.K, img_row_blocks);
@@ -329,10 +331,39 @@ qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t rows, int3
             if (projs[j].wtype == wt) group[n++] = projs[j];
         if (n == 0) continue;
         qk_status st = launch_mmvq_id(static_cast<const uint8_t *>(img), img_row_blocks, (int)rows, k, n, group,
-                                      counts, offsets, items, (cudaStream_t)stream);
+                                      counts, offsets, items, per_pair, (cudaStream_t)stream);
         if (st != QK_OK) return st;
     }
     return QK_OK;
+}
+
+qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k, int32_t n_proj,
+                     const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
+                     const int32_t *items, qk_stream stream) {
+    return mmvq_id_common(img, img_row_blocks, rows, k, n_proj, projs, counts, offsets, items, false, stream);
+}
+
+qk_status qk_mmvq_id_slots(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k, int32_t n_proj,
+                           const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
+                           const int32_t *items, qk_stream stream) {
+    return mmvq_id_common(img, img_row_blocks, rows, k, n_proj, projs, counts, offsets, items, true, stream);
+}
+
+qk_status qk_moe_combine(const float *expert_out, int64_t out_stride, const float *wts, int64_t rows, int32_t k,
+                         int64_t N, float *y, int64_t y_stride, const int32_t *d_live_rows, qk_stream stream) {
+    REQUIRE(expert_out && wts && y, QK_ERR_ARG, "null pointer");
+    REQUIRE(rows >= 0 && rows <= (1 << 24) && k >= 1 && k <= 64 && N >= 1 && N <= (1LL << 25), QK_ERR_ARG,
+            "rows, k or N out of range");
+    REQUIRE(out_stride >= N && y_stride >= N, QK_ERR_SHAPE, "out_stride or y_stride < N");
+    REQUIRE(aligned(expert_out, 16) && aligned(y, 16) && out_stride % 4 == 0 && y_stride % 4 == 0 && N % 4 == 0,
+            QK_ERR_ARG, "expert_out and y must be 16-byte aligned with strides and N multiples of 4");
+    Span se = span(expert_out, rows_span(rows * k, out_stride * 4, N * 4));
+    Span sw = span(wts, (size_t)(rows * k * 4));
+    Span sy = span(y, rows_span(rows, y_stride * 4, N * 4));
+    REQUIRE(!overlap(sy, se) && !overlap(sy, sw), QK_ERR_ALIAS, "y overlaps expert_out or wts");
+    if (rows == 0) return QK_OK;
+    return launch_moe_combine(expert_out, out_stride, wts, (int)rows, k, (int)N, y, y_stride, d_live_rows,
+                              (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------------ routing

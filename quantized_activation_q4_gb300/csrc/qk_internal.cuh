@@ -142,7 +142,9 @@ qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj,
                       cudaStream_t s);
 qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k, int n_proj,
                          const qk_proj_id *projs, const int32_t *counts, const int32_t *offsets,
-                         const int32_t *items, cudaStream_t s);
+                         const int32_t *items, bool per_pair, cudaStream_t s);
+qk_status launch_moe_combine(const float *expert_out, int64_t out_stride, const float *wts, int rows, int k, int N,
+                             float *y, int64_t y_stride, const int32_t *live, cudaStream_t s);
 qk_status launch_topk_route(const float *logits, int rows, int E, int k, int32_t *ids,
                             float *wts, const int32_t *live, cudaStream_t s);
 qk_status launch_moe_plan(const int32_t *ids, int rows, int k, int E, int32_t *counts,

@@ -353,3 +353,49 @@ def test_routed_projection_rows():
             assert np.array_equal(y[p], O.proj_q8_1("q4_0", We, N, K, img[p // k:p // k + 1], K // 32)[0])
         else:
             assert np.all(np.isnan(y[p]))
+
+
+def test_per_slot_projection_reads_each_pairs_own_row():
+    """Per-slot pairs: pair p's output is its expert's projection of image row p
+    (not row p // k); checked against the single-matrix projection of that row."""
+    E, N, K, rows, k, live = 5, 8, 64, 3, 4, 2
+    W = np.concatenate([synth.q4_0_weight(130 + e, N, K) for e in range(E)], axis=0)
+    xs = synth.activations(131, rows * k, K)
+    img = O.quantize_q8_1(xs)
+    ids = synth.rng(132).integers(0, E, size=(rows, k), dtype=np.int32)
+    _, _, items = O.moe_plan(ids, E, live=live)
+    y = O.proj_id_slots_q8_1("q4_0", W, E, N, K, img, K // 32, ids, items)
+    for p in range(rows * k):
+        if p < live * k:
+            e = ids.ravel()[p]
+            ref = O.proj_q8_1("q4_0", W[e * N:(e + 1) * N], N, K, img[p:p + 1], K // 32)[0]
+            assert np.array_equal(y[p], ref)
+        else:
+            assert np.all(np.isnan(y[p]))
+
+
+def test_combine_one_hot_selects_the_slot():
+    """One-hot weights pick exactly one slot's output (catches a slot/row index mix-up),
+    zero weights give zero, and weights summing to one over equal outputs give that output."""
+    rows, k, N = 5, 3, 7
+    eo = synth.rng(140).standard_normal((rows * k, N))
+    pick = np.array([2, 0, 1, 1, 2])
+    w = np.zeros((rows, k))
+    w[np.arange(rows), pick] = 1.0
+    y = O.moe_combine(eo, w)
+    for r in range(rows):
+        assert np.array_equal(y[r], eo[r * k + pick[r]])
+    assert np.array_equal(O.moe_combine(eo, np.zeros((rows, k))), np.zeros((rows, N)))
+    same = np.repeat(eo[:rows], k, axis=0)          # every slot of row r holds eo[r]
+    wn = synth.rng(141).random((rows, k))
+    wn /= wn.sum(axis=1, keepdims=True)
+    assert np.allclose(O.moe_combine(same, wn), eo[:rows], rtol=1e-14, atol=1e-14)
+
+
+def test_combine_skips_rows_past_live():
+    rows, k, N, live = 6, 2, 4, 3
+    eo = synth.rng(142).standard_normal((rows * k, N))
+    w = synth.rng(143).random((rows, k))
+    y = O.moe_combine(eo, w, live=live)
+    assert np.all(np.isnan(y[live:])) and np.all(np.isfinite(y[:live]))
+    assert np.array_equal(y[:live], O.moe_combine(eo[:live * k], w[:live]))
