@@ -562,6 +562,14 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
                                   NE, DR, buf[e * per:(e + 1) * per], per)
             pair.append(buf)
         experts.append(pair)
+    per_d = qk.qk_weight_packed_bytes("q4_0", DR, NE)     # down: 768 -> 2560 per expert
+    downs = []
+    for r in range(R3):
+        buf = torch.empty((E * per_d,), dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            qk.qk_weight_pack("q4_0", dev(synth.q4_0_weight(9000 + 1000 * r + e, DR, NE).reshape(-1)),
+                              DR, NE, buf[e * per_d:(e + 1) * per_d], per_d)
+        downs.append(buf)
     c3 = {}
     for bucket, live in ((16, 1), (16, 9), (128, 128)):
         xr = dev(synth.activations(120 + live, bucket, DR))
@@ -605,14 +613,48 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
                                                           for pj in range(2)], counts, offsets, items)
 
         us_3f = _graph_us(torch, stream, [lambda r=r: routed_fused(r) for r in range(R3)], 10)
+        # the whole routed FFN: + SwiGLU over the planned pairs (live count = offsets[E]) emitting
+        # the per-pair image, the per-slot down projection and the weighted combine
+        h = torch.empty((bucket * KTOP, NE), dtype=torch.float32, device="cuda")
+        himg = torch.empty((bucket * KTOP * (NE // 32) * 36,), dtype=torch.uint8, device="cuda")
+        yd = torch.empty((bucket * KTOP, DR), dtype=torch.float32, device="cuda")
+        yo = torch.empty((bucket, DR), dtype=torch.float32, device="cuda")
+        glu_p = lambda: qk.qk_glu_q8_1("swiglu", "separate", ys[0], NE, ys[1], NE, bucket * KTOP, NE, h, NE, himg,
+                                       NE // 32, offsets[E:])
+        down_p = lambda r: qk.qk_mmvq_id_slots(himg, NE // 32, bucket, KTOP,
+                                               [qk.make_proj_id("q4_0", E, downs[r], DR, NE, yd)],
+                                               counts, offsets, items)
+        comb = lambda: qk.qk_moe_combine(yd, DR, wts, bucket, KTOP, DR, yo, DR, d_live_rows=lv)
+
+        def ffn(r):
+            routed_fused(r)
+            glu_p()
+            down_p(r)
+            comb()
+
+        us_ffn = _graph_us(torch, stream, [lambda r=r: ffn(r) for r in range(R3)], 10)
+        per_kernel["glu_q8_1(pairs)"] = _graph_us(torch, stream, [glu_p] * 16, 10)
+        per_kernel["mmvq_id_slots(down)"] = _graph_us(torch, stream, [lambda r=r: down_p(r)
+                                                                      for r in list(range(R3)) * 8], 10)
+        per_kernel["moe_combine"] = _graph_us(torch, stream, [comb] * 16, 10)
+        per_kernel["route_plan"] = _graph_us(torch, stream, [lambda: qk.qk_route_plan(
+            logits, bucket, E, KTOP, ids, wts, counts, offsets, items, d_live_rows=lv)] * 16, 10)
+        wbd = touched * per_d
         c3[f"live{live}_bucket{bucket}"] = {"us": round(us_3, 3), "us_route_plan_one_launch": round(us_3f, 3),
                                             "distinct_experts": touched, "weight_bytes": wb,
                                             "weight_gbs": gb(wb, us_3),
                                             "kernels": ["rmsnorm_q8_1", "topk_route", "moe_plan", "mmvq_id(gate,up)"],
                                             "per_kernel_us": {k: round(v, 3) for k, v in per_kernel.items()},
-                                            "mmvq_id_gbs": gb(wb, per_kernel["mmvq_id"])}
+                                            "mmvq_id_gbs": gb(wb, per_kernel["mmvq_id"]),
+                                            "ffn": {"us": round(us_ffn, 3),
+                                                    "kernels": ["rmsnorm_q8_1", "route_plan", "mmvq_id(gate,up)",
+                                                                "glu_q8_1(pairs)", "mmvq_id_slots(down)",
+                                                                "moe_combine"],
+                                                    "weight_bytes": wb + wbd, "weight_gbs": gb(wb + wbd, us_ffn),
+                                                    "down_weight_bytes": wbd,
+                                                    "down_gbs": gb(wbd, per_kernel["mmvq_id_slots(down)"])}}
     out["c3_routed"] = c3
-    del experts
+    del experts, downs
 
     # ---- config 4: prefill layer, Q8_0 image once per activation, MMQ q/k/v and gate/up
     TP, DP, NFF = 3325, 3584, 18944

@@ -388,8 +388,9 @@ QK_API qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t row
 /*
  * qk_mmvq_id_slots -- qk_mmvq_id with one image row per pair: y[p][:] =
  * W_e * image row p (the per-slot down projection of a routed FFN, whose
- * input is each pair's own GLU output; TensorFold PR #1047 "Ordinary, K8192
- * / 32 slots" and "K2560 / 128 slots" components). img has rows * k rows.
+ * input is each pair's own GLU output; llama.cpp PR #117, "GLU producer
+ * evidence" table, the per-slot routed components "K8192 / 32 slots / T8" and
+ * "K2560 / 128 slots / T8"). img has rows * k rows.
  * Errors: as qk_mmvq_id.
  */
 QK_API qk_status qk_mmvq_id_slots(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k,

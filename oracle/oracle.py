@@ -241,8 +241,8 @@ def proj_id_q8_1(wtype: str, W: np.ndarray, E: int, N: int, K: int, img: np.ndar
 
 def proj_id_slots_q8_1(wtype: str, W: np.ndarray, E: int, N: int, K: int, img: np.ndarray, row_blocks: int,
                        ids: np.ndarray, items: np.ndarray) -> np.ndarray:
-    """Per-slot routed projection (the down projection of a routed FFN; TensorFold
-    PR #1047 "Ordinary, K8192 / 32 slots" and "K2560 / 128 slots" components):
+    """Per-slot routed projection (the down projection of a routed FFN; llama.cpp
+    PR #117, "GLU producer evidence" table, the per-slot routed components):
     pair p = row*k + slot reads image row p, its own GLU output, instead of the
     token's row. This is the routed projection of the flattened pairs, one slot
     per row, so it reuses proj_id_q8_1 with ids viewed as [rows*k][1]."""

@@ -5,6 +5,8 @@
 //             Overview/Coverage; its "Ordinary, K8192 / T8" component).
 //   mmvq_id : routed MUL_MAT_ID over a stable expert plan; experts with no
 //             planned pair read no weights (TensorFold PR #1047, "The fix").
+//             Per-pair mode reads image row p for pair p (the per-slot down
+//             projection; PR #117 "GLU producer evidence", per-slot routed rows).
 //
 // Per 32-block b of weight row n and image row t, from the stored halves:
 //   Q4_0: y += d_w * (d_a * D - 8 * s_a),   D = sum nibble_i * q_i
