@@ -17,6 +17,8 @@ duration with the case's algorithmic bytes (or flops) per launch. Cases:
   quantize      qk_quantize_q8_1, [8, 8192]         (kernel quantize)
   glu           qk_glu_q8_1 SwiGLU packed [8, 18944] (kernel glu_q8_1)
   mmvq_id_<R>   qk_mmvq_id, gate+up 2560->768 over 128 experts, top-8 of R rows (kernel mmvq_id)
+  mmvq_id_slots_<R>  qk_mmvq_id_slots, per-slot down 768->2560 over 128 experts, top-8 of R rows
+                (one image row per pair; kernel mmvq_id)
   routed_<R>    the routed chain for R live rows of a 16/128 bucket: RMSNorm*w -> image, top-8 of
                 128, plan, mmvq_id gate+up (kernels rmsnorm_q8_1, topk, plan, mmvq_id)
   mmq_qkv       qk_mmq, 3325 tokens, q/k/v          (kernels dequant_b, mmq_tc)
@@ -108,6 +110,28 @@ def build_case(name):
         nbytes = 3 * T * N * 4 + T * (N // 32) * Q8_1_BLOCK
         return (lambda: qk.qk_glu_q8_1("swiglu", "packed", a, 2 * N, None, 0, T, N, out, N, img, N // 32),
                 [a, out, img], {"bytes": nbytes})
+    if name.startswith("mmvq_id_slots_"):
+        # per-slot down projection of the 128-expert FFN: pair p reads image row p (768 columns)
+        E, k, K, N, rows = 128, 8, 768, 2560, int(name.rsplit("_", 1)[1])
+        per = qk.qk_weight_packed_bytes("q4_0", N, K)
+        wd = torch.empty((E * per,), dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            qk.qk_weight_pack("q4_0", _dev(synth.q4_0_weight(3000 + e, N, K).reshape(-1)), N, K,
+                              wd[e * per:(e + 1) * per], per)
+        img = _image(rows * k, K)
+        ids = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+        wts = torch.empty((rows, k), dtype=torch.float32, device="cuda")
+        qk.qk_topk_route(_dev(synth.router_logits(3, rows, E)), rows, E, k, ids, wts)
+        counts = torch.empty((E,), dtype=torch.int32, device="cuda")
+        offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+        items = torch.empty((rows * k,), dtype=torch.int32, device="cuda")
+        qk.qk_moe_plan(ids, rows, k, E, counts, offsets, items)
+        y = torch.empty((rows * k, N), dtype=torch.float32, device="cuda")
+        projs = [qk.make_proj_id("q4_0", E, wd, N, K, y)]
+        live = int((counts > 0).sum().item())
+        nbytes = live * per + rows * k * N * 4 + rows * k * (K // 32) * Q8_1_BLOCK
+        return (lambda: qk.qk_mmvq_id_slots(img, K // 32, rows, k, projs, counts, offsets, items),
+                [wd, img, ids, wts, counts, offsets, items, y], {"bytes": nbytes, "live_experts": live})
     if name.startswith("mmvq_id_"):
         E, k, K, NF, rows = 128, 8, 2560, 768, int(name.rsplit("_", 1)[1])
         per = qk.qk_weight_packed_bytes("q4_0", NF, K)
