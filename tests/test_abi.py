@@ -106,3 +106,33 @@ def test_weight_pack_checks(lib):
     assert lib.qk_weight_pack(0, P(X), 100, 256, P(W), need - 1, None) == 4
     assert lib.qk_weight_pack(0, P(X), 100, 250, P(W), need, None) == 2
     assert lib.qk_weight_pack(0, P(X), 100, 256, P(X + 64), need, None) == 3
+
+
+def test_routed_ffn_checks(lib):
+    """Argument refusals of the per-slot projection and the combine (host checks only: no launch)."""
+    P = C.c_void_p
+    # combine: N not a multiple of 4, stride < N, misaligned y, y over expert_out, N too large, k out of range
+    assert lib.qk_moe_combine(P(X), 64, P(W), 4, 2, 62, P(Y), 64, None, None) == 1
+    assert lib.qk_moe_combine(P(X), 60, P(W), 4, 2, 64, P(Y), 64, None, None) == 2
+    assert lib.qk_moe_combine(P(X), 64, P(W), 4, 2, 64, P(Y + 4), 64, None, None) == 1
+    assert lib.qk_moe_combine(P(X), 64, P(W), 4, 2, 64, P(X + 256), 64, None, None) == 3
+    assert lib.qk_moe_combine(P(X), 1 << 26, P(W), 1, 1, 1 << 26, P(Y), 1 << 26, None, None) == 1
+    assert lib.qk_moe_combine(P(X), 64, P(W), 4, 0, 64, P(Y), 64, None, None) == 1
+    # per-slot projection: the image has rows * k rows, so an output placed after rows image rows
+    # overlaps it (the per-token call would not see an overlap there)
+    rows, k, rb = 2, 4, 8
+    y_in_img = IMG + rows * rb * 36
+    arr = (qk.qk_proj_id * 1)(qk.qk_proj_id(0, 4, W, 128, 256, y_in_img))
+    assert lib.qk_mmvq_id_slots(P(IMG), rb, rows, k, 1, arr, P(X), P(X + 64), P(X + 128), None) == 3
+    arr9 = (qk.qk_proj_id * 9)(*[qk.qk_proj_id(0, 4, W, 128, 256, Y + i * (1 << 20)) for i in range(9)])
+    assert lib.qk_mmvq_id_slots(P(IMG), rb, rows, k, 9, arr9, P(X), P(X + 64), P(X + 128), None) == 5
+    assert lib.qk_mmvq_id_slots(P(IMG), rb, rows, 65, 1, arr, P(X), P(X + 64), P(X + 128), None) == 1
+
+
+def test_grid_limits_are_refused(lib):
+    """Row-block and width limits that keep every grid dimension in range."""
+    P = C.c_void_p
+    assert lib.qk_quantize_q8_1(P(X), 1, 32, 32, P(IMG), (1 << 20) + 1, None, None) == 1
+    assert lib.qk_quantize_q8_1(P(X), 1, (1 << 25) + 32, (1 << 25) + 32, P(IMG), 1 << 20, None, None) == 1
+    assert lib.qk_glu_q8_1(0, 0, P(X), 1 << 26, P(W), 1 << 26, 1, 1 << 26, P(Y), 1 << 26, P(IMG), 1 << 21,
+                           None, None) == 1
