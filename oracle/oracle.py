@@ -29,7 +29,7 @@ _lib = None
 Q8_1_BYTES = 36
 WTYPE = {"q4_0": 0, "q8_0": 1}
 NORM_KIND = {"plain": 0, "mul": 1, "mul_add": 2, "scale": 3}
-GLU_KIND = {"swiglu": 0, "geglu_tanh": 1, "reglu": 2}
+GLU_KIND = {"swiglu": 0, "geglu_tanh": 1, "reglu": 2, "geglu_erf": 3, "geglu_quick": 4, "swiglu_oai": 5}
 GLU_LAYOUT = {"separate": 0, "packed": 1, "packed_swapped": 2}
 
 
@@ -59,7 +59,7 @@ def _load():
             lib.or_quantize_q8_1.argtypes = [P, I64, I64, I64, P, I64, P]
             lib.or_quantize_q8_0.argtypes = [P, I64, I64, I64, P, P, I64, P]
             lib.or_rmsnorm.argtypes = [P, I64, I64, I64, C.c_int, P, P, C.c_double, C.c_double, P, P]
-            lib.or_glu.argtypes = [C.c_int, C.c_int, P, I64, P, I64, I64, I64, P, P]
+            lib.or_glu.argtypes = [C.c_int, C.c_int, P, I64, P, I64, I64, I64, C.c_double, C.c_double, P, P]
             lib.or_dequant.argtypes = [C.c_int, P, I64, I64, P]
             lib.or_proj_q8_1.argtypes = [C.c_int, P, I64, I64, P, I64, I64, P]
             lib.or_proj_q8_0_sampled.argtypes = [C.c_int, P, I64, I64, P, P, I64, P, I64, P, I64, P]
@@ -150,18 +150,20 @@ def rmsnorm(x: np.ndarray, kind: str = "plain", w=None, b=None, scale: float = 1
 
 
 def glu(kind: str, layout: str, a: np.ndarray, b: np.ndarray | None, N: int,
-        live: int | None = None) -> np.ndarray:
+        live: int | None = None, alpha: float = 1.702, limit: float = 7.0) -> np.ndarray:
     """GLU producer output in float64, shape [T, N].
 
     layout "separate": a holds g rows, b holds u rows. "packed": a rows are
-    [g | u]. "packed_swapped": a rows are [u | g].
+    [g | u]. "packed_swapped": a rows are [u | g]. alpha and limit are the
+    SwiGLU-OAI parameters (taken as binary32 values, as the device receives them).
     """
     a = np.ascontiguousarray(a, dtype=np.float32)
     T = a.shape[0]
     bb = a if b is None else np.ascontiguousarray(b, dtype=np.float32)
     out = np.zeros((T, N), dtype=np.float64)
     la, lp = _live(live)
-    _load().or_glu(GLU_KIND[kind], GLU_LAYOUT[layout], _p(a), a.shape[1], _p(bb), bb.shape[1], T, N, _p(out), lp)
+    _load().or_glu(GLU_KIND[kind], GLU_LAYOUT[layout], _p(a), a.shape[1], _p(bb), bb.shape[1], T, N,
+                   float(np.float32(alpha)), float(np.float32(limit)), _p(out), lp)
     return out
 
 

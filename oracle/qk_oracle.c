@@ -281,28 +281,49 @@ void or_rmsnorm(const float *x, int64_t T, int64_t K, int64_t x_stride, int kind
 }
 
 /* ------------------------------------------------------------------------ */
-/* GLU producers ([P1] Coverage: F32 ReGLU, GeGLU, SwiGLU; separate, packed  */
-/* and packed-swapped inputs with independent row strides).                  */
-/*   SwiGLU:     out = g * sigmoid(g) * u                                    */
-/*   GeGLU-tanh: out = 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) * u   */
-/*   ReGLU:      out = max(g, 0) * u                                         */
-/* kind: 0 swiglu, 1 geglu-tanh, 2 reglu. layout: 0 separate (g at a, u at  */
-/* b), 1 packed row [g | u] at a, 2 packed-swapped row [u | g] at a.         */
+/* GLU producers ([P1] Coverage: F32 ReGLU, GeGLU, SwiGLU, GeGLU-erf,       */
+/* GeGLU-quick, SwiGLU-OAI with alpha/limit; separate, packed and            */
+/* packed-swapped inputs with independent row strides). The page names the  */
+/* kinds only; the formulas are the published ones:                          */
+/*   SwiGLU:      out = g * sigmoid(g) * u                                   */
+/*   GeGLU-tanh:  out = 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) * u  */
+/*   ReGLU:       out = max(g, 0) * u                                        */
+/*   GeGLU-erf:   out = 0.5 g (1 + erf(g / sqrt 2)) * u  (GELU, Hendrycks &  */
+/*                Gimpel 2016, exact form)                                   */
+/*   GeGLU-quick: out = g * sigmoid(1.702 g) * u  (the same paper's sigmoid  */
+/*                approximation)                                             */
+/*   SwiGLU-OAI:  x = min(g, limit), v = clamp(u, -limit, limit),            */
+/*                out = x * sigmoid(alpha x) * (v + 1)  (gpt-oss MLP)        */
+/* kind: 0 swiglu, 1 geglu-tanh, 2 reglu, 3 geglu-erf, 4 geglu-quick,         */
+/* 5 swiglu-oai. layout: 0 separate (g at a, u at b), 1 packed row [g | u]   */
+/* at a, 2 packed-swapped row [u | g] at a.                                  */
 /* ------------------------------------------------------------------------ */
-static double glu_act(int kind, double g)
+static double glu_value(int kind, double g, double u, double alpha, double limit)
 {
-    if (kind == 0)
-        return g / (1.0 + exp(-g));
-    if (kind == 1) {
+    switch (kind) {
+    case 0:
+        return g / (1.0 + exp(-g)) * u;
+    case 1: {
         const double c = 0.7978845608028654; /* sqrt(2/pi) */
-        return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g)));
+        return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g))) * u;
     }
-    return g > 0.0 ? g : 0.0;
+    case 3:
+        return 0.5 * g * (1.0 + erf(g / sqrt(2.0))) * u;
+    case 4:
+        return g / (1.0 + exp(-1.702 * g)) * u;
+    case 5: {
+        double x = g < limit ? g : limit;
+        double v = u < -limit ? -limit : (u > limit ? limit : u);
+        return x / (1.0 + exp(-alpha * x)) * (v + 1.0);
+    }
+    default:
+        return (g > 0.0 ? g : 0.0) * u;
+    }
 }
 
 void or_glu(int kind, int layout, const float *a, int64_t a_stride,
             const float *bsrc, int64_t b_stride, int64_t T, int64_t N,
-            double *out, const int32_t *live)
+            double alpha, double limit, double *out, const int32_t *live)
 {
     int64_t nlive = live_count(live, T);
     for (int64_t t = 0; t < nlive; t++) {
@@ -318,7 +339,7 @@ void or_glu(int kind, int layout, const float *a, int64_t a_stride,
             g = u + N;
         }
         for (int64_t i = 0; i < N; i++)
-            out[t * N + i] = glu_act(kind, (double)g[i]) * (double)u[i];
+            out[t * N + i] = glu_value(kind, (double)g[i], (double)u[i], alpha, limit);
     }
 }
 

@@ -21,7 +21,7 @@ QK_OK = 0
 STATUS = {0: "QK_OK", 1: "QK_ERR_ARG", 2: "QK_ERR_SHAPE", 3: "QK_ERR_ALIAS", 4: "QK_ERR_WORKSPACE",
           5: "QK_ERR_UNSUPPORTED", 6: "QK_ERR_CUDA"}
 NORM = {"plain": 0, "mul": 1, "mul_add": 2, "scale": 3}
-GLU = {"swiglu": 0, "geglu_tanh": 1, "reglu": 2}
+GLU = {"swiglu": 0, "geglu_tanh": 1, "reglu": 2, "geglu_erf": 3, "geglu_quick": 4, "swiglu_oai": 5}
 LAYOUT = {"separate": 0, "packed": 1, "packed_swapped": 2}
 WTYPE = {"q4_0": 0, "q8_0": 1}
 Q8_1_BLOCK_BYTES = 36
@@ -57,6 +57,8 @@ _SIGS = {
     "qk_rmsnorm_q8_1": ([P, I64, I64, I64, C.c_int, P, P, F32, F32, P, I64, P, I64, P, P], C.c_int),
     "qk_rmsnorm_q8_0": ([P, I64, I64, I64, C.c_int, P, P, F32, F32, P, I64, P, P, I64, P, P], C.c_int),
     "qk_glu_q8_1": ([C.c_int, C.c_int, P, I64, P, I64, I64, I64, P, I64, P, I64, P, P], C.c_int),
+    "qk_glu_q8_1_ex": ([C.c_int, C.c_int, P, I64, P, I64, I64, I64, P, I64, P, I64, C.c_float, C.c_float, P, P],
+                       C.c_int),
     "qk_weight_packed_bytes": ([C.c_int, I64, I64], SZ),
     "qk_weight_pack": ([C.c_int, P, I64, I64, P, SZ, P], C.c_int),
     "qk_device_faults": ([C.POINTER(C.c_uint32)], C.c_int),
@@ -167,6 +169,16 @@ def qk_glu_q8_1(kind, layout, a, a_stride, b, b_stride, T, N, out, out_stride, i
     _check("qk_glu_q8_1", load().qk_glu_q8_1(kind, layout, _ptr(a), a_stride, _ptr(b), b_stride, T, N, _ptr(out),
                                              out_stride, _ptr(img), img_row_blocks, _ptr(d_live_rows),
                                              _stream(stream)))
+
+
+def qk_glu_q8_1_ex(kind, layout, a, a_stride, b, b_stride, T, N, out, out_stride, img, img_row_blocks,
+                   alpha=1.702, limit=7.0, d_live_rows=None, stream=None):
+    kind = GLU[kind] if isinstance(kind, str) else int(kind)
+    layout = LAYOUT[layout] if isinstance(layout, str) else int(layout)
+    _check("qk_glu_q8_1_ex", load().qk_glu_q8_1_ex(kind, layout, _ptr(a), a_stride, _ptr(b), b_stride, T, N,
+                                                   _ptr(out), out_stride, _ptr(img), img_row_blocks,
+                                                   float(alpha), float(limit), _ptr(d_live_rows),
+                                                   _stream(stream)))
 
 
 # ------------------------------------------------------------------ weights

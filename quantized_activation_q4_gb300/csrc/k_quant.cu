@@ -223,20 +223,30 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
 }
 
 // ---------------------------------------------------------------- GLU producer
-__device__ __forceinline__ float glu_act(int kind, float g) {
-    if (kind == QK_GLU_SWIGLU) return g / (1.0f + expf(-g));
-    if (kind == QK_GLU_GEGLU_TANH) {
-        const float c = 0.7978845608028654f;  // sqrt(2/pi)
-        return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
+// act(g) * u for the GLU kinds; SwiGLU-OAI clamps g from above and u both ways at limit
+// and multiplies by (u + 1).
+__device__ __forceinline__ float glu_out(int kind, float g, float u, float alpha, float limit) {
+    switch (kind) {
+        case QK_GLU_SWIGLU: return g / (1.0f + expf(-g)) * u;
+        case QK_GLU_GEGLU_TANH: {
+            const float c = 0.7978845608028654f;  // sqrt(2/pi)
+            return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g))) * u;
+        }
+        case QK_GLU_GEGLU_ERF: return 0.5f * g * (1.0f + erff(g * 0.7071067811865476f)) * u;
+        case QK_GLU_GEGLU_QUICK: return g / (1.0f + expf(-1.702f * g)) * u;
+        case QK_GLU_SWIGLU_OAI: {
+            const float x = fminf(g, limit), v = fminf(fmaxf(u, -limit), limit);
+            return x / (1.0f + expf(-alpha * x)) * (v + 1.0f);
+        }
+        default: return fmaxf(g, 0.0f) * u;
     }
-    return fmaxf(g, 0.0f);
 }
 
 // grid (ceil(N/1024), T), 256 threads; thread i handles columns 1024*bx + 4i.
 __global__ void __launch_bounds__(256) glu_q8_1_kernel(
     int kind, int layout, const float *__restrict__ a, int64_t a_stride, const float *__restrict__ b,
     int64_t b_stride, int N, float *__restrict__ out, int64_t out_stride, uint8_t *__restrict__ img,
-    int64_t row_blocks, int T, const int32_t *live) {
+    int64_t row_blocks, int T, float alpha, float limit, const int32_t *live) {
     pdl_trigger();
     pdl_wait();
     const int t = blockIdx.x;
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(256) glu_q8_1_kernel(
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
 #pragma unroll
-        for (int i = 0; i < 4; i++) v[i] = glu_act(kind, gv[i]) * uv[i];
+        for (int i = 0; i < 4; i++) v[i] = glu_out(kind, gv[i], uv[i], alpha, limit);
         store4(out + t * out_stride + c, v);
     }
     uint32_t codes;
@@ -331,11 +341,12 @@ qk_status launch_rmsnorm_q8_0(const float *x, int T, int K, int64_t x_stride, in
 
 qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride, const float *b,
                           int64_t b_stride, int T, int N, float *out, int64_t out_stride,
-                          uint8_t *img, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
+                          uint8_t *img, int64_t row_blocks, float alpha, float limit, const int32_t *live,
+                          cudaStream_t s) {
     if (T == 0) return QK_OK;
     dim3 grid((unsigned)T, (unsigned)ceil_div(N, 1024));
     return launch_pdl("glu_q8_1", glu_q8_1_kernel, grid, dim3(256), 0, s, kind, layout, a, a_stride, b, b_stride,
-                      N, out, out_stride, img, row_blocks, T, live);
+                      N, out, out_stride, img, row_blocks, T, alpha, limit, live);
 }
 
 }  // namespace qk

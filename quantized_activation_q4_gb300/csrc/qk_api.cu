@@ -7,6 +7,7 @@
 // emission", Coverage: unsafe input/output aliases keep the original path).
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -169,7 +170,17 @@ qk_status qk_glu_q8_1(qk_glu_kind kind, qk_glu_layout layout, const float *a, in
                       const float *b, int64_t b_stride, int64_t T, int64_t N, float *out,
                       int64_t out_stride, void *img, int64_t img_row_blocks, const int32_t *d_live_rows,
                       qk_stream stream) {
-    REQUIRE(kind >= QK_GLU_SWIGLU && kind <= QK_GLU_REGLU, QK_ERR_ARG, "bad glu kind %d", (int)kind);
+    return qk_glu_q8_1_ex(kind, layout, a, a_stride, b, b_stride, T, N, out, out_stride, img, img_row_blocks,
+                          1.702f, 7.0f, d_live_rows, stream);
+}
+
+qk_status qk_glu_q8_1_ex(qk_glu_kind kind, qk_glu_layout layout, const float *a, int64_t a_stride,
+                         const float *b, int64_t b_stride, int64_t T, int64_t N, float *out,
+                         int64_t out_stride, void *img, int64_t img_row_blocks, float alpha, float limit,
+                         const int32_t *d_live_rows, qk_stream stream) {
+    REQUIRE(kind >= QK_GLU_SWIGLU && kind <= QK_GLU_SWIGLU_OAI, QK_ERR_ARG, "bad glu kind %d", (int)kind);
+    REQUIRE(std::isfinite(alpha) && std::isfinite(limit) && limit > 0.0f, QK_ERR_ARG,
+            "alpha must be finite and limit positive and finite");
     REQUIRE(layout >= QK_GLU_SEPARATE && layout <= QK_GLU_PACKED_SWAPPED, QK_ERR_ARG, "bad glu layout %d", (int)layout);
     REQUIRE(T >= 0 && T <= INT32_MAX && N >= 1 && N <= (1LL << 25), QK_ERR_ARG, "T or N out of range");
     REQUIRE(N % QB == 0, QK_ERR_SHAPE, "N=%lld is not a whole number of 32-blocks", (long long)N);
@@ -187,7 +198,8 @@ qk_status qk_glu_q8_1(qk_glu_kind kind, qk_glu_layout layout, const float *a, in
     REQUIRE(!overlap(so, sa) && !overlap(so, sb) && !overlap(so, si) && !overlap(si, sa) && !overlap(si, sb),
             QK_ERR_ALIAS, "out or img overlaps an input or each other");
     return launch_glu_q8_1((int)kind, (int)layout, a, a_stride, b, b_stride, (int)T, (int)N, out, out_stride,
-                           static_cast<uint8_t *>(img), img_row_blocks, d_live_rows, (cudaStream_t)stream);
+                           static_cast<uint8_t *>(img), img_row_blocks, alpha, limit, d_live_rows,
+                           (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------------ weights

@@ -133,7 +133,8 @@ qk_status launch_rmsnorm_q8_0(const float *x, int T, int K, int64_t x_stride, in
                               uint16_t *dh, int64_t row_blocks, const int32_t *live, cudaStream_t s);
 qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride, const float *b,
                           int64_t b_stride, int T, int N, float *out, int64_t out_stride,
-                          uint8_t *img, int64_t row_blocks, const int32_t *live, cudaStream_t s);
+                          uint8_t *img, int64_t row_blocks, float alpha, float limit, const int32_t *live,
+                          cudaStream_t s);
 qk_status launch_weight_pack(int wtype, const uint8_t *blocks, int64_t N, int64_t K,
                              uint8_t *packed, cudaStream_t s);
 int64_t mmvq_workspace_bytes(int n_proj, const qk_proj *projs);

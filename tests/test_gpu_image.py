@@ -120,7 +120,7 @@ def test_rmsnorm_q8_1(kind, T, K, live):
     assert np.all(blocks_equal[same_y])
 
 
-@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu"])
+@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu", "geglu_erf", "geglu_quick", "swiglu_oai"])
 @pytest.mark.parametrize("layout", ["separate", "packed", "packed_swapped"])
 @pytest.mark.parametrize("T,N", [(8, 18944), (3, 96)])
 def test_glu_q8_1(kind, layout, T, N):
@@ -145,10 +145,31 @@ def test_glu_q8_1(kind, layout, T, N):
     ig = host(img).reshape(T, rb * 36)
     # a few ulp of binary32 expf/tanhf and products; 1 + tanh(z) cancels for
     # very negative z, so allow a few ulp of |g u| as an absolute term too
-    tol = np.abs(ref) * 2e-6 + 3e-7 * np.abs(g.astype(np.float64) * u) + 1e-30
+    # (SwiGLU-OAI: the rounding of v + 1 gives an absolute term in |g| (|u| + 1))
+    uterm = np.abs(u) + 1.0 if kind == "swiglu_oai" else np.abs(u)
+    tol = np.abs(ref) * 2e-6 + 3e-7 * np.abs(g.astype(np.float64)) * uterm + 1e-30
     assert np.all(np.abs(og - ref) <= tol)
     assert np.array_equal(ig, O.quantize_q8_1(og, row_blocks=rb))
     assert np.array_equal(ig, gpu_quantize_q8_1(og, N, rb))
+
+
+@pytest.mark.parametrize("alpha,limit", [(1.0, 1.5), (2.5, 0.75), (1.702, 7.0)])
+def test_glu_swiglu_oai_parameters(alpha, limit):
+    """qk_glu_q8_1_ex passes alpha and limit through; both clamps are hit at these limits."""
+    import torch
+    T, N = 5, 320
+    g = synth.activations(3200, T, N) * np.float32(3.0)
+    u = synth.activations(3201, T, N) * np.float32(3.0)
+    ref = O.glu("swiglu_oai", "separate", g, u, N, alpha=alpha, limit=limit)
+    out = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
+    img = empty_u8(T * (N // 32) * 36)
+    qk.qk_glu_q8_1_ex("swiglu_oai", "separate", dev(g), N, dev(u), N, T, N, out, N, img, N // 32,
+                      alpha=alpha, limit=limit)
+    og, ig = host(out), host(img).reshape(T, -1)
+    tol = np.abs(ref) * 2e-6 + 3e-7 * np.abs(g.astype(np.float64)) * (np.abs(u) + 1.0) + 1e-30
+    assert np.all(np.abs(og - ref) <= tol)
+    assert np.array_equal(ig, O.quantize_q8_1(og, row_blocks=N // 32))
+    assert np.sum(g > limit) > 0 and np.sum(np.abs(u) > limit) > 0
 
 
 def test_glu_live_rows():

@@ -193,7 +193,58 @@ def test_glu_against_library_functions():
     assert np.allclose(gt - gm, g64, rtol=1e-13, atol=1e-13)
 
 
-@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu"])
+def test_glu_gelu_variants_against_library_and_identities():
+    """GeGLU-erf against torch's exact GELU; GeGLU-quick within the sigmoid approximation's
+    known distance of it (a wrong constant, e.g. SiLU's 1.0, misses by > 0.1); both odd parts
+    equal g."""
+    import torch
+    T, N = 3, 512
+    g = synth.activations(33, T, N) * np.float32(3.0)
+    g64 = g.astype(np.float64)
+    ones = np.ones_like(g)
+    ge = O.glu("geglu_erf", "separate", g, ones, N)
+    ref = torch.nn.functional.gelu(torch.from_numpy(g64), approximate="none").numpy()
+    assert np.allclose(ge, ref, rtol=1e-13, atol=1e-15)
+    gq = O.glu("geglu_quick", "separate", g, ones, N)
+    assert np.max(np.abs(gq - ref)) < 0.021
+    for kind in ("geglu_erf", "geglu_quick"):
+        pos = O.glu(kind, "separate", g, ones, N)
+        neg = O.glu(kind, "separate", -g, ones, N)
+        assert np.allclose(pos - neg, g64, rtol=1e-13, atol=1e-13)
+    u = synth.activations(34, T, N)
+    assert np.allclose(O.glu("geglu_erf", "separate", g, u, N), ge * u.astype(np.float64), rtol=1e-15, atol=0)
+
+
+def test_glu_swiglu_oai_reductions_and_clamps():
+    """SwiGLU-OAI inside its clamp range equals SwiGLU (alpha = 1) or GeGLU-quick (alpha = 1.702)
+    times (u + 1); past the limits it is constant in g (from above) and in u (both ways);
+    u = -1 gives 0."""
+    T, N = 2, 256
+    g = np.clip(synth.activations(35, T, N) * np.float32(2.0), -6.5, 6.5).astype(np.float32)
+    u = np.clip(synth.activations(36, T, N), -6.5, 6.5).astype(np.float32)
+    up1 = u.astype(np.float64) + 1.0
+    ones = np.ones_like(u)
+    oai1 = O.glu("swiglu_oai", "separate", g, u, N, alpha=1.0, limit=7.0)
+    assert np.allclose(oai1, O.glu("swiglu", "separate", g, ones, N) * up1, rtol=1e-13, atol=1e-300)
+    oai = O.glu("swiglu_oai", "separate", g, u, N)
+    # alpha arrives as the binary32 1.702 (1.702 + 2.2e-8) and GeGLU-quick uses 1.702 itself: for
+    # negative g the relative difference is about |g| * 2.2e-8 <= 1.5e-7 at |g| <= 6.5
+    assert np.allclose(oai, O.glu("geglu_quick", "separate", g, ones, N) * up1, rtol=1.5e-7, atol=1e-300)
+    big_g = np.full_like(g, 7.0) + np.abs(g)                          # g >= limit
+    at_lim = O.glu("swiglu_oai", "separate", np.full_like(g, 7.0), u, N)
+    assert np.array_equal(O.glu("swiglu_oai", "separate", big_g, u, N), at_lim)
+    for sgn in (1.0, -1.0):
+        far = np.float32(sgn) * (np.float32(7.0) + np.abs(u))        # |u| >= limit
+        lim = np.full_like(u, np.float32(sgn * 7.0))
+        assert np.array_equal(O.glu("swiglu_oai", "separate", g, far, N), O.glu("swiglu_oai", "separate", g, lim, N))
+    assert np.all(O.glu("swiglu_oai", "separate", g, -np.ones_like(u), N) == 0.0)
+    # g below -limit is not clamped (the clamp on g is one-sided)
+    low = np.full_like(g, -9.0)
+    assert not np.array_equal(O.glu("swiglu_oai", "separate", low, u, N),
+                              O.glu("swiglu_oai", "separate", np.full_like(g, -7.0), u, N))
+
+
+@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu", "geglu_erf", "geglu_quick", "swiglu_oai"])
 def test_glu_layouts(kind):
     T, N = 4, 96
     g = synth.activations(41, T, N)
