@@ -472,6 +472,25 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
         qk.qk_weight_pack("q4_0", dev(synth.q4_0_weight(seed, N, K).reshape(-1)), N, K, buf, nbytes)
         return buf
 
+    # ---- config 0: one token, d = 256: RMS*w -> image -> one 256x256 Q4_0 projection (latency only)
+    x0 = dev(synth.activations(10, 1, 256))
+    w0 = dev(synth.norm_weight(11, 256))
+    y0 = torch.empty((1, 256), dtype=torch.float32, device="cuda")
+    img0 = torch.empty((8 * 36,), dtype=torch.uint8, device="cuda")
+    out0 = torch.empty((1, 256), dtype=torch.float32, device="cuda")
+    w0p = packed(12, 256, 256)                # kept alive: the descriptor holds a raw pointer
+    p0 = [qk.make_proj("q4_0", w0p, 256, 256, out0, 256)]
+    ws0_n = qk.qk_mmvq_workspace_bytes(p0)
+    ws0 = torch.zeros((ws0_n,), dtype=torch.uint8, device="cuda")
+
+    def tiny():
+        qk.qk_rmsnorm_q8_1(x0, 1, 256, 256, "mul", w0, None, 1.0, 1e-6, y0, 256, img0, 8)
+        qk.qk_mmvq(img0, 8, 1, p0, ws0, ws0_n)
+
+    out["c0_latency"] = {"us": round(_graph_us(torch, stream, [tiny] * 16, 10), 3),
+                         "kernels": ["rmsnorm_q8_1", "mmvq"],
+                         "note": "latency-bound (36,864 B of weights, L2-warm): microseconds only"}
+
     # ---- config 1 control: RMS writing F32 only, then quantize, then MMVQ (q/k/v)
     x = dev(synth.activations(100, T, D_ATTN))
     w = dev(synth.norm_weight(101, D_ATTN))
@@ -571,7 +590,7 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
                               DR, NE, buf[e * per_d:(e + 1) * per_d], per_d)
         downs.append(buf)
     c3 = {}
-    for bucket, live in ((16, 1), (16, 9), (128, 128)):
+    for bucket, live in ((16, 1), (16, 9), (32, 17), (128, 113), (128, 128)):
         xr = dev(synth.activations(120 + live, bucket, DR))
         wr = dev(synth.norm_weight(121, DR))
         yr = torch.empty((bucket, DR), dtype=torch.float32, device="cuda")
