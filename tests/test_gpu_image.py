@@ -43,6 +43,21 @@ def test_quantize_q8_1_matches_oracle(T, K, stride, rb):
     assert np.array_equal(got, O.quantize_q8_1(x, K=K, row_blocks=rb))
 
 
+def test_quantize_and_glu_more_rows_than_a_grid_y_dimension():
+    """70,000 rows (over the 65,535 limit of a grid's y dimension): rows run on grid x."""
+    import torch
+    T, K = 70000, 64
+    x = synth.activations(1200, T, K)
+    assert np.array_equal(gpu_quantize_q8_1(x, K, 2), O.quantize_q8_1(x))
+    u = synth.activations(1201, T, K)
+    out = torch.full((T, K), float("nan"), dtype=torch.float32, device="cuda")
+    img = empty_u8(T * 2 * 36)
+    qk.qk_glu_q8_1("reglu", "separate", dev(x), K, dev(u), K, T, K, out, K, img, 2)
+    og = host(out)
+    assert np.array_equal(og, (np.maximum(x, 0.0) * u).astype(np.float32))   # one binary32 product each
+    assert np.array_equal(host(img).reshape(T, -1), O.quantize_q8_1(og))
+
+
 def test_quantize_q8_1_live_rows_untouched():
     T, K = 16, 256
     x = synth.poison_rows(synth.activations(1100, T, K), live=9)

@@ -309,3 +309,19 @@ def test_captured_ffn_replay_with_poisoned_padding(ffn, bucket, lives):
         torch.cuda.synchronize()
         assert np.array_equal(H["yd"][:npl].view(np.uint32), host(ref["yd"]).view(np.uint32))
         assert np.array_equal(H["y"][:live].view(np.uint32), host(ref["y"]).view(np.uint32))
+
+
+def test_combine_more_rows_than_a_grid_y_dimension():
+    """70,000 rows (over the 65,535 limit of a grid's y dimension): rows run on grid x."""
+    import torch
+    rows, k, N, live = 70000, 2, 8, 69999
+    g = synth.rng(9995)
+    eo_h = g.standard_normal((rows * k, N)).astype(np.float32)
+    w_h = g.random((rows, k)).astype(np.float32)
+    y = torch.full((rows, N), float(SENTINEL), dtype=torch.float32, device="cuda")
+    qk.qk_moe_combine(dev(eo_h), N, dev(w_h), rows, k, N, y, N, live_ptr(live))
+    got = host(y)
+    ref = O.moe_combine(eo_h, w_h, live=live)
+    terms = np.abs(w_h[:live, :, None].astype(np.float64) * eo_h[:live * k].reshape(live, k, N))
+    assert np.all(np.abs(got[:live] - ref[:live]) <= k * 2.0 ** -24 * terms.sum(axis=1) + 1e-30)
+    assert np.all(got[live:] == SENTINEL)
