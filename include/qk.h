@@ -110,6 +110,9 @@ QK_API const char *qk_status_string(qk_status s);
 /* One-line reason for the last non-QK_OK status returned on this host thread. */
 QK_API const char *qk_last_error(void);
 
+/* The same string as qk_last_error (the name used by the boundary's first sketch). */
+QK_API const char *qk_last_error_string(void);
+
 /* Number of kernels this library has launched in this process (all threads). */
 QK_API uint64_t qk_launch_count(void);
 

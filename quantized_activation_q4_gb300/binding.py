@@ -51,6 +51,7 @@ P, I32, I64, F32, SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
 _SIGS = {
     "qk_status_string": ([C.c_int], C.c_char_p),
     "qk_last_error": ([], C.c_char_p),
+    "qk_last_error_string": ([], C.c_char_p),
     "qk_launch_count": ([], C.c_uint64),
     "qk_quantize_q8_1": ([P, I64, I64, I64, P, I64, P, P], C.c_int),
     "qk_quantize_q8_0": ([P, I64, I64, I64, P, P, I64, P, P], C.c_int),

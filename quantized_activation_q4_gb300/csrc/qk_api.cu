@@ -62,6 +62,7 @@ const char *qk_status_string(qk_status s) {
 }
 
 const char *qk_last_error(void) { return g_err; }
+const char *qk_last_error_string(void) { return g_err; }
 
 uint64_t qk_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
