@@ -325,3 +325,34 @@ def test_combine_more_rows_than_a_grid_y_dimension():
     terms = np.abs(w_h[:live, :, None].astype(np.float64) * eo_h[:live * k].reshape(live, k, N))
     assert np.all(np.abs(got[:live] - ref[:live]) <= k * 2.0 ** -24 * terms.sum(axis=1) + 1e-30)
     assert np.all(got[live:] == SENTINEL)
+
+
+def test_per_slot_at_the_expert_and_slot_limits():
+    """1024 experts (the most a routed call takes) and 64 slots per row (the most a plan takes):
+    every planned pair within the exact-path NMSE, padding pairs untouched."""
+    import torch
+    rows, k, n_exp, N, K, live = 3, 64, 1024, 64, 128, 2
+    rb = K // 32
+    xs = synth.activations(9960, rows * k, K)
+    img_h = O.quantize_q8_1(xs, row_blocks=rb)
+    ids_h = synth.rng(9961).integers(0, n_exp, size=(rows, k), dtype=np.int32)
+    counts, offsets, items = _plan(ids_h, n_exp, live)
+    Ws = [synth.q4_0_weight(10000 + e, N, K) for e in range(n_exp)]
+    pw = pack_experts(Ws, "q4_0", N, K)
+    y = torch.full((rows * k, N), float(SENTINEL), dtype=torch.float32, device="cuda")
+    qk.qk_mmvq_id_slots(dev(img_h.reshape(-1)), rb, rows, k, [qk.make_proj_id("q4_0", n_exp, pw, N, K, y)],
+                        counts, offsets, items)
+    assert qk.qk_device_faults() == 0
+    _, _, rit = O.moe_plan(ids_h, n_exp, live=live)
+    got = host(y)
+    ref = O.proj_id_slots_q8_1("q4_0", np.concatenate(Ws, axis=0), n_exp, N, K, img_h, rb, ids_h, rit)
+    assert O.nmse(got[:live * k], ref[:live * k]) <= 1e-10
+    assert np.all(got[live * k:] == SENTINEL)
+
+
+def test_combine_at_the_slot_limit():
+    eo_h, w_h, got = _combine_case(5, 64, 96, 4, 9970)
+    ref = O.moe_combine(eo_h[:, :96], w_h, live=4)
+    terms = np.abs(w_h[:4, :, None].astype(np.float64) * eo_h[:4 * 64, :96].reshape(4, 64, 96))
+    assert np.all(np.abs(got[:4, :96] - ref[:4]) <= 64 * 2.0 ** -24 * terms.sum(axis=1) + 1e-30)
+    assert np.all(got[4:] == SENTINEL)
