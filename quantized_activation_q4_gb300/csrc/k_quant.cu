@@ -78,9 +78,13 @@ __device__ __forceinline__ void put_q8_1(uint8_t *blk, int j8, float d, uint32_t
 }
 
 // ---------------------------------------------------------------- quantizers
-// grid (T, ceil(row_blocks/32)), 256 threads: warp w, lane group m handles
-// block 32*blockIdx.y + 4*w + m of row blockIdx.x (rows on x: up to 2^31-1).
-template <bool Q81>
+// grid (T, ceil(row_blocks / (32*QPB))), 256 threads: lane group m of warp w
+// handles blocks 32*QPB*blockIdx.y + 32*j + 4*w + m (j < QPB) of row blockIdx.x
+// (rows on x: up to 2^31-1). A lane loads its QPB float4s before it quantises,
+// so that large images keep several loads per thread in flight (QPB = 4), while
+// small ones spread over more CTAs (QPB = 1). Every block is quantised on its
+// own, so the bytes do not depend on QPB.
+template <bool Q81, int QPB>
 __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__ x, int K,
                                                        int64_t x_stride, uint8_t *__restrict__ out,
                                                        int8_t *__restrict__ qs, uint16_t *__restrict__ dh,
@@ -89,23 +93,30 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
     pdl_wait();
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31, j8 = lane & 7;
-    const int64_t b = (int64_t)blockIdx.y * 32 + (threadIdx.x >> 5) * 4 + (lane >> 3);
-    const bool in_row = b < row_blocks;          // whole 8-lane group agrees
-    const int64_t col = b * QB + 4 * j8;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    const int64_t b0 = (int64_t)blockIdx.y * 32 * QPB + (threadIdx.x >> 5) * 4 + (lane >> 3);
+    float v[QPB][4];
     // the row's values are loaded together with the live count (row t < T is in the caller's
-    // buffer even when it is padding), so the two global reads overlap
-    if (in_row && col < K) load4(x + t * x_stride + col, (int)(K - col < 4 ? K - col : 4), v);
+    // buffer even when it is padding), so the global reads overlap
+#pragma unroll
+    for (int j = 0; j < QPB; j++) {
+        const int64_t b = b0 + 32 * j, col = b * QB + 4 * j8;
+        v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
+        if (b < row_blocks && col < K) load4(x + t * x_stride + col, (int)(K - col < 4 ? K - col : 4), v[j]);
+    }
     if (t >= live_rows(live, T)) return;
-    uint32_t codes;
-    int sum;
-    const float d = q8_block(v, &codes, &sum);  // all lanes take part in the shuffles
-    if (!in_row) return;
-    if (Q81) {
-        put_q8_1(out + (t * row_blocks + b) * Q8_1_BYTES, j8, d, codes, sum);
-    } else {
-        reinterpret_cast<uint32_t *>(qs + (t * row_blocks + b) * QB)[j8] = codes;
-        if (j8 == 0) dh[t * row_blocks + b] = __half_as_ushort(__float2half_rn(d));
+#pragma unroll
+    for (int j = 0; j < QPB; j++) {
+        const int64_t b = b0 + 32 * j;
+        uint32_t codes;
+        int sum;
+        const float d = q8_block(v[j], &codes, &sum);   // all lanes take part in the shuffles
+        if (b >= row_blocks) continue;                   // whole 8-lane group agrees
+        if (Q81) {
+            put_q8_1(out + (t * row_blocks + b) * Q8_1_BYTES, j8, d, codes, sum);
+        } else {
+            reinterpret_cast<uint32_t *>(qs + (t * row_blocks + b) * QB)[j8] = codes;
+            if (j8 == 0) dh[t * row_blocks + b] = __half_as_ushort(__float2half_rn(d));
+        }
     }
 }
 
@@ -292,22 +303,26 @@ __global__ void __launch_bounds__(256) glu_q8_1_kernel(
     }
 }
 
+constexpr int64_t QUANT_BIG_BLOCKS = 1 << 17;   // blocks per call from which QPB = 4 is used
+
 }  // namespace
 
 qk_status launch_quantize_q8_1(const float *x, int T, int K, int64_t x_stride, uint8_t *img,
                                int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
-    dim3 grid((unsigned)T, (unsigned)ceil_div(row_blocks, 32));
-    return launch_pdl("quantize_q8_1", quantize_kernel<true>, grid, dim3(256), 0, s, x, K, x_stride, img,
-                      (int8_t *)nullptr, (uint16_t *)nullptr, row_blocks, T, live);
+    const bool big = (int64_t)T * row_blocks >= QUANT_BIG_BLOCKS;
+    dim3 grid((unsigned)T, (unsigned)ceil_div(row_blocks, big ? 128 : 32));
+    return launch_pdl("quantize_q8_1", big ? quantize_kernel<true, 4> : quantize_kernel<true, 1>, grid, dim3(256),
+                      0, s, x, K, x_stride, img, (int8_t *)nullptr, (uint16_t *)nullptr, row_blocks, T, live);
 }
 
 qk_status launch_quantize_q8_0(const float *x, int T, int K, int64_t x_stride, int8_t *qs,
                                uint16_t *d, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
-    dim3 grid((unsigned)T, (unsigned)ceil_div(row_blocks, 32));
-    return launch_pdl("quantize_q8_0", quantize_kernel<false>, grid, dim3(256), 0, s, x, K, x_stride,
-                      (uint8_t *)nullptr, qs, d, row_blocks, T, live);
+    const bool big = (int64_t)T * row_blocks >= QUANT_BIG_BLOCKS;
+    dim3 grid((unsigned)T, (unsigned)ceil_div(row_blocks, big ? 128 : 32));
+    return launch_pdl("quantize_q8_0", big ? quantize_kernel<false, 4> : quantize_kernel<false, 1>, grid,
+                      dim3(256), 0, s, x, K, x_stride, (uint8_t *)nullptr, qs, d, row_blocks, T, live);
 }
 
 template <bool Q81>
