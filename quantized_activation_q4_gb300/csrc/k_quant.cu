@@ -121,17 +121,23 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
 }
 
 // ---------------------------------------------------------------- RMS producer
-// One CTA of 1024 threads per row; the row stays in registers between the
-// sum of squares and the output (thread i holds columns 4i + 4096*it for
-// it < ITEMS, ITEMS = 1, 2, 4 or 8 by K, so K <= 32768). With ITEMS <= 2 the
-// weight and bias are loaded together with the row, before the reduction.
+// One CTA per row; the row stays in registers between the sum of squares and
+// the output. The reference shape is 1024 threads (thread i holds columns
+// 4i + 4096*it for it < ITEMS, ITEMS = 1, 2, 4 or 8 by K, so K <= 32768). For
+// K <= 8192 and many rows a 256-thread CTA takes the row instead (four rows in
+// flight per SM): its thread j plays the reference threads j + 256m (m < 4)
+// and reduces their partial sums in the same order (one warp tree per m, then
+// the same 32-entry tree), so the bits are those of the 1024-thread shape.
+// With ITEMS <= 2 the weight and bias are loaded together with the row, before
+// the reduction.
 constexpr int RMS_THREADS = 1024;
 constexpr int RMS_ITEMS = 8;
+constexpr int RMS_ROWS_FOR_SMALL = 256;   // rows from which the 256-thread shape is used
 
 // Q81: the image is Q8_1 blocks (img); else Q8_0 split planes (qs codes, dh half scales), the
 // prefill layout that qk_mmq reads.
-template <int ITEMS, bool Q81>
-__global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
+template <int NT, int ITEMS, bool Q81>
+__global__ void __launch_bounds__(NT, NT == RMS_THREADS ? 1 : 4) rmsnorm_q8_1_kernel(
     const float *__restrict__ x, int K, int64_t x_stride, int kind, const float *__restrict__ w,
     const float *__restrict__ bias, float scale, float eps, float *__restrict__ y, int64_t y_stride,
     uint8_t *__restrict__ img, int8_t *__restrict__ qs, uint16_t *__restrict__ dh, int64_t row_blocks, int T,
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
     float v[ITEMS][4], wv[EARLY ? ITEMS : 1][4], bv[EARLY ? ITEMS : 1][4];
 #pragma unroll
     for (int it = 0; it < ITEMS; it++) {
-        const int c = 4 * tid + 4 * RMS_THREADS * it;
+        const int c = 4 * tid + 4 * NT * it;
         v[it][0] = v[it][1] = v[it][2] = v[it][3] = 0.0f;
         if (c < K) {
             load4(xr + c, 4, v[it]);
@@ -158,14 +164,19 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
         }
     }
     if (t >= live_rows(live, T)) return;
-    float ss = 0.0f;
-#pragma unroll
-    for (int it = 0; it < ITEMS; it++)
-        ss += v[it][0] * v[it][0] + v[it][1] * v[it][1] + v[it][2] * v[it][2] + v[it][3] * v[it][3];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+    // reference thread j + NT*m holds items m, m + R, m + 2R, ... of this thread (R = 1024 / NT)
+    constexpr int R = RMS_THREADS / NT;
     __shared__ float red[RMS_THREADS / 32];
-    if (lane == 0) red[tid >> 5] = ss;
+#pragma unroll
+    for (int m = 0; m < R; m++) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int it = m; it < ITEMS; it += R)
+            ss += v[it][0] * v[it][0] + v[it][1] * v[it][1] + v[it][2] * v[it][2] + v[it][3] * v[it][3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(FULL, ss, o);
+        if (lane == 0) red[(tid >> 5) + m * (NT / 32)] = ss;
+    }
     __syncthreads();
     if (tid < 32) {
         float tot = red[tid];
@@ -182,8 +193,8 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
     uint16_t *dr = Q81 ? nullptr : dh + t * row_blocks;
 #pragma unroll
     for (int it = 0; it < ITEMS; it++) {
-        if (4 * RMS_THREADS * it >= K) break;               // uniform: no warp has columns left
-        const int c = 4 * tid + 4 * RMS_THREADS * it;
+        if (4 * NT * it >= K) break;                        // uniform: no warp has columns left
+        const int c = 4 * tid + 4 * NT * it;
         const bool ok = c < K;                               // K % 32 == 0: whole 8-lane groups agree
         float o[4] = {0.f, 0.f, 0.f, 0.f};
         if (ok) {
@@ -219,7 +230,7 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_q8_1_kernel(
         }
     }
     // zero blocks of the row padding
-    for (int64_t bb = K / QB + tid; bb < row_blocks; bb += RMS_THREADS) {
+    for (int64_t bb = K / QB + tid; bb < row_blocks; bb += NT) {
         if (Q81) {
             uint32_t *p = reinterpret_cast<uint32_t *>(ir + bb * Q8_1_BYTES);
 #pragma unroll
@@ -330,11 +341,16 @@ static qk_status launch_rmsnorm(const float *x, int T, int K, int64_t x_stride, 
                                 const float *b, float scale, float eps, float *y, int64_t y_stride, uint8_t *img,
                                 int8_t *qs, uint16_t *dh, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
-    const int per = 4 * RMS_THREADS;   // columns per item
-    auto kernel = K <= per ? rmsnorm_q8_1_kernel<1, Q81>
-                  : K <= 2 * per ? rmsnorm_q8_1_kernel<2, Q81>
-                  : K <= 4 * per ? rmsnorm_q8_1_kernel<4, Q81>
-                                 : rmsnorm_q8_1_kernel<RMS_ITEMS, Q81>;
+    const int per = 4 * RMS_THREADS;   // columns per item of the reference shape
+    if (T >= RMS_ROWS_FOR_SMALL && K <= 2 * per) {   // 256 threads, four times the items
+        auto kernel = K <= per ? rmsnorm_q8_1_kernel<256, 4, Q81> : rmsnorm_q8_1_kernel<256, 8, Q81>;
+        return launch_pdl(Q81 ? "rmsnorm_q8_1" : "rmsnorm_q8_0", kernel, dim3((unsigned)T), dim3(256), 0, s, x,
+                          K, x_stride, kind, w, b, scale, eps, y, y_stride, img, qs, dh, row_blocks, T, live);
+    }
+    auto kernel = K <= per ? rmsnorm_q8_1_kernel<RMS_THREADS, 1, Q81>
+                  : K <= 2 * per ? rmsnorm_q8_1_kernel<RMS_THREADS, 2, Q81>
+                  : K <= 4 * per ? rmsnorm_q8_1_kernel<RMS_THREADS, 4, Q81>
+                                 : rmsnorm_q8_1_kernel<RMS_THREADS, RMS_ITEMS, Q81>;
     return launch_pdl(Q81 ? "rmsnorm_q8_1" : "rmsnorm_q8_0", kernel, dim3((unsigned)T), dim3(RMS_THREADS), 0, s, x,
                       K, x_stride, kind, w, b, scale, eps, y, y_stride, img, qs, dh, row_blocks, T, live);
 }

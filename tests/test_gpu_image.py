@@ -229,3 +229,33 @@ def test_rmsnorm_q8_0_planes(kind, T, K, live):
     q_o, d_o = O.quantize_q8_0(yg[:n], row_blocks=rb)
     assert np.array_equal(qg[:n], q_o) and np.array_equal(dg[:n], d_o)
     assert np.all(np.isnan(yg[n:])) and np.all(qg[n:] == 0x5A) and np.all(dg[n:] == 0x5A5A)
+
+
+@pytest.mark.parametrize("K", [3584, 8192, 256])
+@pytest.mark.parametrize("q81", [True, False])
+def test_rmsnorm_bits_do_not_depend_on_the_row_count(K, q81):
+    """Many rows run in 256-thread CTAs that reduce in the 1024-thread order: the first rows of a
+    300-row call equal an 8-row call byte for byte (F32 output and image)."""
+    import torch
+    T_big, T_small, rb = 300, 8, K // 32
+    x = synth.activations(5100 + K, T_big, K)
+    w = dev(synth.norm_weight(5101, K))
+
+    def run(T):
+        y = torch.full((T, K), float("nan"), dtype=torch.float32, device="cuda")
+        xd = dev(x[:T])
+        if q81:
+            img = empty_u8(T * rb * 36)
+            qk.qk_rmsnorm_q8_1(xd, T, K, K, "mul", w, None, 1.0, 1e-6, y, K, img, rb)
+            return host(y), host(img).reshape(T, -1)
+        qs = torch.zeros((T * rb * 32,), dtype=torch.int8, device="cuda")
+        d = torch.zeros((T * rb,), dtype=torch.int16, device="cuda")
+        qk.qk_rmsnorm_q8_0(xd, T, K, K, "mul", w, None, 1.0, 1e-6, y, K, qs, d, rb)
+        return host(y), np.concatenate([host(qs).reshape(T, -1).view(np.uint8), host(d).reshape(T, -1).view(np.uint8)], 1)
+
+    yb, ib = run(T_big)
+    ys, is_ = run(T_small)
+    assert np.array_equal(yb[:T_small].view(np.uint32), ys.view(np.uint32))
+    assert np.array_equal(ib[:T_small], is_)
+    ref = O.rmsnorm(x, "mul", w=synth.norm_weight(5101, K), eps=1e-6)
+    assert np.all(np.abs(yb - ref) <= _y_tolerance(ref, None))
