@@ -412,6 +412,9 @@ QK_API qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t row
  * input is each pair's own GLU output; llama.cpp PR #117, "GLU producer
  * evidence" table, the per-slot routed components "K8192 / 32 slots / T8" and
  * "K2560 / 128 slots / T8"). img has rows * k rows.
+ * In a routed FFN the per-pair image comes from qk_glu_q8_1 over the rows * k
+ * gate/up output rows; passing offsets + E (the plan's count of planned pairs,
+ * live * k) as that call's d_live_rows leaves the padding pairs untouched.
  * Errors: as qk_mmvq_id.
  */
 QK_API qk_status qk_mmvq_id_slots(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k,
