@@ -136,3 +136,17 @@ def test_grid_limits_are_refused(lib):
     assert lib.qk_quantize_q8_1(P(X), 1, (1 << 25) + 32, (1 << 25) + 32, P(IMG), 1 << 20, None, None) == 1
     assert lib.qk_glu_q8_1(0, 0, P(X), 1 << 26, P(W), 1 << 26, 1, 1 << 26, P(Y), 1 << 26, P(IMG), 1 << 21,
                            None, None) == 1
+
+
+def test_glu_parameter_checks(lib):
+    """qk_glu_q8_1_ex refuses a non-finite alpha and a limit that is not positive and finite,
+    and unknown kinds (host checks only: no launch)."""
+    P = C.c_void_p
+    inf, nan = float("inf"), float("nan")
+    args = (P(X), 64, P(W), 64, 2, 64, P(Y), 64, P(IMG), 2)
+    assert lib.qk_glu_q8_1_ex(5, 0, *args, 1.702, 0.0, None, None) == 1
+    assert lib.qk_glu_q8_1_ex(5, 0, *args, 1.702, -1.0, None, None) == 1
+    assert lib.qk_glu_q8_1_ex(5, 0, *args, 1.702, inf, None, None) == 1
+    assert lib.qk_glu_q8_1_ex(5, 0, *args, nan, 7.0, None, None) == 1
+    assert lib.qk_glu_q8_1_ex(6, 0, *args, 1.702, 7.0, None, None) == 1
+    assert lib.qk_glu_q8_1(6, 0, *args, None, None) == 1
