@@ -23,6 +23,7 @@ duration with the case's algorithmic bytes (or flops) per launch. Cases:
                 128, plan, mmvq_id gate+up (kernels rmsnorm_q8_1, topk, plan, mmvq_id)
   mmq_qkv       qk_mmq, 3325 tokens, q/k/v          (kernels dequant_b, mmq_tc)
   quantize_q8_0 qk_quantize_q8_0, [3325, 3584]      (kernel quantize)
+  rmsnorm_q8_0  qk_rmsnorm_q8_0, [3325, 3584] x w -> F32 + Q8_0 planes (kernel rmsnorm_q8_1)
 """
 from __future__ import annotations
 
@@ -193,6 +194,15 @@ def build_case(name):
         keep = ws + ys + [x, w, y, img, logits, ids, wts, counts, offsets, items, lv]
         nbytes = 2 * live_e * per + 2 * bucket * k * NF * 4 + bucket * (K // 32) * Q8_1_BLOCK
         return chain, keep, {"bytes": nbytes, "live_experts": live_e}
+    if name == "rmsnorm_q8_0":
+        T, K, rb = 3325, 3584, 112
+        x, w = _dev(synth.activations(4, T, K)), _dev(synth.norm_weight(2, K))
+        y = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        qs = torch.empty((T * rb * 32,), dtype=torch.int8, device="cuda")
+        d = torch.empty((T * rb,), dtype=torch.int16, device="cuda")
+        nbytes = 2 * T * K * 4 + K * 4 + T * K + T * rb * 2
+        return (lambda: qk.qk_rmsnorm_q8_0(x, T, K, K, "mul", w, None, 1.0, 1e-6, y, K, qs, d, rb),
+                [x, w, y, qs, d], {"bytes": nbytes})
     if name in ("mmq_qkv", "quantize_q8_0"):
         T, K = 3325, 3584
         x = _dev(synth.activations(4, T, K))
