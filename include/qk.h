@@ -87,8 +87,11 @@ typedef enum qk_glu_kind {
     QK_GLU_REGLU = 2,      /* out = max(g, 0) * u */
     QK_GLU_GEGLU_ERF = 3,  /* out = 0.5 g (1 + erf(g / sqrt 2)) * u   (exact GELU) */
     QK_GLU_GEGLU_QUICK = 4,/* out = g * sigmoid(1.702 g) * u          (sigmoid GELU) */
-    QK_GLU_SWIGLU_OAI = 5  /* x = min(g, limit), v = clamp(u, -limit, limit):
+    QK_GLU_SWIGLU_OAI = 5, /* x = min(g, limit), v = clamp(u, -limit, limit):
                               out = x * sigmoid(alpha x) * (v + 1)     */
+    QK_GLU_SWIGLU_CLAMP = 6/* x = min(g, limit), v = clamp(u, -limit, limit):
+                              out = x * sigmoid(x) * v  (a reading: the
+                              pages give no formula)                   */
 } qk_glu_kind;
 
 typedef enum qk_glu_layout {
@@ -216,9 +219,9 @@ QK_API qk_status qk_rmsnorm_q8_0(const float *x, int64_t T, int64_t K, int64_t x
 
 /*
  * qk_glu_q8_1 -- GLU producer that emits the image (llama.cpp PR #117,
- * Coverage: F32 ReGLU, GeGLU, SwiGLU, GeGLU-erf, GeGLU-quick and SwiGLU-OAI
- * with separate, packed and packed-swapped inputs and independent source row
- * strides; output width whole Q8_1 blocks). SwiGLU-clamp is not provided.
+ * Coverage: F32 ReGLU, GeGLU, SwiGLU, GeGLU-erf, GeGLU-quick, SwiGLU-OAI and
+ * SwiGLU-clamp with separate, packed and packed-swapped inputs and independent
+ * source row strides; output width whole Q8_1 blocks).
  *   out [T][out_stride] F32 = act(g) * u for live rows, columns 0..N-1
  *   img the Q8_1 image of exactly the stored out values
  *   SEPARATE: g = a + t*a_stride, u = b + t*b_stride
@@ -235,8 +238,8 @@ QK_API qk_status qk_glu_q8_1(qk_glu_kind kind, qk_glu_layout layout,
 /*
  * qk_glu_q8_1_ex -- qk_glu_q8_1 with the SwiGLU-OAI parameters (llama.cpp PR
  * #117, Coverage: the GLU producers keep their alpha/limit parameters).
- * alpha and limit are read by QK_GLU_SWIGLU_OAI only; qk_glu_q8_1 passes
- * alpha = 1.702, limit = 7.0. Errors: as qk_glu_q8_1, and QK_ERR_ARG for a
+ * alpha is read by QK_GLU_SWIGLU_OAI, limit by it and QK_GLU_SWIGLU_CLAMP;
+ * qk_glu_q8_1 passes alpha = 1.702, limit = 7.0. Errors: as qk_glu_q8_1, and QK_ERR_ARG for a
  * non-finite alpha or a limit that is not a positive finite number.
  */
 QK_API qk_status qk_glu_q8_1_ex(qk_glu_kind kind, qk_glu_layout layout,

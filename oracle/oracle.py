@@ -29,7 +29,8 @@ _lib = None
 Q8_1_BYTES = 36
 WTYPE = {"q4_0": 0, "q8_0": 1}
 NORM_KIND = {"plain": 0, "mul": 1, "mul_add": 2, "scale": 3}
-GLU_KIND = {"swiglu": 0, "geglu_tanh": 1, "reglu": 2, "geglu_erf": 3, "geglu_quick": 4, "swiglu_oai": 5}
+GLU_KIND = {"swiglu": 0, "geglu_tanh": 1, "reglu": 2, "geglu_erf": 3, "geglu_quick": 4, "swiglu_oai": 5,
+            "swiglu_clamp": 6}
 GLU_LAYOUT = {"separate": 0, "packed": 1, "packed_swapped": 2}
 
 

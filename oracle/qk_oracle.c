@@ -294,9 +294,11 @@ void or_rmsnorm(const float *x, int64_t T, int64_t K, int64_t x_stride, int kind
 /*                approximation)                                             */
 /*   SwiGLU-OAI:  x = min(g, limit), v = clamp(u, -limit, limit),            */
 /*                out = x * sigmoid(alpha x) * (v + 1)  (gpt-oss MLP)        */
+/*   SwiGLU-clamp: the same clamps on SwiGLU, out = x * sigmoid(x) * v (a    */
+/*                reading: no formula is published with the name)           */
 /* kind: 0 swiglu, 1 geglu-tanh, 2 reglu, 3 geglu-erf, 4 geglu-quick,         */
-/* 5 swiglu-oai. layout: 0 separate (g at a, u at b), 1 packed row [g | u]   */
-/* at a, 2 packed-swapped row [u | g] at a.                                  */
+/* 5 swiglu-oai, 6 swiglu-clamp. layout: 0 separate (g at a, u at b),        */
+/* 1 packed row [g | u] at a, 2 packed-swapped row [u | g] at a.             */
 /* ------------------------------------------------------------------------ */
 static double glu_value(int kind, double g, double u, double alpha, double limit)
 {
@@ -315,6 +317,11 @@ static double glu_value(int kind, double g, double u, double alpha, double limit
         double x = g < limit ? g : limit;
         double v = u < -limit ? -limit : (u > limit ? limit : u);
         return x / (1.0 + exp(-alpha * x)) * (v + 1.0);
+    }
+    case 6: {
+        double x = g < limit ? g : limit;
+        double v = u < -limit ? -limit : (u > limit ? limit : u);
+        return x / (1.0 + exp(-x)) * v;
     }
     default:
         return (g > 0.0 ? g : 0.0) * u;

@@ -21,7 +21,8 @@ QK_OK = 0
 STATUS = {0: "QK_OK", 1: "QK_ERR_ARG", 2: "QK_ERR_SHAPE", 3: "QK_ERR_ALIAS", 4: "QK_ERR_WORKSPACE",
           5: "QK_ERR_UNSUPPORTED", 6: "QK_ERR_CUDA"}
 NORM = {"plain": 0, "mul": 1, "mul_add": 2, "scale": 3}
-GLU = {"swiglu": 0, "geglu_tanh": 1, "reglu": 2, "geglu_erf": 3, "geglu_quick": 4, "swiglu_oai": 5}
+GLU = {"swiglu": 0, "geglu_tanh": 1, "reglu": 2, "geglu_erf": 3, "geglu_quick": 4, "swiglu_oai": 5,
+       "swiglu_clamp": 6}
 LAYOUT = {"separate": 0, "packed": 1, "packed_swapped": 2}
 WTYPE = {"q4_0": 0, "q8_0": 1}
 Q8_1_BLOCK_BYTES = 36

@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(NT, NT == RMS_THREADS ? 1 : 4) rmsnorm_q8_1_ke
 }
 
 // ---------------------------------------------------------------- GLU producer
-// act(g) * u for the GLU kinds; SwiGLU-OAI clamps g from above and u both ways at limit
-// and multiplies by (u + 1).
+// act(g) * u for the GLU kinds; SwiGLU-OAI and SwiGLU-clamp clamp g from above and u both
+// ways at limit (SwiGLU-OAI also scales the gate by alpha and multiplies by u + 1).
 __device__ __forceinline__ float glu_out(int kind, float g, float u, float alpha, float limit) {
     switch (kind) {
         case QK_GLU_SWIGLU: return g / (1.0f + expf(-g)) * u;
@@ -259,6 +259,10 @@ __device__ __forceinline__ float glu_out(int kind, float g, float u, float alpha
         case QK_GLU_SWIGLU_OAI: {
             const float x = fminf(g, limit), v = fminf(fmaxf(u, -limit), limit);
             return x / (1.0f + expf(-alpha * x)) * (v + 1.0f);
+        }
+        case QK_GLU_SWIGLU_CLAMP: {
+            const float x = fminf(g, limit), v = fminf(fmaxf(u, -limit), limit);
+            return x / (1.0f + expf(-x)) * v;
         }
         default: return fmaxf(g, 0.0f) * u;
     }

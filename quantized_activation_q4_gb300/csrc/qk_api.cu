@@ -179,7 +179,7 @@ qk_status qk_glu_q8_1_ex(qk_glu_kind kind, qk_glu_layout layout, const float *a,
                          const float *b, int64_t b_stride, int64_t T, int64_t N, float *out,
                          int64_t out_stride, void *img, int64_t img_row_blocks, float alpha, float limit,
                          const int32_t *d_live_rows, qk_stream stream) {
-    REQUIRE(kind >= QK_GLU_SWIGLU && kind <= QK_GLU_SWIGLU_OAI, QK_ERR_ARG, "bad glu kind %d", (int)kind);
+    REQUIRE(kind >= QK_GLU_SWIGLU && kind <= QK_GLU_SWIGLU_CLAMP, QK_ERR_ARG, "bad glu kind %d", (int)kind);
     REQUIRE(std::isfinite(alpha) && std::isfinite(limit) && limit > 0.0f, QK_ERR_ARG,
             "alpha must be finite and limit positive and finite");
     REQUIRE(layout >= QK_GLU_SEPARATE && layout <= QK_GLU_PACKED_SWAPPED, QK_ERR_ARG, "bad glu layout %d", (int)layout);

@@ -148,5 +148,6 @@ def test_glu_parameter_checks(lib):
     assert lib.qk_glu_q8_1_ex(5, 0, *args, 1.702, -1.0, None, None) == 1
     assert lib.qk_glu_q8_1_ex(5, 0, *args, 1.702, inf, None, None) == 1
     assert lib.qk_glu_q8_1_ex(5, 0, *args, nan, 7.0, None, None) == 1
-    assert lib.qk_glu_q8_1_ex(6, 0, *args, 1.702, 7.0, None, None) == 1
-    assert lib.qk_glu_q8_1(6, 0, *args, None, None) == 1
+    assert lib.qk_glu_q8_1_ex(7, 0, *args, 1.702, 7.0, None, None) == 1
+    assert lib.qk_glu_q8_1(7, 0, *args, None, None) == 1
+    assert lib.qk_glu_q8_1_ex(6, 0, *args, 1.702, -1.0, None, None) == 1    # SwiGLU-clamp reads limit too

@@ -135,7 +135,8 @@ def test_rmsnorm_q8_1(kind, T, K, live):
     assert np.all(blocks_equal[same_y])
 
 
-@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu", "geglu_erf", "geglu_quick", "swiglu_oai"])
+@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu", "geglu_erf", "geglu_quick", "swiglu_oai",
+                                  "swiglu_clamp"])
 @pytest.mark.parametrize("layout", ["separate", "packed", "packed_swapped"])
 @pytest.mark.parametrize("T,N", [(8, 18944), (3, 96)])
 def test_glu_q8_1(kind, layout, T, N):

@@ -244,7 +244,26 @@ def test_glu_swiglu_oai_reductions_and_clamps():
                               O.glu("swiglu_oai", "separate", np.full_like(g, -7.0), u, N))
 
 
-@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu", "geglu_erf", "geglu_quick", "swiglu_oai"])
+def test_glu_swiglu_clamp_reductions_and_clamps():
+    """SwiGLU-clamp (a reading: SwiGLU with SwiGLU-OAI's clamps): inside the limits it is SwiGLU;
+    past them it is constant in g (from above) and in u (both ways); below -limit g is not clamped."""
+    T, N = 2, 256
+    g = np.clip(synth.activations(37, T, N) * np.float32(2.0), -6.5, 6.5).astype(np.float32)
+    u = np.clip(synth.activations(38, T, N) * np.float32(2.0), -6.5, 6.5).astype(np.float32)
+    assert np.array_equal(O.glu("swiglu_clamp", "separate", g, u, N), O.glu("swiglu", "separate", g, u, N))
+    lim = np.full_like(g, 7.0)
+    assert np.array_equal(O.glu("swiglu_clamp", "separate", lim + np.abs(g), u, N),
+                          O.glu("swiglu_clamp", "separate", lim, u, N))
+    for sgn in (1.0, -1.0):
+        far = np.float32(sgn) * (np.float32(7.0) + np.abs(u))
+        assert np.array_equal(O.glu("swiglu_clamp", "separate", g, far, N),
+                              O.glu("swiglu_clamp", "separate", g, np.float32(sgn) * lim, N))
+    low = np.full_like(g, -9.0)
+    assert np.array_equal(O.glu("swiglu_clamp", "separate", low, u, N), O.glu("swiglu", "separate", low, u, N))
+
+
+@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu", "geglu_erf", "geglu_quick", "swiglu_oai",
+                                  "swiglu_clamp"])
 def test_glu_layouts(kind):
     T, N = 4, 96
     g = synth.activations(41, T, N)
