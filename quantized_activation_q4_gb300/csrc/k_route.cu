@@ -1,7 +1,7 @@
-// Router top-k and the stable expert plan, both live-row aware
-// (TensorFold PR #1047 "padding rows no longer go through routed experts",
-// "The fix": router, top-k and plan read the live-row count on the device and
-// skip rows from it up; launches stay sized for the bucket).
+// Router top-k, the stable expert plan and the weighted combine, all live-row
+// aware (TensorFold PR #1047 "padding rows no longer go through routed experts",
+// "The fix": router, top-k, plan and combine read the live-row count on the
+// device and skip rows from it up; launches stay sized for the bucket).
 
 #include "qk_internal.cuh"
 
@@ -218,10 +218,10 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(const float *__restric
     plan_body(ids, n_live * k, E, counts, offsets, items, sm, wsum);
 }
 
-
 // ---------------------------------------------------------------- combine
 // y[r][n] = sum over slots s (ascending) of wts[r][s] * expert_out[r*k + s][n], one binary32 fma
-// per slot, for live rows r. Grid (ceil(N/1024), rows); thread i handles columns 4i..4i+3.
+// per slot, for live rows r. Grid (rows, ceil(N/1024)); thread i of CTA (r, cy) handles columns
+// 1024*cy + 4i .. +3 of row r.
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ eo, int64_t eo_stride,
                                                       const float *__restrict__ wts, int rows, int k, int N,
                                                       float *__restrict__ y, int64_t y_stride, const int32_t *live) {
