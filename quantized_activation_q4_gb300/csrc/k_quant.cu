@@ -268,7 +268,7 @@ __device__ __forceinline__ float glu_out(int kind, float g, float u, float alpha
     }
 }
 
-// grid (ceil(N/1024), T), 256 threads; thread i handles columns 1024*bx + 4i.
+// grid (T, ceil(N/1024)), 256 threads; thread i of CTA (t, cy) handles columns 1024*cy + 4i of row t.
 __global__ void __launch_bounds__(256) glu_q8_1_kernel(
     int kind, int layout, const float *__restrict__ a, int64_t a_stride, const float *__restrict__ b,
     int64_t b_stride, int N, float *__restrict__ out, int64_t out_stride, uint8_t *__restrict__ img,
