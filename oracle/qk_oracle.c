@@ -508,8 +508,10 @@ void or_topk_route(const float *logits, int64_t rows, int E, int k,
 /* Stable grouped plan of the live pairs ([P3] "The fix": counts and ranks,  */
 /* exclusive-scan offsets, scatter; only the first live*k pairs). Pair p =   */
 /* row*k + slot names expert ids[p]. counts[e] = pairs for e; offsets is the */
-/* exclusive scan (offsets[E] = live*k); items lists the pairs of expert 0,  */
-/* then 1, ..., each group in ascending p.                                   */
+/* exclusive scan; items lists the pairs of expert 0, then 1, ..., each      */
+/* group in ascending p. A pair whose id lies outside [0, E) names no expert */
+/* and is left out (reading of the pages: such a pair has no expert work),   */
+/* so offsets[E] = the number of live pairs with a valid id.                 */
 /* ------------------------------------------------------------------------ */
 void or_moe_plan(const int32_t *ids, int64_t rows, int k, int E,
                  int32_t *counts, int32_t *offsets, int32_t *items, const int32_t *live)
@@ -518,7 +520,8 @@ void or_moe_plan(const int32_t *ids, int64_t rows, int k, int E,
     for (int e = 0; e < E; e++)
         counts[e] = 0;
     for (int64_t p = 0; p < npairs; p++)
-        counts[ids[p]]++;
+        if (ids[p] >= 0 && ids[p] < E)
+            counts[ids[p]]++;
     offsets[0] = 0;
     for (int e = 0; e < E; e++)
         offsets[e + 1] = offsets[e] + counts[e];
@@ -526,7 +529,8 @@ void or_moe_plan(const int32_t *ids, int64_t rows, int k, int E,
     for (int e = 0; e < E; e++)
         fill[e] = offsets[e];
     for (int64_t p = 0; p < npairs; p++)
-        items[fill[ids[p]]++] = (int32_t)p;
+        if (ids[p] >= 0 && ids[p] < E)
+            items[fill[ids[p]]++] = (int32_t)p;
     free(fill);
 }
 

@@ -55,6 +55,28 @@ def test_plan_matches_oracle(rows, live, k):
     assert gc.sum() == live * k and (ri.size == 0 or ri.max() < live * k)
 
 
+@pytest.mark.parametrize("rows,live,k", [(16, 9, 8), (128, 113, 9), (128, 128, 8)])
+def test_plan_leaves_out_invalid_ids_like_the_oracle(rows, live, k):
+    """Pairs whose id is outside [0, E) (-1, E, E + 5, INT32_MAX) get no count and no
+    item on the GPU, exactly as in the oracle; the valid pairs keep their stable order."""
+    import torch
+    g = synth.rng(6200 + rows + live + k)
+    ids_h = g.integers(0, E, size=(rows, k), dtype=np.int32)
+    bad = g.random(size=ids_h.shape) < 0.25
+    ids_h[bad] = g.choice(np.array([-1, E, E + 5, 2**31 - 1], dtype=np.int64), size=int(bad.sum())).astype(np.int32)
+    counts = torch.full((E,), -7, dtype=torch.int32, device="cuda")
+    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    items = torch.full((rows * k,), -7, dtype=torch.int32, device="cuda")
+    qk.qk_moe_plan(dev(ids_h), rows, k, E, counts, offsets, items, live_ptr(live))
+    rc, ro, ri = O.moe_plan(ids_h, E, live=live)
+    n_valid = int(((ids_h.ravel()[:live * k] >= 0) & (ids_h.ravel()[:live * k] < E)).sum())
+    assert ro[E] == n_valid < live * k
+    gc, go, gi = host(counts), host(offsets), host(items)
+    assert np.array_equal(gc, rc) and np.array_equal(go, ro)
+    assert np.array_equal(gi[:n_valid], ri)
+    assert np.all(gi[n_valid:] == -7)                      # positions past the planned pairs untouched
+
+
 def _experts(seed, n, N, K):
     return [synth.q4_0_weight(seed + e, N, K) for e in range(n)]
 

@@ -193,6 +193,25 @@ def test_glu_against_library_functions():
     assert np.allclose(gt - gm, g64, rtol=1e-13, atol=1e-13)
 
 
+def test_geglu_tanh_against_torch_tanh_gelu():
+    """GeGLU-tanh against torch's tanh-approximated GELU in float64 (a library routine
+    with the published constants sqrt(2/pi) and 0.044715): a truncated constant
+    (0.0447, 0.7978) moves the result by more than 1e-6 at |g| ~ 2..3, far past 1e-13."""
+    import torch
+    T, N = 4, 1024
+    g = synth.activations(33, T, N) * np.float32(3.0)
+    u = synth.activations(34, T, N)
+    g64 = torch.from_numpy(g.astype(np.float64))
+    ref = (torch.nn.functional.gelu(g64, approximate="tanh") * torch.from_numpy(u.astype(np.float64))).numpy()
+    got = O.glu("geglu_tanh", "separate", g, u, N)
+    assert np.max(np.abs(got - ref)) <= 1e-13 * max(1.0, float(np.max(np.abs(ref))))
+    # the same through the packed layouts (the half order of the two layouts)
+    gu = np.concatenate([g, u], axis=1)
+    ug = np.concatenate([u, g], axis=1)
+    assert np.array_equal(O.glu("geglu_tanh", "packed", gu, None, N), got)
+    assert np.array_equal(O.glu("geglu_tanh", "packed_swapped", ug, None, N), got)
+
+
 def test_glu_gelu_variants_against_library_and_identities():
     """GeGLU-erf against torch's exact GELU; GeGLU-quick within the sigmoid approximation's
     known distance of it (a wrong constant, e.g. SiLU's 1.0, misses by > 0.1); both odd parts
@@ -406,6 +425,24 @@ def test_plan_matches_stable_sort(rows, live, k):
     assert offsets[0] == 0 and offsets[E] == npairs and np.all(np.diff(offsets) == counts)
     assert np.array_equal(items, np.array(sorted(range(npairs), key=lambda p: flat[p]), dtype=np.int32))
     assert items.size == 0 or items.max() < npairs
+
+
+@pytest.mark.parametrize("rows,live,k", [(16, 9, 8), (128, 113, 9), (4, 4, 2)])
+def test_plan_leaves_out_pairs_with_invalid_ids(rows, live, k):
+    """A pair whose id lies outside [0, E) names no expert: it gets no count and
+    no item, and the plan of the rest equals the stable sort of the valid pairs."""
+    E = 128
+    g = synth.rng(140 + rows + live)
+    ids = g.integers(0, E, size=(rows, k), dtype=np.int32)
+    bad = g.random(size=ids.shape) < 0.2
+    ids[bad] = g.choice(np.array([-1, -7, E, E + 5, 2**31 - 1], dtype=np.int64), size=int(bad.sum())).astype(np.int32)
+    counts, offsets, items = O.moe_plan(ids, E, live=live)
+    flat = ids.ravel()[:live * k]
+    valid = [p for p in range(live * k) if 0 <= flat[p] < E]
+    assert len(valid) < live * k   # the case really has invalid ids in the live range
+    assert np.array_equal(counts, np.bincount(flat[valid], minlength=E))
+    assert offsets[0] == 0 and offsets[E] == len(valid) and np.all(np.diff(offsets) == counts)
+    assert np.array_equal(items, np.array(sorted(valid, key=lambda p: flat[p]), dtype=np.int32))
 
 
 def test_routed_projection_rows():
