@@ -259,7 +259,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     torch.cuda.synchronize()
 
     K = args.steps
-    KC = max(3, K // R)                    # replays of each component graph (R components each)
+    KC = max(-(-200 // R), K // R)         # replays of each component graph (R components each): >= 200 launches
     ev = lambda: torch.cuda.Event(enable_timing=True)
     e_s0, e_s1 = ev(), ev()
     e_c = {name: (ev(), ev()) for name in comp_graphs}
@@ -288,6 +288,22 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
     faults = qk.qk_device_faults()
     if faults:
         raise RuntimeError(f"device fault word {faults:#x} after the timed region")
+    # The dominant kernel alone: each launch right behind a 512 MB write that flushes the L2 (the
+    # write also keeps the device busy while the host enqueues the events and the launch), timed
+    # with CUDA events on its stream, so it starts cold and overlaps no neighbour; median of 30.
+    flush = torch.empty((512 << 20,), dtype=torch.uint8, device="cuda")
+    iso = []
+    for i in range(30):
+        e_i0, e_i1 = ev(), ev()
+        with torch.cuda.stream(stream):
+            flush.fill_(i & 0xFF)
+            e_i0.record(stream)
+            comp_m(i % R)
+            e_i1.record(stream)
+        torch.cuda.synchronize()
+        iso.append(e_i0.elapsed_time(e_i1) * 1e3)
+    iso_us = float(np.median(iso))
+    del flush
     ms_per_step = e_s0.elapsed_time(e_s1) / K
     comp_us = {name: e_c[name][0].elapsed_time(e_c[name][1]) * 1e3 / (KC * R) for name in comp_graphs}
     ms_per_step = max_over_ranks(ms_per_step, world, "cuda")
@@ -396,7 +412,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         "mmvq_8192x8192": {"us": round(us_m, 3), "weight_bytes": W_BIG,
                            "weight_gbs": round(W_BIG / (us_m * 1e-6) / 1e9, 1),
                            "hbm_frac_weights": round(W_BIG / (us_m * 1e-6) / 1e9 / hbm, 4)},
-        "timing": f"each component graph holds {R} back-to-back replicas (rotating weights), replayed {KC} times",
+        "timing": f"each component graph holds {R} back-to-back replicas (rotating weights), replayed {KC} times "
+                  f"({KC * R} launches per component)",
     }
     return {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -415,10 +432,17 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         "other_configs": others,
         "roofline": {"kernel": "mmvq (Q4_0, K=N=8192, T=8)", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "launch_us_back_to_back": round(us_m, 3),
+                     "launch_us_isolated": round(iso_us, 3),
+                     "frac_isolated": round(MMVQ_BIG_BYTES / (iso_us * 1e-6) / 1e9 / hbm, 4),
+                     "timing": (f"achieved/frac: mean launch time of {KC * R} back-to-back launches in graphs of {R} "
+                                "rotating replicas (programmatic dependent launch overlaps a launch's start with the "
+                                "previous one's tail); isolated: median of 30 single launches, each right behind an "
+                                "L2-flushing 512 MB write"),
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, copy burst)",
                      "algorithmic_bytes_per_launch": MMVQ_BIG_BYTES, "traffic": recorded_traffic(),
-                     "traffic_source": "profiles/mmvq_q4_0_8192x8192_t8.md (ncu, one launch; null if the "
-                                       "kernel sources changed since)"},
+                     "traffic_source": "ncu DRAM read + write bytes of one launch, from the committed capture "
+                                       "record (null once the kernel sources have changed since)"},
         "e2e": {"value": round(job_gbs(world, W_STEP, e2e_ms), 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "outputs_match_device_path": e2e_match,
@@ -751,7 +775,365 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
                 "memory; kind::i8 is not available on sm_103a); its fraction is against the measured cuBLAS "
                 "bf16 dense peak (f16 and bf16 share the dense rate)",
         "replicas": R4}
+    del layers
+    out["c4_prefill_28"] = prefill_28(qk, torch, stream, peak_t)
     return out
+
+
+def prefill_28(qk, torch, stream, peak_t) -> dict:
+    """Config 4 as a whole prefill: 28 layers of 3325 tokens x d = 3584, each with its own weights
+    and activations drawn from a seeded generator (seed 4000 + layer): q/k/v (3584 -> 3584, 512,
+    512) on one Q8_0 image of the attention input and gate/up (3584 -> 18944) on one image of the
+    FFN input. Timed as one CUDA graph per variant:
+      dedup:    one standalone Q8_0 quantize per distinct activation (2 per layer)
+      per_gemm: one quantize per GEMM (5 per layer: the image is recomputed for k, v and up)
+      fused:    the RMSNorm*w producers emit the Q8_0 planes (no standalone quantize)
+      unfused:  RMSNorm*w writes F32, then the standalone quantize re-reads it (2 per layer)
+    and a launch ledger (library launches and standalone quantize launches per variant).
+    Inputs come from torch's seeded CUDA generator, with the configuration's distributions: N(0,1)
+    activations, uniform Q4_0 nibbles and half scales U[0.002, 0.02]."""
+    L, TP, DP, NFF = 28, 3325, 3584, 18944
+    rb = DP // 32
+    shapes = (3584, 512, 512, NFF, NFF)
+
+    def gen(layer):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(4000 + layer)
+        xa = torch.randn((TP, DP), generator=g, device="cuda", dtype=torch.float32)
+        xb = torch.randn((TP, DP), generator=g, device="cuda", dtype=torch.float32)
+        ws = []
+        for n in shapes:
+            nblk = n * rb
+            blocks = torch.randint(0, 256, (nblk, 18), generator=g, device="cuda", dtype=torch.uint8)
+            d = (0.002 + 0.018 * torch.rand((nblk,), generator=g, device="cuda")).to(torch.float16)
+            blocks[:, :2] = d.view(torch.uint8).view(nblk, 2)
+            nbytes = qk.qk_weight_packed_bytes("q4_0", n, DP)
+            buf = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
+            qk.qk_weight_pack("q4_0", blocks.reshape(-1), n, DP, buf, nbytes)
+            ws.append(buf)
+        return xa, xb, ws
+
+    layers = [gen(layer) for layer in range(L)]
+    wn = torch.ones((DP,), dtype=torch.float32, device="cuda")
+    ys = [torch.empty((TP, n), dtype=torch.float32, device="cuda") for n in shapes]
+    ya = torch.empty((TP, DP), dtype=torch.float32, device="cuda")
+    scratch = torch.empty((TP * rb * 36,), dtype=torch.uint8, device="cuda")
+    qs = torch.empty((TP * rb * 32,), dtype=torch.int8, device="cuda")
+    dh = torch.empty((TP * rb,), dtype=torch.int16, device="cuda")
+    mk = lambda ws, idx: [qk.make_proj("q4_0", ws[i], shapes[i], DP, ys[i], shapes[i]) for i in idx]
+    wsn = qk.qk_mmq_workspace_bytes(TP, mk(layers[0][2], (0,)))
+    wsb = torch.empty((wsn,), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    quant_calls = [0]
+
+    def quant(x):
+        quant_calls[0] += 1
+        qk.qk_quantize_q8_0(x, TP, DP, DP, qs, dh, rb)
+
+    def mmq(idx, ws):
+        qk.qk_mmq(qs, dh, rb, TP, mk(ws, idx), wsb, wsn)
+
+    def rms_q8_0(x):
+        qk.qk_rmsnorm_q8_0(x, TP, DP, DP, "mul", wn, None, 1.0, 1e-6, ya, DP, qs, dh, rb)
+
+    def rms_f32(x):
+        qk.qk_rmsnorm_q8_1(x, TP, DP, DP, "mul", wn, None, 1.0, 1e-6, ya, DP, scratch, rb)
+
+    variants = {
+        "dedup": lambda xa, xb, ws: (quant(xa), mmq((0, 1, 2), ws), quant(xb), mmq((3, 4), ws)),
+        "per_gemm": lambda xa, xb, ws: [(quant(xa if i < 3 else xb), mmq((i,), ws)) for i in range(5)],
+        "fused": lambda xa, xb, ws: (rms_q8_0(xa), mmq((0, 1, 2), ws), rms_q8_0(xb), mmq((3, 4), ws)),
+        "unfused": lambda xa, xb, ws: (rms_f32(xa), quant(ya), mmq((0, 1, 2), ws), rms_f32(xb), quant(ya),
+                                       mmq((3, 4), ws)),
+    }
+    res = {}
+    ops = 2 * TP * DP * sum(shapes) * L
+    for name, fn in variants.items():
+        with torch.cuda.stream(stream):
+            for xa, xb, ws in layers:   # eager warm-up
+                fn(xa, xb, ws)
+        torch.cuda.synchronize()
+        quant_calls[0] = 0
+        n0 = qk.launch_count()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for xa, xb, ws in layers:
+                fn(xa, xb, ws)
+        launches, quants = qk.launch_count() - n0, quant_calls[0]
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms": round(ms, 3), "tokens_per_s": round(TP / (ms * 1e-3), 1),
+                     "library_launches": launches, "standalone_quantize_launches": quants,
+                     "tflops": round(ops / (ms * 1e-3) / 1e12, 1)}
+        del g
+    res["dedup"]["quantize_ratio_vs_per_gemm"] = round(res["dedup"]["standalone_quantize_launches"] /
+                                                       res["per_gemm"]["standalone_quantize_launches"], 3)
+    res["layers"], res["tokens"], res["ops"] = L, TP, ops
+    if peak_t:
+        res["dedup"]["frac_of_measured_bf16_dense_peak"] = round(ops / (res["dedup"]["ms"] * 1e-3) / 1e12 / peak_t, 4)
+    res["inputs"] = "torch CUDA generator, seed 4000 + layer per layer (fresh weights and activations each layer)"
+    del layers
+    torch.cuda.synchronize()
+    return res
+
+
+# ------------------------------------------------------------------ single-kernel cases
+# python bench.py --case NAME [--reps N] [--time N]
+#
+# Each case builds its seeded inputs, runs the case's kernel `reps` times
+# through the C ABI (the first launches warm up) and synchronises, so that an
+# ncu capture of the last launch (`-k regex:<kernel> -s <reps-1> -c 1`) sees
+# one steady-state launch. With `--time N` it then times N more launches, one
+# by one with CUDA events on the current stream, each after a 512 MB write that
+# flushes the 129 MB L2 (so weights come from HBM), and prints the median
+# duration with the case's algorithmic bytes (or flops) per launch. Cases:
+#
+#   mmvq_8192     qk_mmvq, Q4_0 8192x8192, T=8        (kernel mmvq_sk)
+#   mmvq_qkv      qk_mmvq, q/k/v 3584->3584/512/512   (kernel mmvq_sk)
+#   mmvq_down     qk_mmvq, Q4_0 18944->3584, T=8      (kernel mmvq_sk)
+#   rmsnorm       qk_rmsnorm_q8_1, [8, 3584] x w      (kernel rmsnorm_q8_1)
+#   quantize      qk_quantize_q8_1, [8, 8192]         (kernel quantize)
+#   glu           qk_glu_q8_1 SwiGLU packed [8, 18944] (kernel glu_q8_1)
+#   mmvq_id_<R>   qk_mmvq_id, gate+up 2560->768 over 128 experts, top-8 of R rows (kernel mmvq_id)
+#   mmvq_id_slots_<R>  qk_mmvq_id_slots, per-slot down 768->2560 over 128 experts, top-8 of R rows
+#                 (one image row per pair; kernel mmvq_id)
+#   routed_<R>    the routed chain for R live rows of a 16/128 bucket: RMSNorm*w -> image, top-8 of
+#                 128, plan, mmvq_id gate+up (kernels rmsnorm_q8_1, topk, plan, mmvq_id)
+#   mmq_qkv       qk_mmq, 3325 tokens, q/k/v          (kernels dequant_b, mmq_tc)
+#   quantize_q8_0 qk_quantize_q8_0, [3325, 3584]      (kernel quantize)
+#   rmsnorm_q8_0  qk_rmsnorm_q8_0, [3325, 3584] x w -> F32 + Q8_0 planes (kernel rmsnorm_q8_1)
+
+Q4_ROW_BYTES = 18          # one Q4_0 block of 32 weights
+Q8_1_BLOCK = 36
+
+
+def _case_dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _case_packed(seed, N, K):
+    import torch
+    from quantized_activation_q4_gb300 import binding as qk
+    from quantized_activation_q4_gb300 import synth
+    nb = qk.qk_weight_packed_bytes("q4_0", N, K)
+    w = torch.empty((nb,), dtype=torch.uint8, device="cuda")
+    qk.qk_weight_pack("q4_0", _case_dev(synth.q4_0_weight(seed, N, K).reshape(-1)), N, K, w, nb)
+    return w
+
+
+def _case_image(T, K, seed=2):
+    import torch
+    from quantized_activation_q4_gb300 import binding as qk
+    from quantized_activation_q4_gb300 import synth
+    img = torch.empty((T * (K // 32) * 36,), dtype=torch.uint8, device="cuda")
+    qk.qk_quantize_q8_1(_case_dev(synth.activations(seed, T, K)), T, K, K, img, K // 32)
+    return img
+
+
+def _case_mmvq(shapes, K, T=8):
+    import torch
+    from quantized_activation_q4_gb300 import binding as qk
+    keep, projs = [], []
+    nbytes = sum(N * (K // 32) * Q4_ROW_BYTES + T * N * 4 for N in shapes) + T * (K // 32) * Q8_1_BLOCK
+    for i, N in enumerate(shapes):
+        w = _case_packed(10 + i, N, K)
+        y = torch.empty((T, N), dtype=torch.float32, device="cuda")
+        keep += [w, y]
+        projs.append(qk.make_proj("q4_0", w, N, K, y, N))
+    img = _case_image(T, K)
+    n = qk.qk_mmvq_workspace_bytes(projs)
+    ws = torch.zeros((n,), dtype=torch.uint8, device="cuda")
+    keep += [img, ws]
+    return lambda: qk.qk_mmvq(img, K // 32, T, projs, ws, n), keep, {"bytes": nbytes}
+
+
+def build_case(name):
+    from quantized_activation_q4_gb300 import binding as qk
+    from quantized_activation_q4_gb300 import synth
+    import torch
+    if name == "mmvq_8192":
+        return _case_mmvq([8192], 8192)
+    if name == "mmvq_qkv":
+        return _case_mmvq([3584, 512, 512], 3584)
+    if name == "mmvq_down":
+        return _case_mmvq([3584], 18944)
+    if name == "rmsnorm":
+        T, K = 8, 3584
+        x, w = _case_dev(synth.activations(1, T, K)), _case_dev(synth.norm_weight(2, K))
+        y = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        img = torch.empty((T * K // 32 * 36,), dtype=torch.uint8, device="cuda")
+        nbytes = 2 * T * K * 4 + K * 4 + T * (K // 32) * Q8_1_BLOCK
+        return (lambda: qk.qk_rmsnorm_q8_1(x, T, K, K, "mul", w, None, 1.0, 1e-6, y, K, img, K // 32),
+                [x, w, y, img], {"bytes": nbytes})
+    if name == "quantize":
+        T, K = 8, 8192
+        x = _case_dev(synth.activations(1, T, K))
+        img = torch.empty((T * K // 32 * 36,), dtype=torch.uint8, device="cuda")
+        return (lambda: qk.qk_quantize_q8_1(x, T, K, K, img, K // 32), [x, img],
+                {"bytes": T * K * 4 + T * (K // 32) * Q8_1_BLOCK})
+    if name == "glu":
+        T, N = 8, 18944
+        a = _case_dev(np.concatenate([synth.activations(1, T, N), synth.activations(2, T, N)], axis=1))
+        out = torch.empty((T, N), dtype=torch.float32, device="cuda")
+        img = torch.empty((T * N // 32 * 36,), dtype=torch.uint8, device="cuda")
+        nbytes = 3 * T * N * 4 + T * (N // 32) * Q8_1_BLOCK
+        return (lambda: qk.qk_glu_q8_1("swiglu", "packed", a, 2 * N, None, 0, T, N, out, N, img, N // 32),
+                [a, out, img], {"bytes": nbytes})
+    if name.startswith("mmvq_id_slots_"):
+        # per-slot down projection of the 128-expert FFN: pair p reads image row p (768 columns)
+        E, k, K, N, rows = 128, 8, 768, 2560, int(name.rsplit("_", 1)[1])
+        per = qk.qk_weight_packed_bytes("q4_0", N, K)
+        wd = torch.empty((E * per,), dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            qk.qk_weight_pack("q4_0", _case_dev(synth.q4_0_weight(3000 + e, N, K).reshape(-1)), N, K,
+                              wd[e * per:(e + 1) * per], per)
+        img = _case_image(rows * k, K)
+        ids = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+        wts = torch.empty((rows, k), dtype=torch.float32, device="cuda")
+        qk.qk_topk_route(_case_dev(synth.router_logits(3, rows, E)), rows, E, k, ids, wts)
+        counts = torch.empty((E,), dtype=torch.int32, device="cuda")
+        offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+        items = torch.empty((rows * k,), dtype=torch.int32, device="cuda")
+        qk.qk_moe_plan(ids, rows, k, E, counts, offsets, items)
+        y = torch.empty((rows * k, N), dtype=torch.float32, device="cuda")
+        projs = [qk.make_proj_id("q4_0", E, wd, N, K, y)]
+        live = int((counts > 0).sum().item())
+        nbytes = live * per + rows * k * N * 4 + rows * k * (K // 32) * Q8_1_BLOCK
+        return (lambda: qk.qk_mmvq_id_slots(img, K // 32, rows, k, projs, counts, offsets, items),
+                [wd, img, ids, wts, counts, offsets, items, y], {"bytes": nbytes, "live_experts": live})
+    if name.startswith("mmvq_id_"):
+        E, k, K, NF, rows = 128, 8, 2560, 768, int(name.rsplit("_", 1)[1])
+        per = qk.qk_weight_packed_bytes("q4_0", NF, K)
+        ws = []
+        for p in range(2):
+            buf = torch.empty((E * per,), dtype=torch.uint8, device="cuda")
+            for e in range(E):
+                qk.qk_weight_pack("q4_0", _case_dev(synth.q4_0_weight(1000 * p + e, NF, K).reshape(-1)), NF, K,
+                                  buf[e * per:(e + 1) * per], per)
+            ws.append(buf)
+        img = _case_image(rows, K)
+        ids = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+        wts = torch.empty((rows, k), dtype=torch.float32, device="cuda")
+        qk.qk_topk_route(_case_dev(synth.router_logits(3, rows, E)), rows, E, k, ids, wts)
+        counts = torch.empty((E,), dtype=torch.int32, device="cuda")
+        offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+        items = torch.empty((rows * k,), dtype=torch.int32, device="cuda")
+        qk.qk_moe_plan(ids, rows, k, E, counts, offsets, items)
+        ys = [torch.empty((rows * k, NF), dtype=torch.float32, device="cuda") for _ in range(2)]
+        projs = [qk.make_proj_id("q4_0", E, ws[p], NF, K, ys[p]) for p in range(2)]
+        keep = ws + ys + [img, ids, wts, counts, offsets, items]
+        live = int((counts > 0).sum().item())
+        nbytes = 2 * live * NF * (K // 32) * Q4_ROW_BYTES + 2 * rows * k * NF * 4 + rows * (K // 32) * Q8_1_BLOCK
+        return (lambda: qk.qk_mmvq_id(img, K // 32, rows, k, projs, counts, offsets, items), keep,
+                {"bytes": nbytes, "live_experts": live})
+    if name.startswith("routed_"):
+        E, k, K, NF, live = 128, 8, 2560, 768, int(name.rsplit("_", 1)[1])
+        bucket = 16 if live <= 16 else 128
+        per = qk.qk_weight_packed_bytes("q4_0", NF, K)
+        ws = []
+        for p in range(2):
+            buf = torch.empty((E * per,), dtype=torch.uint8, device="cuda")
+            for e in range(E):
+                qk.qk_weight_pack("q4_0", _case_dev(synth.q4_0_weight(1000 * p + e, NF, K).reshape(-1)), NF, K,
+                                  buf[e * per:(e + 1) * per], per)
+            ws.append(buf)
+        x, w = _case_dev(synth.activations(5, bucket, K)), _case_dev(synth.norm_weight(6, K))
+        y = torch.empty((bucket, K), dtype=torch.float32, device="cuda")
+        img = torch.empty((bucket * (K // 32) * 36,), dtype=torch.uint8, device="cuda")
+        logits = _case_dev(synth.router_logits(3, bucket, E))
+        ids = torch.empty((bucket, k), dtype=torch.int32, device="cuda")
+        wts = torch.empty((bucket, k), dtype=torch.float32, device="cuda")
+        counts = torch.empty((E,), dtype=torch.int32, device="cuda")
+        offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+        items = torch.empty((bucket * k,), dtype=torch.int32, device="cuda")
+        lv = torch.tensor([live], dtype=torch.int32, device="cuda")
+        ys = [torch.empty((bucket * k, NF), dtype=torch.float32, device="cuda") for _ in range(2)]
+        projs = [qk.make_proj_id("q4_0", E, ws[p], NF, K, ys[p]) for p in range(2)]
+
+        def chain():
+            qk.qk_rmsnorm_q8_1(x, bucket, K, K, "mul", w, None, 1.0, 1e-6, y, K, img, K // 32, d_live_rows=lv)
+            qk.qk_topk_route(logits, bucket, E, k, ids, wts, d_live_rows=lv)
+            qk.qk_moe_plan(ids, bucket, k, E, counts, offsets, items, d_live_rows=lv)
+            qk.qk_mmvq_id(img, K // 32, bucket, k, projs, counts, offsets, items)
+
+        chain()
+        torch.cuda.synchronize()
+        live_e = int((counts > 0).sum().item())
+        keep = ws + ys + [x, w, y, img, logits, ids, wts, counts, offsets, items, lv]
+        nbytes = 2 * live_e * per + 2 * bucket * k * NF * 4 + bucket * (K // 32) * Q8_1_BLOCK
+        return chain, keep, {"bytes": nbytes, "live_experts": live_e}
+    if name == "rmsnorm_q8_0":
+        T, K, rb = 3325, 3584, 112
+        x, w = _case_dev(synth.activations(4, T, K)), _case_dev(synth.norm_weight(2, K))
+        y = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        qs = torch.empty((T * rb * 32,), dtype=torch.int8, device="cuda")
+        d = torch.empty((T * rb,), dtype=torch.int16, device="cuda")
+        nbytes = 2 * T * K * 4 + K * 4 + T * K + T * rb * 2
+        return (lambda: qk.qk_rmsnorm_q8_0(x, T, K, K, "mul", w, None, 1.0, 1e-6, y, K, qs, d, rb),
+                [x, w, y, qs, d], {"bytes": nbytes})
+    if name in ("mmq_qkv", "quantize_q8_0"):
+        T, K = 3325, 3584
+        x = _case_dev(synth.activations(4, T, K))
+        qs = torch.empty((T * 112 * 32,), dtype=torch.int8, device="cuda")
+        d = torch.empty((T * 112,), dtype=torch.int16, device="cuda")
+        quant = lambda: qk.qk_quantize_q8_0(x, T, K, K, qs, d, 112)
+        if name == "quantize_q8_0":
+            return quant, [x, qs, d], {"bytes": T * K * 4 + T * K + T * (K // 32) * 2}
+        quant()
+        keep, projs = [x, qs, d], []
+        for i, N in enumerate((3584, 512, 512)):
+            w = _case_packed(20 + i, N, K)
+            y = torch.empty((T, N), dtype=torch.float32, device="cuda")
+            keep += [w, y]
+            projs.append(qk.make_proj("q4_0", w, N, K, y, N))
+        n = qk.qk_mmq_workspace_bytes(T, projs)
+        ws = torch.empty((n,), dtype=torch.uint8, device="cuda")
+        keep.append(ws)
+        return lambda: qk.qk_mmq(qs, d, 112, T, projs, ws, n), keep, {"flops": 2 * T * K * (3584 + 512 + 512)}
+    raise SystemExit(f"unknown case {name!r}")
+
+
+def run_case(args):
+    """--case NAME: one named kernel case for profiling (see CASES)."""
+    import torch
+    from quantized_activation_q4_gb300 import binding as qk
+    qk.load(build_if_missing=True)
+    run, keep, info = build_case(args.case)
+    torch.cuda.synchronize()
+    for _ in range(args.reps):
+        run()
+    torch.cuda.synchronize()
+    faults = qk.qk_device_faults()
+    if faults:
+        raise SystemExit(f"device fault word {faults:#x}")
+    print(f"{args.case}: {args.reps} launches ok")
+    if args.time:
+        flush = torch.empty((512 << 20,), dtype=torch.uint8, device="cuda")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.time)]
+        for e0, e1 in ev:
+            flush.fill_(1)
+            e0.record()
+            run()
+            e1.record()
+        torch.cuda.synchronize()
+        us = float(np.median([e0.elapsed_time(e1) * 1e3 for e0, e1 in ev]))
+        line = {"case": args.case, "median_us": round(us, 3), "launches": args.time, **info}
+        if "bytes" in info:
+            line["GB_per_s"] = round(info["bytes"] / us / 1e3, 1)
+        if "flops" in info:
+            line["TFLOP_per_s"] = round(info["flops"] / us / 1e6, 2)
+        print(json.dumps(line))
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -827,7 +1209,8 @@ def cpu_prefill_sample(cols_per_core: int = 16) -> dict:
     return {"gop_per_s": round(ops / dt / 1e9, 3), "cores": cores, "kind": "oracle",
             "sample": f"{TP} tokens x {cols_per_core * cores} of 3584 q columns, K=3584, {cores} processes "
                       f"({ops / 1e9:.2f} GOP, {dt:.2f} s)",
-            "layer_seconds_extrapolated": round(layer_ops / (ops / dt), 1)}
+            "layer_seconds_extrapolated": round(layer_ops / (ops / dt), 1),
+            "prefill_28_layers_seconds_extrapolated": round(28 * layer_ops / (ops / dt), 1)}
 
 
 def run_reference(args, rank: int) -> dict | None:
@@ -864,7 +1247,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip the per-component times of the other workloads (GLU+down, routed MoE, prefill MMQ)")
+    ap.add_argument("--case", default=None, help="run one named kernel case (for ncu) instead of the benchmark")
+    ap.add_argument("--reps", type=int, default=4, help="--case: launches before the optional timing")
+    ap.add_argument("--time", type=int, default=0, metavar="N", help="--case: time N more launches after L2 flushes")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -324,10 +324,11 @@ QK_API qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T,
  * exits). Inputs and outputs are still passed by the caller.
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
+ *   - Every argument is checked as in qk_mmvq before anything is enqueued.
  *   - Calls whose workspace need (qk_mmvq_workspace_bytes) exceeds
  *     QK_MMVQ_STATIC_WS_BYTES are refused with QK_ERR_UNSUPPORTED.
- *   - Each call clears the array's completion counters on its stream before
- *     its kernels run; it allocates nothing.
+ *   - Each call clears the array's completion counters (only those) on its
+ *     stream before its kernels run; it allocates nothing.
  *   - All calls on a device share the one array, so calls that may overlap on
  *     the GPU (different streams, or graphs replayed concurrently) race and
  *     give wrong results; order them on one stream.

@@ -1133,14 +1133,16 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ s
 }  // namespace
 
 int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
+    constexpr int MAXDEV = 64;
+    static int n[MAXDEV] = {};   // per device: the grid sizes and workspace layout depend on it
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAXDEV) return 148;
+    if (n[dev] <= 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n[dev] = v;
     }
-    return n;
+    return n[dev];
 }
 
 namespace {
@@ -1156,6 +1158,12 @@ size_t sk_smem() {
 // Workspace of the ordinary path: [G][2][VALS] partial sums, then one counter
 // per 128-row tile; G = min(units, SMs) CTAs.
 int64_t mmvq_workspace_bytes(int n_proj, const qk_proj *projs) {
+    int64_t off = 0, bytes = 0;
+    mmvq_counter_range(n_proj, projs, &off, &bytes);
+    return off + bytes;
+}
+
+void mmvq_counter_range(int n_proj, const qk_proj *projs, int64_t *offset, int64_t *bytes) {
     int64_t U = 0, R = 0;
     for (int j = 0; j < n_proj; j++) {
         const int64_t rts = ceil_div(projs[j].N, UNIT_ROWS);
@@ -1163,7 +1171,8 @@ int64_t mmvq_workspace_bytes(int n_proj, const qk_proj *projs) {
         R += rts;
     }
     const int64_t G = U < sm_count() ? U : sm_count();
-    return G * 2 * VALS * (int64_t)sizeof(float) + R * (int64_t)sizeof(unsigned int);
+    *offset = G * 2 * VALS * (int64_t)sizeof(float);
+    *bytes = R * (int64_t)sizeof(unsigned int);
 }
 
 qk_status launch_wait_selftest(cudaStream_t s) {
@@ -1309,12 +1318,13 @@ void *g_static_ws_ptr[MAX_DEVICES] = {};
 extern "C" QK_API qk_status qk_mmvq_static_ws(const void *img, int64_t img_row_blocks, int64_t T,
                                               int32_t n_proj, const qk_proj *projs,
                                               const int32_t *d_live_rows, qk_stream stream) {
-    if (!projs || n_proj < 1 || n_proj > 8)
-        return qk::fail(QK_ERR_ARG, "qk_mmvq_static_ws: projs null or n_proj=%d not in 1..8", (int)n_proj);
+    // Every argument is checked before anything is enqueued, as in qk_mmvq.
+    qk_status st = qk::mmvq_validate(img, img_row_blocks, T, n_proj, projs);
+    if (st != QK_OK) return st;
     const size_t need = qk_mmvq_workspace_bytes(n_proj, projs);
     if (need > QK_MMVQ_STATIC_WS_BYTES)
         return qk::fail(QK_ERR_UNSUPPORTED, "qk_mmvq_static_ws: needs %zu bytes of scratch, the static array holds %u",
-                    need, (unsigned)QK_MMVQ_STATIC_WS_BYTES);
+                        need, (unsigned)QK_MMVQ_STATIC_WS_BYTES);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return qk::fail(QK_ERR_CUDA, "qk_mmvq_static_ws: %s", cudaGetErrorString(e));
@@ -1331,8 +1341,21 @@ extern "C" QK_API qk_status qk_mmvq_static_ws(const void *img, int64_t img_row_b
         }
         ws = g_static_ws_ptr[dev];
     }
-    // the counters (and, simply, all scratch this call uses) must start at zero
-    e = cudaMemsetAsync(ws, 0, need, (cudaStream_t)stream);
-    if (e != cudaSuccess) return qk::fail(QK_ERR_CUDA, "qk_mmvq_static_ws: clearing scratch: %s", cudaGetErrorString(e));
+    // Only the completion counters must start at zero: every launch returns them to
+    // zero itself, so this clear matters after a bounded wait ran out and left one
+    // set. The partial-sum slots are always written before they are read. One
+    // launch per weight type present, so one counter range per type.
+    for (int wt = QK_W_Q4_0; wt <= QK_W_Q8_0; wt++) {
+        qk_proj group[8];
+        int n = 0;
+        for (int j = 0; j < n_proj; j++)
+            if (projs[j].wtype == wt) group[n++] = projs[j];
+        if (n == 0) continue;
+        int64_t off = 0, bytes = 0;
+        qk::mmvq_counter_range(n, group, &off, &bytes);
+        e = cudaMemsetAsync(static_cast<unsigned char *>(ws) + off, 0, (size_t)bytes, (cudaStream_t)stream);
+        if (e != cudaSuccess)
+            return qk::fail(QK_ERR_CUDA, "qk_mmvq_static_ws: clearing the counters: %s", cudaGetErrorString(e));
+    }
     return qk_mmvq(img, img_row_blocks, T, n_proj, projs, d_live_rows, ws, QK_MMVQ_STATIC_WS_BYTES, stream);
 }

@@ -46,6 +46,45 @@ using namespace qk;
 
 static bool aligned(const void *p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+static qk_status check_proj_common(int32_t wtype, const void *w, int64_t N, int64_t K, int64_t img_row_blocks) {
+    REQUIRE(wtype == QK_W_Q4_0 || wtype == QK_W_Q8_0, QK_ERR_ARG, "bad wtype %d", (int)wtype);
+    REQUIRE(w, QK_ERR_ARG, "null weight pointer");
+    REQUIRE(aligned(w, 16), QK_ERR_ARG, "packed weights must be 16-byte aligned");
+    REQUIRE(N >= 1 && N <= INT32_MAX && K >= 32 && K <= INT32_MAX, QK_ERR_ARG, "N or K out of range");
+    REQUIRE(K % QB == 0, QK_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
+    REQUIRE(K / QB <= img_row_blocks, QK_ERR_SHAPE, "K=%lld reaches past the image row (%lld blocks)",
+            (long long)K, (long long)img_row_blocks);
+    return QK_OK;
+}
+
+namespace qk {
+// Every check of qk_mmvq except those of the workspace: the image, T, the
+// projections, their outputs and aliasing between them.
+qk_status mmvq_validate(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_proj, const qk_proj *projs) {
+    REQUIRE(img && projs, QK_ERR_ARG, "null pointer");
+    REQUIRE(aligned(img, 4), QK_ERR_ARG, "img not 4-byte aligned");
+    REQUIRE(T >= 1 && img_row_blocks >= 1, QK_ERR_ARG, "T or img_row_blocks < 1");
+    REQUIRE(T <= 8, QK_ERR_UNSUPPORTED, "T=%lld > 8 (use qk_mmq for larger batches)", (long long)T);
+    REQUIRE(n_proj >= 1 && n_proj <= 8, QK_ERR_UNSUPPORTED, "n_proj=%d not in 1..8", (int)n_proj);
+    Span si = span(img, (size_t)(T * img_row_blocks * Q8_1_BYTES));
+    for (int j = 0; j < n_proj; j++) {
+        const qk_proj &p = projs[j];
+        qk_status st = check_proj_common(p.wtype, p.w, p.N, p.K, img_row_blocks);
+        if (st != QK_OK) return st;
+        REQUIRE(p.y, QK_ERR_ARG, "projection %d: y is null", j);
+        REQUIRE(p.y_stride >= p.N, QK_ERR_SHAPE, "projection %d: y_stride < N", j);
+        Span sy = span(p.y, rows_span(T, p.y_stride * 4, p.N * 4));
+        Span sw = span(p.w, (size_t)packed_bytes(p.wtype, p.N, p.K));
+        REQUIRE(!overlap(sy, si) && !overlap(sy, sw), QK_ERR_ALIAS, "projection %d: y overlaps img or w", j);
+        for (int i = 0; i < j; i++) {
+            REQUIRE(!rows_overlap(projs[i].y, projs[i].y_stride * 4, projs[i].N * 4, p.y, p.y_stride * 4, p.N * 4, T),
+                    QK_ERR_ALIAS, "outputs of projections %d and %d overlap", i, j);
+        }
+    }
+    return QK_OK;
+}
+}  // namespace qk
+
 extern "C" {
 
 const char *qk_status_string(qk_status s) {
@@ -225,16 +264,6 @@ qk_status qk_weight_pack(qk_wtype wtype, const void *blocks, int64_t N, int64_t 
 }
 
 // ------------------------------------------------------------------ projections
-static qk_status check_proj_common(int32_t wtype, const void *w, int64_t N, int64_t K, int64_t img_row_blocks) {
-    REQUIRE(wtype == QK_W_Q4_0 || wtype == QK_W_Q8_0, QK_ERR_ARG, "bad wtype %d", (int)wtype);
-    REQUIRE(w, QK_ERR_ARG, "null weight pointer");
-    REQUIRE(aligned(w, 16), QK_ERR_ARG, "packed weights must be 16-byte aligned");
-    REQUIRE(N >= 1 && N <= INT32_MAX && K >= 32 && K <= INT32_MAX, QK_ERR_ARG, "N or K out of range");
-    REQUIRE(K % QB == 0, QK_ERR_SHAPE, "K=%lld is not a multiple of 32", (long long)K);
-    REQUIRE(K / QB <= img_row_blocks, QK_ERR_SHAPE, "K=%lld reaches past the image row (%lld blocks)",
-            (long long)K, (long long)img_row_blocks);
-    return QK_OK;
-}
 
 size_t qk_mmvq_workspace_bytes(int32_t n_proj, const qk_proj *projs) {
     if (n_proj < 1 || n_proj > 8 || !projs) return 0;
@@ -264,26 +293,9 @@ qk_status qk_selftest_wait_timeout(qk_stream stream) { return launch_wait_selfte
 
 qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_proj, const qk_proj *projs,
                   const int32_t *d_live_rows, void *ws, size_t ws_bytes, qk_stream stream) {
-    REQUIRE(img && projs, QK_ERR_ARG, "null pointer");
-    REQUIRE(aligned(img, 4), QK_ERR_ARG, "img not 4-byte aligned");
-    REQUIRE(T >= 1 && img_row_blocks >= 1, QK_ERR_ARG, "T or img_row_blocks < 1");
-    REQUIRE(T <= 8, QK_ERR_UNSUPPORTED, "T=%lld > 8 (use qk_mmq for larger batches)", (long long)T);
-    REQUIRE(n_proj >= 1 && n_proj <= 8, QK_ERR_UNSUPPORTED, "n_proj=%d not in 1..8", (int)n_proj);
+    qk_status vs = mmvq_validate(img, img_row_blocks, T, n_proj, projs);
+    if (vs != QK_OK) return vs;
     Span si = span(img, (size_t)(T * img_row_blocks * Q8_1_BYTES));
-    for (int j = 0; j < n_proj; j++) {
-        const qk_proj &p = projs[j];
-        qk_status st = check_proj_common(p.wtype, p.w, p.N, p.K, img_row_blocks);
-        if (st != QK_OK) return st;
-        REQUIRE(p.y, QK_ERR_ARG, "projection %d: y is null", j);
-        REQUIRE(p.y_stride >= p.N, QK_ERR_SHAPE, "projection %d: y_stride < N", j);
-        Span sy = span(p.y, rows_span(T, p.y_stride * 4, p.N * 4));
-        Span sw = span(p.w, (size_t)packed_bytes(p.wtype, p.N, p.K));
-        REQUIRE(!overlap(sy, si) && !overlap(sy, sw), QK_ERR_ALIAS, "projection %d: y overlaps img or w", j);
-        for (int i = 0; i < j; i++) {
-            REQUIRE(!rows_overlap(projs[i].y, projs[i].y_stride * 4, projs[i].N * 4, p.y, p.y_stride * 4, p.N * 4, T),
-                    QK_ERR_ALIAS, "outputs of projections %d and %d overlap", i, j);
-        }
-    }
     REQUIRE(ws && aligned(ws, 16), QK_ERR_WORKSPACE, "workspace null or not 16-byte aligned");
     // one launch per weight type present, in order on the stream; they share ws
     for (int wt = QK_W_Q4_0; wt <= QK_W_Q8_0; wt++) {

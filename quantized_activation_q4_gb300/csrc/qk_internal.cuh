@@ -89,7 +89,7 @@ inline int64_t packed_bytes(int wtype, int64_t N, int64_t K) {
     return ceil_div(N, UNIT_ROWS) * ceil_div(K, UNIT_COLS) * unit_bytes(wtype);
 }
 
-// Streaming multiprocessors of the current device (cached after the first call).
+// Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
 // Reads and clears the device-side fault word (bit 0: a bounded mbarrier
@@ -138,6 +138,11 @@ qk_status launch_glu_q8_1(int kind, int layout, const float *a, int64_t a_stride
 qk_status launch_weight_pack(int wtype, const uint8_t *blocks, int64_t N, int64_t K,
                              uint8_t *packed, cudaStream_t s);
 int64_t mmvq_workspace_bytes(int n_proj, const qk_proj *projs);
+// Every argument check of qk_mmvq except those of the workspace (nothing is enqueued).
+qk_status mmvq_validate(const void *img, int64_t img_row_blocks, int64_t T, int32_t n_proj, const qk_proj *projs);
+// Byte range of the ordinary path's completion counters inside its workspace, for the
+// projections of one weight type (they start at zero and every launch leaves them at zero).
+void mmvq_counter_range(int n_proj, const qk_proj *projs, int64_t *offset, int64_t *bytes);
 qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj,
                       const qk_proj *projs, const int32_t *live, void *ws, size_t ws_bytes,
                       cudaStream_t s);

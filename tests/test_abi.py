@@ -90,6 +90,24 @@ def test_projection_checks(lib):
     assert lib.qk_mmvq(P(IMG), 8, 8, 1, arr, None, P(Y), 1 << 20, None) == 3        # workspace over y
 
 
+def test_static_workspace_checks_everything_before_touching_the_device(lib):
+    """qk_mmvq_static_ws runs every argument check of qk_mmvq before it looks up its
+    scratch array or enqueues its counter clear. On a machine without a GPU any CUDA
+    call would report QK_ERR_CUDA (6), so the codes below come from the checks alone."""
+    P = C.c_void_p
+    good = qk.qk_proj(0, 0, W, 64, 256, Y, 64)
+    arr = (qk.qk_proj * 1)(good)
+    assert lib.qk_mmvq_static_ws(P(IMG), 8, 9, 1, arr, None, None) == 5           # T > 8
+    arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W, -5, 256, Y, 64))
+    assert lib.qk_mmvq_static_ws(P(IMG), 8, 8, 1, arr, None, None) == 1           # N < 0
+    arr = (qk.qk_proj * 1)(qk.qk_proj(7, 0, W, 64, 256, Y, 64))
+    assert lib.qk_mmvq_static_ws(P(IMG), 8, 8, 1, arr, None, None) == 1           # bad weight type
+    arr = (qk.qk_proj * 2)(good, qk.qk_proj(0, 0, W, 64, 256, Y + 128, 64))
+    assert lib.qk_mmvq_static_ws(P(IMG), 8, 8, 2, arr, None, None) == 3           # overlapping outputs
+    arr = (qk.qk_proj * 1)(qk.qk_proj(0, 0, W, 64, 288, Y, 64))
+    assert lib.qk_mmvq_static_ws(P(IMG), 8, 8, 1, arr, None, None) == 2           # K past the image row
+
+
 def test_routing_checks(lib):
     P = C.c_void_p
     assert lib.qk_topk_route(P(X), 16, 512, 8, P(Y), P(W), None, None) == 5    # E > 256

@@ -65,11 +65,11 @@ def test_mmq_small_full(T, N, K, rb):
     assert O.nmse(yg, O.proj_plain("q4_0", W, N, K, x)) <= NMSE_GATE
 
 
-def _sampled_check(yg, W, N, K, qsh, dh, rb, x, seed):
+def _sampled_check(yg, W, N, K, qsh, dh, rb, x, seed, ncols=64, nrows=16):
     T = yg.shape[0]
     g = synth.rng(seed)
-    cols = np.sort(g.choice(N, size=min(64, N), replace=False))
-    rows = np.sort(g.choice(T, size=16, replace=False))
+    cols = np.sort(g.choice(N, size=min(ncols, N), replace=False))
+    rows = np.sort(g.choice(T, size=nrows, replace=False))
     exact_cols = O.proj_q8_0_sampled("q4_0", W, N, K, qsh, dh, rb, np.arange(T), cols)
     assert O.nmse(yg[:, cols], exact_cols) <= NMSE_EXACT
     exact_rows = O.proj_q8_0_sampled("q4_0", W, N, K, qsh, dh, rb, rows, np.arange(N))
@@ -129,3 +129,39 @@ def test_dedup_one_quantize_per_distinct_activation():
         assert O.nmse(yg, O.proj_plain("q4_0", W, W.shape[0], K, x)) <= NMSE_GATE
     for W, yg in zip(Wg, outs_gu):
         assert O.nmse(yg, O.proj_plain("q4_0", W, W.shape[0], K, x2)) <= NMSE_GATE
+
+
+def test_prefill_layers_with_fresh_seeds():
+    """Several prefill layers in a row (3325 tokens, d = 3584), each with its own seeded weights
+    and activations (seed 4000 + layer): per layer one Q8_0 image of the attention input read by
+    q/k/v in one launch and one image of the FFN input read by gate/up in one launch. The image
+    planes and the workspace are reused from layer to layer, as in a whole prefill; every layer's
+    outputs are checked on sampled columns and rows against the oracle."""
+    import torch
+    T, K, rb, NFF = 3325, 3584, 112, 18944
+    qs = torch.zeros((T * rb * 32,), dtype=torch.int8, device="cuda")
+    d = torch.zeros((T * rb,), dtype=torch.int16, device="cuda")
+    kmax_projs = [qk.make_proj("q4_0", 16, 128, K, 16, 128)]
+    n = qk.qk_mmq_workspace_bytes(T, kmax_projs)
+    ws = torch.empty((n,), dtype=torch.uint8, device="cuda")
+    for layer in range(3):
+        seed = 4000 + layer
+        for part, shapes in (("attn", (3584, 512, 512)), ("ffn", (NFF, NFF))):
+            x = synth.activations(seed * 10 + (0 if part == "attn" else 1), T, K)
+            qk.qk_quantize_q8_0(dev(x), T, K, K, qs, d, rb)
+            Ws = [synth.q4_0_weight(seed * 100 + (0 if part == "attn" else 10) + i, N, K) for i, N in enumerate(shapes)]
+            keep, projs, outs = [], [], []
+            for W, N in zip(Ws, shapes):
+                pw = pack_weight(W, "q4_0", N, K)
+                y = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
+                keep += [pw, y]
+                outs.append(y)
+                projs.append(qk.make_proj("q4_0", pw, N, K, y, N))
+            qk.qk_mmq(qs, d, rb, T, projs, ws, n)
+            qsh = host(qs).view(np.int8).reshape(T, -1)
+            dh = host(d).view(np.uint16).reshape(T, -1)
+            for i, (W, N, y) in enumerate(zip(Ws, shapes, outs)):
+                yg = host(y)
+                assert not np.isnan(yg).any()
+                _sampled_check(yg, W, N, K, qsh, dh, rb, x, seed * 7 + i, ncols=24, nrows=6)
+    assert qk.qk_device_faults() == 0

@@ -60,12 +60,42 @@ def test_static_workspace_matches_workspace_entry_point_twice():
     assert qk.qk_device_faults() == 0
 
 
+def test_static_workspace_honours_a_device_live_row_count():
+    """With a device live count below T, rows at or past it are left as they were and
+    the live rows equal those of qk_mmvq with an ordinary workspace."""
+    import torch
+
+    T, K, N, live = 8, 2048, 1024, 5
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    img = torch.empty((T * (K // 32) * 36,), dtype=torch.uint8, device="cuda")
+    qk.qk_quantize_q8_1(dev(synth.activations(9520, T, K)), T, K, K, img, K // 32)
+    nb = qk.qk_weight_packed_bytes("q4_0", N, K)
+    w = torch.empty((nb,), dtype=torch.uint8, device="cuda")
+    qk.qk_weight_pack("q4_0", dev(synth.q4_0_weight(9521, N, K).reshape(-1)), N, K, w, nb)
+    live_d = torch.tensor([live], dtype=torch.int32, device="cuda")
+    ref = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
+    got = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
+    ref_p = [qk.make_proj("q4_0", w, N, K, ref, N)]
+    ws_n = qk.qk_mmvq_workspace_bytes(ref_p)
+    ws = torch.zeros((ws_n,), dtype=torch.uint8, device="cuda")
+    qk.qk_mmvq(img, K // 32, T, ref_p, ws, ws_n, d_live_rows=live_d)
+    qk.qk_mmvq_static_ws(img, K // 32, T, [qk.make_proj("q4_0", w, N, K, got, N)], d_live_rows=live_d)
+    torch.cuda.synchronize()
+    r, g = ref.cpu().numpy(), got.cpu().numpy()
+    assert np.isnan(g[live:]).all()
+    assert not np.isnan(g[:live]).any()
+    assert O.nmse(g[:live], r[:live]) <= NMSE_EXACT
+    assert qk.qk_device_faults() == 0
+
+
 def test_static_workspace_refuses_oversized_problems():
     """A problem whose scratch need exceeds the static array is refused before any launch."""
     import torch
 
     big_N = 1 << 27                       # row tiles alone need more counters than the array holds
-    projs = [qk.make_proj("q4_0", 256, big_N, 128, 1024, big_N)]   # fake, never-dereferenced pointers
+    # fake, never-dereferenced pointers far enough apart that the arguments pass every other check
+    w, y, img = 1 << 36, 1 << 38, 1 << 12
+    projs = [qk.make_proj("q4_0", w, big_N, 128, y, big_N)]
     with pytest.raises(qk.QkError) as e:
-        qk.qk_mmvq_static_ws(64, 4, 8, projs, stream=torch.cuda.current_stream())
+        qk.qk_mmvq_static_ws(img, 4, 8, projs, stream=torch.cuda.current_stream())
     assert e.value.name == "QK_ERR_UNSUPPORTED"
