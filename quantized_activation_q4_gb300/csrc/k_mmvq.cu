@@ -88,6 +88,7 @@ struct SkArgs {
     float *ws_part;      // [G][2][VALS]
     unsigned int *ws_cnt;
     int owner_spin;      // short sleeps an owner waits for the other parts (0: general path at once)
+    int csplit;          // 0: stream-K; else CTAs per 128-row tile (a cluster of that size when > 1)
     SkProj p[MAX_PROJ];
 };
 
@@ -513,7 +514,21 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
 
     pdl_trigger();
     const int G = gridDim.x, cta = blockIdx.x;
-    const int64_t u0 = cta_start(cta, a.U, G), u1 = cta_start(cta + 1, a.U, G);
+    int64_t u0, u1;
+    int crank = 0;   // rank in the cluster (cluster split)
+    if (a.csplit) {   // cluster split: CTA c takes part c % csplit of row tile c / csplit (all of K split evenly)
+        const int R = cta / a.csplit;
+        crank = cta % a.csplit;
+        int jj = 0;
+        while (jj + 1 < a.n_proj && R >= a.p[jj + 1].rt_base) jj++;
+        const SkProj &P = a.p[jj];
+        const int64_t first = P.unit_base + (int64_t)(R - P.rt_base) * P.chunks;
+        u0 = first + (int64_t)crank * P.chunks / a.csplit;
+        u1 = first + (int64_t)(crank + 1) * P.chunks / a.csplit;
+    } else {
+        u0 = cta_start(cta, a.U, G);
+        u1 = cta_start(cta + 1, a.U, G);
+    }
     const int n_units = (int)(u1 - u0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t ring = smem_addr(smem);
@@ -566,7 +581,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
     if (tid < 2) {
         SharedTile st = {};
         st.R = -1;
-        if (n_units > 0) {
+        if (n_units > 0 && !a.csplit) {
             int jj, rr, cc;
             decode_unit(a, tid == 0 ? u0 : u1 - 1, jj, rr, cc);
             const SkProj &P = a.p[jj];
@@ -587,6 +602,11 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
     }
 
     all_consumers_sync();   // s_tile is planned
+    // Cluster split: the leader's (rank 0) part slots, [csplit][VALS] floats after the barriers,
+    // addressed through the cluster's shared-memory window.
+    uint32_t cpart_leader = 0;
+    if (a.csplit > 1)
+        asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(cpart_leader) : "r"(ring + (uint32_t)S::BYTES));
     int signalled = 0;          // thread 0: slot + 1 of a part signalled in the loop
     unsigned signal_old = 0;
 
@@ -736,6 +756,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
                 val_pos(tv, row, tok);
                 row += rt * UNIT_ROWS;
                 if (row < P.N && tok < tl) P.y[(int64_t)tok * P.y_stride + row] = sum;
+            } else if (a.csplit) {   // cluster split: into slot crank of the leader's parts
+                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cpart_leader + (uint32_t)(crank * VALS + tv) * 4u),
+                             "f"(sum)
+                             : "memory");
             } else if (cta == s_tile[part_slot].c_first) {
                 keep[part_slot * VALS + tv] = sum;   // owner: kept for the end
             } else {
@@ -743,7 +767,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
             }
         }
         all_consumers_sync();   // red is rewritten by the next segment
-        if (!whole && cta != s_tile[part_slot].c_first && tid == 0) {
+        if (!whole && !a.csplit && cta != s_tile[part_slot].c_first && tid == 0) {
             // signal the part; the result is only looked at after the loop,
             // so the atomic's latency is not waited for here
             signalled = part_slot + 1;
@@ -756,6 +780,31 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
             rt = 0;
             j++;
         }
+    }
+
+    if (a.csplit) {
+        if (a.csplit > 1) {
+            // every part is in the leader's shared memory once all threads of the cluster have
+            // passed this barrier (the producer warps have exited); the leader adds them in rank
+            // order, and no CTA leaves while the leader may still be written
+            asm volatile("fence.acq_rel.cluster;\n barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;"
+                         ::: "memory");
+            if (crank == 0 && n_units > 0) {
+                int jj, rr, cc;
+                decode_unit(a, u0, jj, rr, cc);
+                const SkProj &P = a.p[jj];
+                const float *parts = reinterpret_cast<const float *>(smem + S::BYTES);
+                for (int tv = tid; tv < VALS; tv += SK_CONS * 32) {
+                    float sum = parts[tv];
+                    for (int r = 1; r < a.csplit; r++) sum += parts[r * VALS + tv];
+                    int row, tok;
+                    val_pos(tv, row, tok);
+                    row += rr * UNIT_ROWS;
+                    if (ok && row < P.N && tok < tl) P.y[(int64_t)tok * P.y_stride + row] = sum;
+                }
+            }
+        }
+        return;
     }
 
     // A signalled part whose atomic found all the others already there: this
@@ -1204,15 +1253,74 @@ qk_status launch_weight_pack(int wtype, const uint8_t *blocks, int64_t N, int64_
 }
 
 template <int WT>
-static qk_status launch_sk(const SkArgs &a, int G, cudaStream_t s) {
+static qk_status configure_sk() {
     static bool configured = false;
-    const size_t smem = sk_smem<WT>();
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(mmvq_sk_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        // room for the cluster split's part slots (up to 8 x VALS floats) after the stream-K layout
+        const int smem = (int)(sk_smem<WT>() + 8 * VALS * sizeof(float));
+        cudaError_t e = cudaFuncSetAttribute(mmvq_sk_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq: shared memory attribute: %s", cudaGetErrorString(e));
         configured = true;
     }
-    return launch_pdl("mmvq", mmvq_sk_kernel<WT>, dim3(G), dim3(SK_THREADS), smem, s, a);
+    return QK_OK;
+}
+
+template <int WT>
+static qk_status launch_sk(const SkArgs &a, int G, cudaStream_t s) {
+    qk_status st = configure_sk<WT>();
+    if (st != QK_OK) return st;
+    const int cl = a.csplit > 1 ? a.csplit : 1;
+    const size_t smem = sk_smem<WT>() + (cl > 1 ? (size_t)cl * VALS * sizeof(float) : 0);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(SK_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cl;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cl > 1 ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mmvq_sk_kernel<WT>, a);
+    count_launch();
+    if (e != cudaSuccess) return fail(QK_ERR_CUDA, "mmvq: %s", cudaGetErrorString(e));
+    return check_launch("mmvq");
+}
+
+// Clusters of `cl` CTAs of the ordinary kernel that can be resident at once on the current
+// device (cached per device; -1 when the query fails, so the cluster split is not used).
+template <int WT>
+static int sk_max_clusters(int cl) {
+    constexpr int MAXDEV = 64;
+    static int cache[MAXDEV][9] = {};
+    int dev = 0;
+    if (cl < 2 || cl > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAXDEV) return -1;
+    int &v = cache[dev][cl];
+    if (v == 0) {
+        if (configure_sk<WT>() != QK_OK) return -1;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(cl * 64);
+        cfg.blockDim = dim3(SK_THREADS);
+        cfg.dynamicSmemBytes = sk_smem<WT>() + (size_t)cl * VALS * sizeof(float);
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mmvq_sk_kernel<WT>, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = -1;
+        }
+        v = n;
+    }
+    return v;
 }
 
 qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj, const qk_proj *projs,
@@ -1245,13 +1353,33 @@ qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj,
         return e ? atoi(e) : OWNER_SPIN;
     }();
     a.owner_spin = owner_spin;
-    const int G = (int)(U < sm_count() ? U : sm_count());
+    int G = (int)(U < sm_count() ? U : sm_count());
     const int64_t need = mmvq_workspace_bytes(n_proj, projs);
     if (!ws || ws_bytes < (size_t)need)
         return fail(QK_ERR_WORKSPACE, "mmvq: workspace %zu < %lld bytes", ws_bytes, (long long)need);
     a.ws_part = static_cast<float *>(ws);
     a.ws_cnt = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(ws) + (int64_t)G * 2 * VALS * sizeof(float));
-    return projs[0].wtype == QK_W_Q4_0 ? launch_sk<QK_W_Q4_0>(a, G, s) : launch_sk<QK_W_Q8_0>(a, G, s);
+    // Cluster split instead of stream-K when the row tiles map onto the SMs in one wave of
+    // clusters (csplit CTAs per tile, each a contiguous part of K) and no CTA then takes more
+    // than two units beyond the stream-K share: the tile's parts are added through the
+    // leader's shared memory instead of the workspace and L2 (q/k/v: 36 tiles x 4 CTAs, 7 units each).
+    const bool q4 = projs[0].wtype == QK_W_Q4_0;
+    int cmin = 1 << 30;
+    for (int j = 0; j < n_proj; j++) cmin = a.p[j].chunks < cmin ? a.p[j].chunks : cmin;
+    int cs = R > 0 ? sm_count() / R : 0;
+    cs = cs > 8 ? 8 : cs;
+    cs = cs > cmin ? cmin : cs;
+    if (cs >= 1) {
+        int cmax = 0;
+        for (int j = 0; j < n_proj; j++) cmax = a.p[j].chunks > cmax ? a.p[j].chunks : cmax;
+        const int64_t per_cluster_cta = ceil_div(cmax, cs), per_sk_cta = ceil_div(U, G);
+        const int fit = cs == 1 ? sm_count() : (q4 ? sk_max_clusters<QK_W_Q4_0>(cs) : sk_max_clusters<QK_W_Q8_0>(cs));
+        if (per_cluster_cta <= per_sk_cta + 2 && fit >= R) {
+            a.csplit = cs;
+            G = R * cs;
+        }
+    }
+    return q4 ? launch_sk<QK_W_Q4_0>(a, G, s) : launch_sk<QK_W_Q8_0>(a, G, s);
 }
 
 qk_status launch_mmvq_id(const uint8_t *img, int64_t row_blocks, int rows, int k, int n_proj,
