@@ -787,8 +787,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
             // every part is in the leader's shared memory once all threads of the cluster have
             // passed this barrier (the producer warps have exited); the leader adds them in rank
             // order, and no CTA leaves while the leader may still be written
-            asm volatile("fence.acq_rel.cluster;\n barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;"
-                         ::: "memory");
+            // (the arrive releases this thread's shared::cluster stores; the wait acquires the others')
+            asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
             if (crank == 0 && n_units > 0) {
                 int jj, rr, cc;
                 decode_unit(a, u0, jj, rr, cc);
@@ -1360,21 +1360,23 @@ qk_status launch_mmvq(const uint8_t *img, int64_t row_blocks, int T, int n_proj,
     a.ws_part = static_cast<float *>(ws);
     a.ws_cnt = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(ws) + (int64_t)G * 2 * VALS * sizeof(float));
     // Cluster split instead of stream-K when the row tiles map onto the SMs in one wave of
-    // clusters (csplit CTAs per tile, each a contiguous part of K) and no CTA then takes more
-    // than two units beyond the stream-K share: the tile's parts are added through the
-    // leader's shared memory instead of the workspace and L2 (q/k/v: 36 tiles x 4 CTAs, 7 units each).
+    // clusters of at most 4 CTAs (csplit CTAs per tile, each a contiguous part of K) and no CTA
+    // then takes more units than its stream-K share: the tile's parts are added through the
+    // leader's shared memory instead of the workspace and L2 (q/k/v: 36 tiles x 4 CTAs, 7 units
+    // each). Measured: 5-CTA clusters over the 18944 -> 3584 down projection (30 units per CTA
+    // instead of 28) ran 44% slower than stream-K, so larger clusters and longer ranges are not used.
     const bool q4 = projs[0].wtype == QK_W_Q4_0;
     int cmin = 1 << 30;
     for (int j = 0; j < n_proj; j++) cmin = a.p[j].chunks < cmin ? a.p[j].chunks : cmin;
     int cs = R > 0 ? sm_count() / R : 0;
-    cs = cs > 8 ? 8 : cs;
+    cs = cs > 4 ? 4 : cs;
     cs = cs > cmin ? cmin : cs;
     if (cs >= 1) {
         int cmax = 0;
         for (int j = 0; j < n_proj; j++) cmax = a.p[j].chunks > cmax ? a.p[j].chunks : cmax;
         const int64_t per_cluster_cta = ceil_div(cmax, cs), per_sk_cta = ceil_div(U, G);
         const int fit = cs == 1 ? sm_count() : (q4 ? sk_max_clusters<QK_W_Q4_0>(cs) : sk_max_clusters<QK_W_Q8_0>(cs));
-        if (per_cluster_cta <= per_sk_cta + 2 && fit >= R) {
+        if (per_cluster_cta <= per_sk_cta && fit >= R) {
             a.csplit = cs;
             G = R * cs;
         }

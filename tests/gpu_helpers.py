@@ -64,3 +64,22 @@ def mmvq(img, rb, T, projs, live=None):
     ws, n = workspace(projs)
     qk.qk_mmvq(img, rb, T, projs, ws, n, live)
     return ws
+
+
+def assert_exact_path(got, exact, nmse_max=1e-10, rel_max=1e-5, what=""):
+    """A GPU projection against the oracle's exact quantised path, as a whole and element by element.
+
+    Whole output: NMSE <= nmse_max. Every element: |got - exact| <= rel_max * max|exact|. Only
+    binary32 summation order separates the exact block paths from the oracle (about 2^-24 times
+    the square root of the block count, relative), so 1e-5 of the largest output leaves a margin
+    of more than 20x at K = 18944; a dropped, doubled or misplaced block moves an element by about
+    max|exact| / (4 sqrt(blocks)), hundreds of times the bound."""
+    from oracle import oracle as O
+    got = np.asarray(got, dtype=np.float64)
+    exact = np.asarray(exact, dtype=np.float64)
+    assert got.shape == exact.shape, what
+    assert O.nmse(got, exact) <= nmse_max, f"{what}: NMSE {O.nmse(got, exact):.3e}"
+    if exact.size:
+        bound = rel_max * float(np.max(np.abs(exact)))
+        worst = float(np.max(np.abs(got - exact)))
+        assert worst <= bound, f"{what}: element off by {worst:.3e} > {bound:.3e}"

@@ -16,12 +16,16 @@ import pytest
 from oracle import oracle as O
 from quantized_activation_q4_gb300 import binding as qk
 from quantized_activation_q4_gb300 import synth
-from tests.gpu_helpers import dev, host, pack_weight
+from tests.gpu_helpers import assert_exact_path, dev, host, pack_weight
 
 pytestmark = pytest.mark.gpu
 
 NMSE_GATE = 5e-4
 NMSE_EXACT = 2e-6   # binary16 operand rounding, see the module docstring
+# element by element: each product carries about 2^-11 relative error, so an element's error is
+# about 4e-4 of the output's rms (5 rms ~ the largest output); a dropped block moves an element by
+# about rms / sqrt(112) at K = 3584, far past 2e-3 of the largest output
+REL_EXACT = 2e-3
 
 
 def quantize_q8_0(x, K, rb):
@@ -61,7 +65,7 @@ def test_mmq_small_full(T, N, K, rb):
     qsh = host(qs).view(np.int8).reshape(T, -1)
     dh = host(d).view(np.uint16).reshape(T, -1)
     exact = O.proj_q8_0_sampled("q4_0", W, N, K, qsh, dh, rb, np.arange(T), np.arange(N))
-    assert O.nmse(yg, exact) <= NMSE_EXACT
+    assert_exact_path(yg, exact, NMSE_EXACT, REL_EXACT, what="mmq")
     assert O.nmse(yg, O.proj_plain("q4_0", W, N, K, x)) <= NMSE_GATE
 
 
@@ -71,9 +75,9 @@ def _sampled_check(yg, W, N, K, qsh, dh, rb, x, seed, ncols=64, nrows=16):
     cols = np.sort(g.choice(N, size=min(ncols, N), replace=False))
     rows = np.sort(g.choice(T, size=nrows, replace=False))
     exact_cols = O.proj_q8_0_sampled("q4_0", W, N, K, qsh, dh, rb, np.arange(T), cols)
-    assert O.nmse(yg[:, cols], exact_cols) <= NMSE_EXACT
+    assert_exact_path(yg[:, cols], exact_cols, NMSE_EXACT, REL_EXACT, what="mmq columns")
     exact_rows = O.proj_q8_0_sampled("q4_0", W, N, K, qsh, dh, rb, rows, np.arange(N))
-    assert O.nmse(yg[rows], exact_rows) <= NMSE_EXACT
+    assert_exact_path(yg[rows], exact_rows, NMSE_EXACT, REL_EXACT, what="mmq rows")
     Wd = O.dequant("q4_0", W[cols], len(cols), K)
     assert O.nmse(yg[:, cols], x.astype(np.float64) @ Wd.T) <= NMSE_GATE
 

@@ -12,7 +12,7 @@ import pytest
 from oracle import oracle as O
 from quantized_activation_q4_gb300 import binding as qk
 from quantized_activation_q4_gb300 import synth
-from tests.gpu_helpers import dev, empty_u8, host, live_ptr, mmvq, pack_weight, workspace
+from tests.gpu_helpers import assert_exact_path, dev, empty_u8, host, live_ptr, mmvq, pack_weight, workspace
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def run_mmvq(img, rb, T, projs_spec, live=None, y_fill=np.nan):
 
 def check(yg, wtype, W, N, K, x, img_host, rb, rows_plain=None):
     exact = O.proj_q8_1(wtype, W, N, K, img_host, rb)
-    assert O.nmse(yg, exact) <= NMSE_EXACT
+    assert_exact_path(yg, exact, NMSE_EXACT, what=f"{wtype} {N}x{K}")
     sel = np.arange(N) if rows_plain is None else rows_plain
     plain = O.proj_plain(wtype, W[sel], len(sel), K, x)
     assert O.nmse(yg[:, sel], plain) <= NMSE_GATE
@@ -122,6 +122,34 @@ def test_config2_down_projection():
     check(yg, "q4_0", W, N, K, x, host(img).reshape(T, -1), 592, rows_plain=np.arange(0, N, 37))
 
 
+@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "reglu"])
+def test_config2_glu_chain_end_to_end(kind):
+    """Config 2 as one chain: the GLU producer over packed [8, 37888] = [g | u] writes F32
+    [8, 18944] and ONE image of exactly those values, and the Q4_0 down projection 18944 -> 3584
+    reads that image. The image equals the oracle's quantisation of the producer's own output,
+    the projection equals the oracle's exact path on that image on every element, and against the
+    plain definition from the oracle's binary64 GLU (two quantisations on the way: the image, and
+    nothing else on the activation side) it stays inside the pages' NMSE bound."""
+    import torch
+    T, NF, DM = 8, 18944, 3584
+    rb = NF // 32
+    g = synth.activations(60, T, NF)
+    u = synth.activations(61, T, NF)
+    a = np.concatenate([g, u], axis=1)
+    out = torch.full((T, NF), float("nan"), dtype=torch.float32, device="cuda")
+    img = empty_u8(T * rb * 36)
+    qk.qk_glu_q8_1(kind, "packed", dev(a), 2 * NF, None, 0, T, NF, out, NF, img, rb)
+    W = synth.q4_0_weight(62, DM, NF)
+    (yg,) = run_mmvq(img, rb, T, [("q4_0", pack_weight(W, "q4_0", DM, NF), DM, NF)])
+    og, ih = host(out), host(img).reshape(T, -1)
+    assert np.array_equal(ih, O.quantize_q8_1(og, row_blocks=rb))
+    assert_exact_path(yg, O.proj_q8_1("q4_0", W, DM, NF, ih, rb), NMSE_EXACT, what=f"{kind} -> down")
+    glu64 = O.glu(kind, "packed", a, None, NF)
+    rows = np.arange(0, DM, 29)
+    plain = glu64 @ O.dequant("q4_0", W[rows], len(rows), NF).T
+    assert O.nmse(yg[:, rows], plain) <= NMSE_GATE
+
+
 def test_mixed_weight_types_and_live_rows():
     T, K = 8, 512
     x = synth.activations(50, T, K)
@@ -134,7 +162,7 @@ def test_mixed_weight_types_and_live_rows():
     for yg, (wt, W, N) in zip(outs, [("q4_0", W4, 64), ("q8_0", W8, 40)]):
         assert np.all(np.isnan(yg[5:]))                          # rows past live not written
         exact = O.proj_q8_1(wt, W, N, K, ih[:5], 16)
-        assert O.nmse(yg[:5], exact) <= NMSE_EXACT
+        assert_exact_path(yg[:5], exact, NMSE_EXACT, what=wt)
 
 
 def test_deterministic_and_live_independent():

@@ -21,7 +21,7 @@ import pytest
 from oracle import oracle as O
 from quantized_activation_q4_gb300 import binding as qk
 from quantized_activation_q4_gb300 import synth
-from tests.gpu_helpers import dev, empty_u8, host, live_ptr, pack_experts
+from tests.gpu_helpers import assert_exact_path, dev, empty_u8, host, live_ptr, pack_experts
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +67,7 @@ def test_per_slot_matches_oracle(rows, k, n_exp, N, K, live):
     got = host(y)
     ref = O.proj_id_slots_q8_1("q4_0", np.concatenate(Ws, axis=0), n_exp, N, K, img_h, rb, ids_h, rit)
     npl = live * k
-    assert O.nmse(got[:npl], ref[:npl]) <= 1e-10
+    assert_exact_path(got[:npl], ref[:npl], what="per-slot")
     assert np.all(got[npl:] == SENTINEL)                   # padding pairs: no expert work
     flat = ids_h.ravel()
     for p in range(0, npl, max(1, npl // 6)):              # plain definition, each pair's own row
@@ -102,7 +102,7 @@ def test_per_slot_two_projections_one_launch():
     for (wt, N, _), (Ws, _), y in zip(specs, keep, ys):
         got = host(y)
         ref = O.proj_id_slots_q8_1(wt, np.concatenate(Ws, axis=0), n_exp, N, K, img_h, rb, ids_h, rit)
-        assert O.nmse(got[:live * k], ref[:live * k]) <= 1e-10
+        assert_exact_path(got[:live * k], ref[:live * k], what="per-slot")
         assert np.all(got[live * k:] == SENTINEL)
 
 
@@ -242,7 +242,8 @@ def test_routed_ffn_chain_matches_oracle(ffn):
     img = H["img"].reshape(rows, -1)
     ref_g = O.proj_id_q8_1("q4_0", np.concatenate(Wg, axis=0), E, NF, HID, img, HID // 32, ids, rit)
     ref_u = O.proj_id_q8_1("q4_0", np.concatenate(Wu, axis=0), E, NF, HID, img, HID // 32, ids, rit)
-    assert O.nmse(H["yg"][:npl], ref_g[:npl]) <= 1e-10 and O.nmse(H["yu"][:npl], ref_u[:npl]) <= 1e-10
+    assert_exact_path(H["yg"][:npl], ref_g[:npl], what="gate")
+    assert_exact_path(H["yu"][:npl], ref_u[:npl], what="up")
     # GLU over the planned pairs only; its image is the quantisation of the stored output
     ref_h = O.glu("swiglu", "separate", H["yg"][:npl], H["yu"][:npl], NF)
     gu = np.abs(H["yg"][:npl].astype(np.float64) * H["yu"][:npl])
@@ -253,7 +254,7 @@ def test_routed_ffn_chain_matches_oracle(ffn):
     assert np.all(himg[npl:] == 0xA5)
     # per-slot down projection and combine
     ref_d = O.proj_id_slots_q8_1("q4_0", np.concatenate(Wd, axis=0), E, HID, NF, himg, NF // 32, ids, rit)
-    assert O.nmse(H["yd"][:npl], ref_d[:npl]) <= 1e-10
+    assert_exact_path(H["yd"][:npl], ref_d[:npl], what="down")
     assert np.all(H["yd"][npl:] == SENTINEL)
     ref_y = O.moe_combine(H["yd"][:npl], H["wts"][:live])
     terms = np.abs(H["wts"][:live, :, None].astype(np.float64) * H["yd"][:npl].reshape(live, TOPK, HID))
@@ -346,7 +347,7 @@ def test_per_slot_at_the_expert_and_slot_limits():
     _, _, rit = O.moe_plan(ids_h, n_exp, live=live)
     got = host(y)
     ref = O.proj_id_slots_q8_1("q4_0", np.concatenate(Ws, axis=0), n_exp, N, K, img_h, rb, ids_h, rit)
-    assert O.nmse(got[:live * k], ref[:live * k]) <= 1e-10
+    assert_exact_path(got[:live * k], ref[:live * k], what="per-slot")
     assert np.all(got[live * k:] == SENTINEL)
 
 

@@ -14,7 +14,7 @@ import pytest
 from oracle import oracle as O
 from quantized_activation_q4_gb300 import binding as qk
 from quantized_activation_q4_gb300 import synth
-from tests.gpu_helpers import dev, empty_u8, host, live_ptr, pack_experts
+from tests.gpu_helpers import assert_exact_path, dev, empty_u8, host, live_ptr, pack_experts
 
 pytestmark = pytest.mark.gpu
 
@@ -160,7 +160,7 @@ def test_routed_projection_matches_oracle(moe):
         yg = host(bufs[name])
         ref = O.proj_id_q8_1("q4_0", Wall, E, NF, K, img, 80, ids, rit)
         live_pairs = np.arange(live * TOPK)
-        assert O.nmse(yg[live_pairs], ref[live_pairs]) <= 1e-10
+        assert_exact_path(yg[live_pairs], ref[live_pairs], what="routed")
         assert np.all(yg[live * TOPK:] == SENTINEL)             # padding pairs: no expert work
         # plain definition gate on each pair's expert
         for p in live_pairs[::13]:
@@ -246,7 +246,7 @@ def test_routed_widths_passes_and_ragged_tiles(wtype, n_exp, k):
     for j, N in enumerate(Ns):
         got = host(ys[j])
         ref = O.proj_id_q8_1(wtype, np.concatenate(Ws[j], axis=0), n_exp, N, Kp, img_h, Kp // 32, ids_h, rit)
-        assert O.nmse(got[planned], ref[planned]) <= 1e-10
+        assert_exact_path(got[planned], ref[planned], what="routed")
         assert np.all(got[~planned] == SENTINEL)
 
 

@@ -5,9 +5,12 @@ running while a stream is captured into a CUDA graph, a plugin that is handed
 only its input and output tensors, or a latency-critical path that must not
 touch the allocator. For them qk_mmvq_static_ws runs the same kernels as
 qk_mmvq, with the library's own fixed scratch array in place of a
-caller-supplied workspace. This test calls it through the C ABI twice in a
-row and checks both results against qk_mmvq with an ordinary workspace, within
-the exact-path tolerance the other projection tests use. It lives in its own
+caller-supplied workspace (the scratch holds the partial sums of row tiles
+that several CTAs share, and their completion counters). This test calls it
+through the C ABI twice in a row and checks both results against qk_mmvq with
+an ordinary workspace, within the exact-path tolerance the other projection
+tests use, on q/k/v and on an 8192 x 8192 projection whose launch shares row
+tiles between CTAs through the scratch. It lives in its own
 file, collected last, and passes both alone and after the other tests.
 """
 import numpy as np
@@ -16,19 +19,21 @@ import pytest
 from oracle import oracle as O
 from quantized_activation_q4_gb300 import binding as qk
 from quantized_activation_q4_gb300 import synth
+from tests.gpu_helpers import assert_exact_path
 
 pytestmark = pytest.mark.gpu
 
 NMSE_EXACT = 1e-10
 
 
-def test_static_workspace_matches_workspace_entry_point_twice():
+@pytest.mark.parametrize("K,shapes", [(3584, [3584, 512, 512]),   # q, k, v reading one image
+                                      (8192, [8192])])             # a launch that keeps partial sums in the scratch
+def test_static_workspace_matches_workspace_entry_point_twice(K, shapes):
     import torch
 
-    T, K = 8, 3584
-    shapes = [3584, 512, 512]                       # q, k, v reading one image
+    T = 8
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    x = synth.activations(9500, T, K)
+    x = synth.activations(9500 + K, T, K)
     img = torch.empty((T * (K // 32) * 36,), dtype=torch.uint8, device="cuda")
     qk.qk_quantize_q8_1(dev(x), T, K, K, img, K // 32)
     packed, ref_out, new_out = [], [], []
@@ -56,7 +61,7 @@ def test_static_workspace_matches_workspace_entry_point_twice():
         for ref, y in zip(refs, new_out):
             got = y.cpu().numpy()
             assert not np.isnan(got).any(), f"call {call}: output not fully written"
-            assert O.nmse(got, ref) <= NMSE_EXACT, f"call {call}"
+            assert_exact_path(got, ref, NMSE_EXACT, what=f"call {call}")
     assert qk.qk_device_faults() == 0
 
 
@@ -84,7 +89,7 @@ def test_static_workspace_honours_a_device_live_row_count():
     r, g = ref.cpu().numpy(), got.cpu().numpy()
     assert np.isnan(g[live:]).all()
     assert not np.isnan(g[:live]).any()
-    assert O.nmse(g[:live], r[:live]) <= NMSE_EXACT
+    assert_exact_path(g[:live], r[:live], NMSE_EXACT, what="live rows")
     assert qk.qk_device_faults() == 0
 
 
