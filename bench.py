@@ -238,7 +238,6 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         with torch.cuda.graph(g, stream=stream):
             comp_a(r); comp_q(); comp_m(r)
         step_graphs.append(g)
-    kernels_per_step = (qk.launch_count() - n0) // R
     comp_graphs = {}
     for name, fn in (("a", lambda r: comp_a(r)), ("b", lambda r: (comp_q(), comp_m(r))), ("m", lambda r: comp_m(r))):
         n1 = qk.launch_count()
@@ -252,13 +251,25 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         for i in range(n):
             step_graphs[(start + i) % R].replay()
 
+    # The timed steps: one graph holding all K steps back to back (weights rotating over the
+    # replicas), as a serving loop captures many layers in one graph, so no graph-launch gap
+    # separates two steps; the same kernels, arguments and order as K single-step replays.
+    K = args.steps
+    n_run = qk.launch_count()
+    run_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(run_graph, stream=stream):
+        for i in range(K):
+            r = (args.warmup + i) % R
+            comp_a(r); comp_q(); comp_m(r)
+    run_launches = qk.launch_count() - n_run
+
     with torch.cuda.stream(stream):
         enqueue_steps(args.warmup)
+        run_graph.replay()
         for g, _ in comp_graphs.values():
             g.replay()
     torch.cuda.synchronize()
 
-    K = args.steps
     KC = max(-(-200 // R), K // R)         # replays of each component graph (R components each): >= 200 launches
     ev = lambda: torch.cuda.Event(enable_timing=True)
     e_s0, e_s1 = ev(), ev()
@@ -272,9 +283,9 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         with torch.cuda.stream(stream):
             torch.cuda._sleep(int(4e6 + 250_000 * (K + 3 * KC)))  # hold the stream while the host enqueues
             e_s0.record(stream)
-            enqueue_steps(K, start=args.warmup)
+            run_graph.replay()
             e_s1.record(stream)
-            launches += kernels_per_step * K
+            launches += run_launches
             for name, (g, nk) in comp_graphs.items():
                 e_c[name][0].record(stream)
                 for _ in range(KC):
@@ -355,31 +366,29 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
             sets[b]["xin"].copy_(xinh, non_blocking=True)
             e2e_step(0, b)
     torch.cuda.synchronize()
-    e2e_graphs = {}
-    for r in range(R):
-        for b in range(NB):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                e2e_step(r, b)
-            e2e_graphs[(r, b)] = g
 
-    def e2e_run(n, start):
-        """n steps: the first step's input copy, n step graphs, the last step's output copy (so
-        n + 1 copies each way are timed for n steps)."""
-        sets[start % NB]["xin"].copy_(xinh, non_blocking=True)
-        for i in range(start, start + n):
-            e2e_graphs[(i % R, i % NB)].replay()
-        last = (start + n - 1) % NB
-        youth[last].copy_(sets[last]["yout"], non_blocking=True)
+    def e2e_graph(n, start):
+        """n steps in one CUDA graph: the first step's input copy, then each step (its kernels on the
+        main stream while the side stream copies the next step's inputs in and the previous step's
+        outputs out), then the last step's output copy (so n + 1 copies each way for n steps)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            sets[start % NB]["xin"].copy_(xinh, non_blocking=True)
+            for i in range(start, start + n):
+                e2e_step(i % R, i % NB)
+            last = (start + n - 1) % NB
+            youth[last].copy_(sets[last]["yout"], non_blocking=True)
+        return g
 
+    g_warm = e2e_graph(args.warmup, 0)
+    g_run = e2e_graph(K, args.warmup)
     with torch.cuda.stream(stream):
-        e2e_run(args.warmup, 0)
+        g_warm.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        torch.cuda._sleep(int(2e6 + 100_000 * K))   # hold the stream while the host enqueues
         e0.record(stream)
-        e2e_run(K, args.warmup)
+        g_run.replay()
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, "cuda")
@@ -426,7 +435,8 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                    "weight_replicas": R, "weight_bytes_in_rotation": R * W_STEP,
                    "l2_policy": f"weights rotate over {R} replicas ({R * W_STEP / 1e6:.0f} MB > 3x L2 "
                                 f"{l2 / 1e6:.0f} MB); activations and images are small and stay resident",
-                   "graphs": "one CUDA graph per step (4 kernels, programmatic dependent launch between them)",
+                   "graphs": "the K timed steps in one CUDA graph (4 kernels per step, programmatic dependent "
+                             "launch between consecutive kernels, weights rotating over the replicas)",
                    "parallelism": "replicas only" if world > 1 else "single GPU"},
         "components": comp,
         "other_configs": others,
@@ -447,10 +457,10 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "outputs_match_device_path": e2e_match,
                 "schedule": "every step copies x and x2 in from pinned host memory (one copy: column ranges of one "
-                            "buffer) and its 4 outputs back (one copy: column ranges of one buffer); one CUDA graph "
-                            "per step, two device buffer sets, a two-deep pipeline: while a step's kernels run, a "
-                            "second stream copies the next step's inputs in and the previous step's outputs out; "
-                            "n + 1 copies each way are timed for n steps"},
+                            "buffer) and its 4 outputs back (one copy: column ranges of one buffer); the K steps with "
+                            "their copies in one CUDA graph, two device buffer sets, a two-deep pipeline: while a "
+                            "step's kernels run, a second stream copies the next step's inputs in and the previous "
+                            "step's outputs out; K + 1 copies each way are timed for K steps"},
         "gpu_launches": launches,
         "clocks": clocks,
     }
