@@ -28,11 +28,13 @@
 //             shared memory;
 //     warp 1: allocates tensor memory (one 256-column accumulator and five
 //             32-column A stages) and issues the MMAs (one thread);
-//     warps 10-17: read the finished accumulator (two 64-column loads per
-//             warp), release it to the next tile's MMAs as soon as the loads
-//             are done, then store C. (Two 208-column accumulators leave room
-//             for only three A stages; five stages at 256 tokens measured 11%
-//             faster on the gate/up launch.)
+//     warps 10-25: read the finished accumulator (64 columns of one lane
+//             quarter per warp), release it to the next tile's MMAs before
+//             storing anything, then store C (8 warps that stored their first
+//             64 columns before reading the second held the next tile's MMAs
+//             back by about 7% on the gate/up launch). (Two 208-column
+//             accumulators leave room for only three A stages; five stages at
+//             256 tokens measured 11% faster on the gate/up launch.)
 // Within a 32-block the K positions follow the order in which the converters
 // store a packed weight word (column 2t+p: elements 4t+p and 4t+p+2; column
 // 8+2t+p: elements 16+4t+p and 18+4t+p); dequant_b writes B in the same order.
@@ -54,8 +56,9 @@ constexpr int NU = 6;                // packed-unit staging slots (a unit = 2 st
 constexpr int PF = 10;               // units prefetched into L2 ahead of the one being loaded
 constexpr int B_TILE = TN * KC * 2;  // 32 KB
 constexpr uint32_t A_COLS = KC / 2;  // tensor-memory columns of one A stage (two f16 per column)
-constexpr int EPI0 = 10;             // first epilogue warp (8 epilogue warps)
-constexpr int THREADS = 18 * 32;
+constexpr int EPI0 = 10;             // first epilogue warp
+constexpr int N_EPI = 16;            // epilogue warps: 4 lane quarters x 4 column quarters of 64
+constexpr int THREADS = (EPI0 + N_EPI) * 32;
 constexpr uint32_t A_TMEM = TN;           // A stages follow the accumulator
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(A_TMEM + NS * A_COLS <= TMEM_COLS, "tensor memory");
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
             mbar_init(uempty + 8 * u, 256);
         }
         mbar_init(acc_full, 1);      // the MMA commit after a tile's last stage
-        mbar_init(acc_empty, 256);   // the eight epilogue warps, once they have read it
+        mbar_init(acc_empty, N_EPI * 32);   // the epilogue warps, once they have read it
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {   // tensor memory: the accumulator (256 columns) and A stages (5 x 32 columns)
@@ -371,10 +374,10 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                 }
             }
         }
-    } else {   // ---------------- warps 10..17: epilogue (accumulator lane = tile row, column = token)
-        // warp w reads lanes 32 (w % 4).. of columns 128 ((w - 10) / 4) ..+127, releases the
-        // accumulator as soon as its last load is done, then stores the last chunk
-        const int quad = warp & 3, c_half = ((warp - EPI0) >> 2) * (TN / 2);
+    } else {   // ---------------- warps 10..25: epilogue (accumulator lane = tile row, column = token)
+        // warp w reads lanes 32 (w % 4).. of columns 64 ((w - 10) / 4) ..+63 in one load and releases
+        // the accumulator before storing anything, so the next tile's MMAs start while C is written
+        const int quad = warp & 3, c0 = ((warp - EPI0) >> 2) * 64;
         int i = 0;
         for (int tau = blockIdx.x; tau < a.tiles; tau += G, i++) {
             const Tile t = tile_of(a, tau);
@@ -382,36 +385,32 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
             if (!mbar_wait(acc_full, i & 1u)) break;
             tc_fence_after();
             const int row = t.rt * TM + quad * 32 + lane;
-#pragma unroll 1
-            for (int c0 = c_half; c0 < c_half + TN / 2; c0 += 64) {
-                uint32_t v[64];
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
-                    "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63},"
-                    " [%64];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                      "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-                      "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-                      "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]),
-                      "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]),
-                      "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]),
-                      "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]),
-                      "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
-                    : "r"(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (c0 + 64 >= c_half + TN / 2) {   // last chunk read: the MMAs of the next tile may start
-                    tc_fence_before();
-                    mbar_arrive(acc_empty);
-                }
-                if (row < P.N) {
+            uint32_t v[64];
+            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0;
 #pragma unroll
-                    for (int k = 0; k < 64; k++) {
-                        const int tok = t.tok0 + c0 + k;
-                        if (tok < a.T) P.y[(int64_t)tok * P.y_stride + row] = __uint_as_float(v[k]);
-                    }
-                }
+            for (int h = 0; h < 2; h++)   // two 32-column loads (a 64-column load needs more registers)
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                    : "=r"(v[32 * h + 0]), "=r"(v[32 * h + 1]), "=r"(v[32 * h + 2]), "=r"(v[32 * h + 3]),
+                      "=r"(v[32 * h + 4]), "=r"(v[32 * h + 5]), "=r"(v[32 * h + 6]), "=r"(v[32 * h + 7]),
+                      "=r"(v[32 * h + 8]), "=r"(v[32 * h + 9]), "=r"(v[32 * h + 10]), "=r"(v[32 * h + 11]),
+                      "=r"(v[32 * h + 12]), "=r"(v[32 * h + 13]), "=r"(v[32 * h + 14]), "=r"(v[32 * h + 15]),
+                      "=r"(v[32 * h + 16]), "=r"(v[32 * h + 17]), "=r"(v[32 * h + 18]), "=r"(v[32 * h + 19]),
+                      "=r"(v[32 * h + 20]), "=r"(v[32 * h + 21]), "=r"(v[32 * h + 22]), "=r"(v[32 * h + 23]),
+                      "=r"(v[32 * h + 24]), "=r"(v[32 * h + 25]), "=r"(v[32 * h + 26]), "=r"(v[32 * h + 27]),
+                      "=r"(v[32 * h + 28]), "=r"(v[32 * h + 29]), "=r"(v[32 * h + 30]), "=r"(v[32 * h + 31])
+                    : "r"(taddr + 32u * h));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(acc_empty);   // read: the MMAs of the next tile may start
+            const int ntok = a.T - (t.tok0 + c0);   // tokens of this column quarter that exist
+            if (row < P.N && ntok > 0) {
+                float *yp = P.y + (int64_t)(t.tok0 + c0) * P.y_stride + row;
+                const int64_t step = P.y_stride;
+#pragma unroll
+                for (int k = 0; k < 64; k++, yp += step)
+                    if (k < ntok) *yp = __uint_as_float(v[k]);
             }
         }
     }
