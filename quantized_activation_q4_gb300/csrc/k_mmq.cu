@@ -19,22 +19,24 @@
 //   mmq_tc: persistent, one CTA per SM, tiles of (projection, 128-row weight
 //     tile, 256-token tile) taken round-robin, tokens fastest so that the CTAs
 //     running at one time share a few weight row tiles through L2.
+//     A stage is one packed unit: 128 K elements, B as two 64-column boxes
+//     (64 KB), A as 64 tensor-memory columns, eight MMAs; three stages.
+//     (Stages of 64 K elements measured 6-11% slower: each stage pays a fixed
+//     round of barrier hand-offs between the warps below.)
 //     warp 0: TMA -- the B tiles (2D tensor copies, 128-byte swizzle) and the
 //             packed weight units (bulk copies) into shared-memory rings, with
 //             L2 prefetches of the units a few ahead;
 //     warps 2-9: turn each unit's nibbles into f16 A stages held in tensor
-//             memory (tcgen05.st; two warps per 32-lane quarter, one 32-block
+//             memory (tcgen05.st; two warps per 32-lane quarter, two 32-blocks
 //             each), so the MMAs read A from tensor memory and only B from
 //             shared memory;
-//     warp 1: allocates tensor memory (one 256-column accumulator and five
-//             32-column A stages) and issues the MMAs (one thread);
+//     warp 1: allocates tensor memory (one 256-column accumulator and three
+//             64-column A stages) and issues the MMAs (one thread);
 //     warps 10-25: read the finished accumulator (64 columns of one lane
 //             quarter per warp), release it to the next tile's MMAs before
 //             storing anything, then store C (8 warps that stored their first
 //             64 columns before reading the second held the next tile's MMAs
-//             back by about 7% on the gate/up launch). (Two 208-column
-//             accumulators leave room for only three A stages; five stages at
-//             256 tokens measured 11% faster on the gate/up launch.)
+//             back by about 7% on the gate/up launch).
 // Within a 32-block the K positions follow the order in which the converters
 // store a packed weight word (column 2t+p: elements 4t+p and 4t+p+2; column
 // 8+2t+p: elements 16+4t+p and 18+4t+p); dequant_b writes B in the same order.
@@ -50,12 +52,14 @@ namespace {
 constexpr int MAX_PROJ = 8;
 constexpr int TM = 128;              // weight rows per CTA (MMA M)
 constexpr int TN = 256;              // tokens per CTA (MMA N; 3325 tokens = 13 tiles)
-constexpr int KC = 64;               // K elements per stage (one 128-byte swizzle row of f16)
-constexpr int NS = 5;                // stages (A in tensor memory, B in shared memory)
-constexpr int NU = 6;                // packed-unit staging slots (a unit = 2 stages)
+constexpr int KC = 64;               // K elements of one B box (one 128-byte swizzle row of f16)
+constexpr int SK = 128;              // K elements per stage: one packed unit, two B boxes
+constexpr int NS = 3;                // stages (A in tensor memory, B in shared memory)
+constexpr int NU = 3;                // packed-unit staging slots (a unit = one stage)
 constexpr int PF = 10;               // units prefetched into L2 ahead of the one being loaded
-constexpr int B_TILE = TN * KC * 2;  // 32 KB
-constexpr uint32_t A_COLS = KC / 2;  // tensor-memory columns of one A stage (two f16 per column)
+constexpr int B_BOX = TN * KC * 2;   // 32 KB
+constexpr int B_TILE = TN * SK * 2;  // 64 KB
+constexpr uint32_t A_COLS = SK / 2;  // tensor-memory columns of one A stage (two f16 per column)
 constexpr int EPI0 = 10;             // first epilogue warp
 constexpr int N_EPI = 16;            // epilogue warps: 4 lane quarters x 4 column quarters of 64
 constexpr int THREADS = (EPI0 + N_EPI) * 32;
@@ -101,7 +105,7 @@ __device__ __forceinline__ Tile tile_of(const MmqArgs &a, int tau) {
     while (j + 1 < a.n_proj && r >= a.p[j + 1].rt_begin) j++;
     t.j = j;
     t.rt = r - a.p[j].rt_begin;
-    t.nkc = (a.p[j].K + KC - 1) / KC;
+    t.nkc = (a.p[j].K + SK - 1) / SK;   // stages = packed units
     return t;
 }
 
@@ -267,10 +271,10 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                 const Tile t = tile_of(a, tau);
                 const MmqProj &P = a.p[t.j];
                 const uint8_t *units = P.w + (int64_t)t.rt * P.chunks * Q4_UNIT_BYTES;
-                for (int kc = 0; kc < t.nkc; kc++, g++) {
+                for (int kc = 0; kc < t.nkc; kc++, g++) {   // stage kc = packed unit kc
                     const uint32_t s = g % NS;
-                    if ((kc & 1) == 0) {   // a packed unit covers two stages
-                        const int u = kc >> 1;
+                    {
+                        const int u = kc;
                         const uint32_t us = gu % NU;
                         if (gu >= NU && !mbar_wait(uempty + 8 * us, ((gu / NU) - 1) & 1u)) {
                             ok = false;
@@ -295,8 +299,10 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                         ok = false;
                         break;
                     }
+                    // the stage's B: two 64-column boxes (past K they read as zeros)
                     mbar_expect_tx(full_b + 8 * s, B_TILE);
-                    tma_2d(sbase + OFF_B + s * B_TILE, &a.bmap, kc * KC, t.tok0, full_b + 8 * s);
+                    tma_2d(sbase + OFF_B + s * B_TILE, &a.bmap, kc * SK, t.tok0, full_b + 8 * s);
+                    tma_2d(sbase + OFF_B + s * B_TILE + B_BOX, &a.bmap, kc * SK + KC, t.tok0, full_b + 8 * s);
                 }
             }
         }
@@ -319,8 +325,8 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                     tc_fence_after();
                     const uint32_t at = tmem + A_TMEM + s * A_COLS, bt = sbase + OFF_B + s * B_TILE;
 #pragma unroll
-                    for (int ks = 0; ks < KC / 16; ks++)   // K = 16 per MMA: 8 A columns, 32 B bytes
-                        tc_mma(acc, at + 8 * ks, sdesc(bt + 32 * ks), (kc | ks) != 0);
+                    for (int ks = 0; ks < SK / 16; ks++)   // K = 16 per MMA: 8 A columns, 32 B bytes of a box
+                        tc_mma(acc, at + 8 * ks, sdesc(bt + (ks >> 2) * B_BOX + 32 * (ks & 3)), (kc | ks) != 0);
                     tc_commit(empty + 8 * s);   // frees the stage once these MMAs are done
                 }
                 if (ok) tc_commit(acc_full);   // the accumulator is final once its MMAs are done
@@ -335,15 +341,15 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
         bool ok = true;
         for (int tau = blockIdx.x; tau < a.tiles && ok; tau += G) {
             const Tile t = tile_of(a, tau);
-            for (int kc = 0; kc < t.nkc; kc++, g++) {
+            for (int kc = 0; kc < t.nkc; kc++, g++) {   // stage kc = packed unit kc
                 const uint32_t s = g % NS, us = gu % NU;
-                const int h = kc & 1;
-                if (h == 0) ok = mbar_wait(ufull + 8 * us, (gu / NU) & 1u);
+                ok = mbar_wait(ufull + 8 * us, (gu / NU) & 1u);
                 if (ok && g >= NS) ok = mbar_wait(empty + 8 * s, ((g / NS) - 1) & 1u);
                 if (!ok) break;
                 tc_fence_after();
                 const uint8_t *unit = smem + OFF_U + us * Q4_UNIT_BYTES;
-                {
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
                     // Lane (g, t) loads word t of rows g, g+8, 16+g, 24+g of the warp's 32 rows (one
                     // conflict-free 16-byte load) and stores them with the 16x256b shape: registers 0,1
                     // go to lane g and 2,3 to lane g+8 at columns 2t, 2t+1, registers 4..7 the same way
@@ -355,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                     const __half2 s01 = *reinterpret_cast<const __half2 *>(&sc.x), s23 = *reinterpret_cast<const __half2 *>(&sc.y);
                     const uint4 a0 = a_word(wv.x, __low2half2(s01)), a1 = a_word(wv.y, __high2half2(s01));
                     const uint4 a2 = a_word(wv.z, __low2half2(s23)), a3 = a_word(wv.w, __high2half2(s23));
-                    const uint32_t base = arow + s * A_COLS + 16 * qb;
+                    const uint32_t base = arow + s * A_COLS + 16 * jb;
                     asm volatile(
                         "tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(base),
                         "r"(a0.x), "r"(a0.y), "r"(a1.x), "r"(a1.y), "r"(a0.z), "r"(a0.w), "r"(a1.z), "r"(a1.w)
@@ -368,10 +374,8 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 mbar_arrive(full_a + 8 * s);
-                if (h == 1 || kc == t.nkc - 1) {
-                    mbar_arrive(uempty + 8 * us);
-                    gu++;
-                }
+                mbar_arrive(uempty + 8 * us);
+                gu++;
             }
         }
     } else {   // ---------------- warps 10..25: epilogue (accumulator lane = tile row, column = token)
