@@ -458,6 +458,54 @@ QK_API qk_status qk_moe_combine(const float *expert_out, int64_t out_stride, con
  * Errors: QK_ERR_ARG, QK_ERR_SHAPE, QK_ERR_UNSUPPORTED, QK_ERR_ALIAS,
  * QK_ERR_WORKSPACE.
  */
+/*
+ * qk_image_memo -- the consecutive-window memo of minfer doc 52 ("r49 A-quantize
+ * prepass shared-A dedup", sections 2 and 3.1): which activation the caller's
+ * image buffers hold, so that the GEMMs that read one activation (q/k/v,
+ * gate/up) quantise it once. Caller-owned plain data; all zeros is empty.
+ *   key: image format (QK_MEMO_Q8_0 planes or QK_MEMO_Q8_1 image), the source
+ *   pointer x, T, K, x_stride, row_blocks, the stream, and the buffers the image
+ *   was written to (qs and d, or img and NULL): a hit needs every field equal,
+ *   the destination pointers included (the page's physical-pointer check).
+ *   The quantisers are pure functions of these, so a hit equals a recompute byte
+ *   for byte -- provided x was not written since. The memo cannot see writes, so
+ *   it is valid only while that holds, which the page guarantees with two rules
+ *   that the CALLER applies by calling qk_image_memo_clear:
+ *     1. any node that is not a quantised-weight GEMM reading this image clears it
+ *        (the window is consecutive GEMMs; a buffer can only be rewritten by some
+ *        other node, and that node has cleared the memo first);
+ *     2. every synchronisation or graph execution boundary clears it (the next
+ *        execution can hand the same addresses to new data).
+ *   The image buffers must not be any node's output (they live outside the
+ *   caller's activation pool), or another node could overwrite them.
+ *   Live-row counts are not supported (a device-side value cannot be a key).
+ * qk_image_memo_quantize_q8_0 / _q8_1: on a hit nothing is enqueued and *hit = 1;
+ * otherwise as qk_quantize_q8_0 / qk_quantize_q8_1 (no live count), *hit = 0,
+ * and on success the memo records the call's key. Any error clears the memo.
+ * qk_image_memo_match: 1 if a call with these arguments would be a hit, else 0
+ * (host only; enqueues nothing).
+ * Errors: those of the quantisers; QK_ERR_ARG for a null memo or hit pointer.
+ */
+typedef enum qk_memo_format { QK_MEMO_EMPTY = 0, QK_MEMO_Q8_0 = 1, QK_MEMO_Q8_1 = 2 } qk_memo_format;
+typedef struct qk_image_memo {
+    int32_t format; /* qk_memo_format; QK_MEMO_EMPTY: nothing recorded */
+    int32_t reserved;
+    const void *x;
+    int64_t T, K, x_stride, row_blocks;
+    const void *dst0, *dst1; /* qs and d, or img and NULL */
+    qk_stream stream;
+} qk_image_memo;
+QK_API void qk_image_memo_clear(qk_image_memo *memo);
+QK_API int32_t qk_image_memo_match(const qk_image_memo *memo, int32_t format, const float *x, int64_t T,
+                                   int64_t K, int64_t x_stride, const void *dst0, const void *dst1,
+                                   int64_t row_blocks, qk_stream stream);
+QK_API qk_status qk_image_memo_quantize_q8_0(qk_image_memo *memo, const float *x, int64_t T, int64_t K,
+                                             int64_t x_stride, int8_t *qs, uint16_t *d, int64_t row_blocks,
+                                             int32_t *hit, qk_stream stream);
+QK_API qk_status qk_image_memo_quantize_q8_1(qk_image_memo *memo, const float *x, int64_t T, int64_t K,
+                                             int64_t x_stride, void *img, int64_t img_row_blocks,
+                                             int32_t *hit, qk_stream stream);
+
 QK_API size_t qk_mmq_workspace_bytes(int64_t T, int32_t n_proj, const qk_proj *projs);
 QK_API qk_status qk_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, int64_t T,
                  int32_t n_proj, const qk_proj *projs, void *ws, size_t ws_bytes,

@@ -45,6 +45,15 @@ class qk_proj_id(C.Structure):
                 ("K", C.c_int64), ("y", C.c_void_p)]
 
 
+class qk_image_memo(C.Structure):
+    """The consecutive-window memo (see qk.h): all zeros is empty."""
+    _fields_ = [("format", C.c_int32), ("reserved", C.c_int32), ("x", C.c_void_p), ("T", C.c_int64),
+                ("K", C.c_int64), ("x_stride", C.c_int64), ("row_blocks", C.c_int64), ("dst0", C.c_void_p),
+                ("dst1", C.c_void_p), ("stream", C.c_void_p)]
+
+
+MEMO_Q8_0, MEMO_Q8_1 = 1, 2
+
 _lock = threading.Lock()
 _lib = None
 
@@ -75,6 +84,12 @@ _SIGS = {
     "qk_mmvq_id_slots": ([P, I64, I64, I32, I32, C.POINTER(qk_proj_id), P, P, P, P], C.c_int),
     "qk_moe_combine": ([P, I64, P, I64, I32, I64, P, I64, P, P], C.c_int),
     "qk_mmq_workspace_bytes": ([I64, I32, C.POINTER(qk_proj)], C.c_size_t),
+    "qk_image_memo_clear": ([C.POINTER(qk_image_memo)], None),
+    "qk_image_memo_match": ([C.POINTER(qk_image_memo), I32, P, I64, I64, I64, P, P, I64, P], I32),
+    "qk_image_memo_quantize_q8_0": ([C.POINTER(qk_image_memo), P, I64, I64, I64, P, P, I64, C.POINTER(I32), P],
+                                    C.c_int),
+    "qk_image_memo_quantize_q8_1": ([C.POINTER(qk_image_memo), P, I64, I64, I64, P, I64, C.POINTER(I32), P],
+                                    C.c_int),
     "qk_mmq": ([P, P, I64, I64, I32, C.POINTER(qk_proj), P, C.c_size_t, P], C.c_int),
 }
 
@@ -254,6 +269,27 @@ def qk_moe_combine(expert_out, out_stride, wts, rows, k, N, y, y_stride, d_live_
 def qk_mmq_workspace_bytes(T, projs) -> int:
     arr = (qk_proj * len(projs))(*projs)
     return int(load().qk_mmq_workspace_bytes(T, len(projs), arr))
+
+
+def qk_image_memo_clear(memo):
+    load().qk_image_memo_clear(C.byref(memo))
+
+
+def qk_image_memo_quantize_q8_0(memo, x, T, K, x_stride, qs, d, row_blocks, stream=None) -> bool:
+    """Quantises x into (qs, d) unless memo says they already hold it; returns whether it was a hit."""
+    hit = I32(0)
+    _check("qk_image_memo_quantize_q8_0",
+           load().qk_image_memo_quantize_q8_0(C.byref(memo), _ptr(x), T, K, x_stride, _ptr(qs), _ptr(d), row_blocks,
+                                              C.byref(hit), _stream(stream)))
+    return bool(hit.value)
+
+
+def qk_image_memo_quantize_q8_1(memo, x, T, K, x_stride, img, img_row_blocks, stream=None) -> bool:
+    hit = I32(0)
+    _check("qk_image_memo_quantize_q8_1",
+           load().qk_image_memo_quantize_q8_1(C.byref(memo), _ptr(x), T, K, x_stride, _ptr(img), img_row_blocks,
+                                              C.byref(hit), _stream(stream)))
+    return bool(hit.value)
 
 
 def qk_mmq(qs, d, row_blocks, T, projs, ws, ws_bytes, stream=None):

@@ -146,6 +146,63 @@ qk_status qk_quantize_q8_0(const float *x, int64_t T, int64_t K, int64_t x_strid
     return launch_quantize_q8_0(x, (int)T, (int)K, x_stride, qs, d, row_blocks, d_live_rows, (cudaStream_t)stream);
 }
 
+// ------------------------------------------------------------------ image memo
+void qk_image_memo_clear(qk_image_memo *memo) {
+    if (memo) *memo = qk_image_memo{};
+}
+
+int32_t qk_image_memo_match(const qk_image_memo *m, int32_t format, const float *x, int64_t T, int64_t K,
+                            int64_t x_stride, const void *dst0, const void *dst1, int64_t row_blocks,
+                            qk_stream stream) {
+    return m && m->format != QK_MEMO_EMPTY && m->format == format && m->x == x && m->T == T && m->K == K &&
+           m->x_stride == x_stride && m->row_blocks == row_blocks && m->dst0 == dst0 && m->dst1 == dst1 &&
+           m->stream == stream;
+}
+
+static qk_status memo_record(qk_image_memo *m, qk_status st, int32_t format, const float *x, int64_t T,
+                             int64_t K, int64_t x_stride, const void *dst0, const void *dst1, int64_t row_blocks,
+                             qk_stream stream) {
+    qk_image_memo_clear(m);
+    if (st == QK_OK) {
+        m->format = format;
+        m->x = x;
+        m->T = T;
+        m->K = K;
+        m->x_stride = x_stride;
+        m->row_blocks = row_blocks;
+        m->dst0 = dst0;
+        m->dst1 = dst1;
+        m->stream = stream;
+    }
+    return st;
+}
+
+qk_status qk_image_memo_quantize_q8_0(qk_image_memo *memo, const float *x, int64_t T, int64_t K, int64_t x_stride,
+                                      int8_t *qs, uint16_t *d, int64_t row_blocks, int32_t *hit, qk_stream stream) {
+    REQUIRE(memo, QK_ERR_ARG, "memo is null");
+    if (!hit) {
+        qk_image_memo_clear(memo);
+        return fail(QK_ERR_ARG, "hit is null");
+    }
+    *hit = qk_image_memo_match(memo, QK_MEMO_Q8_0, x, T, K, x_stride, qs, d, row_blocks, stream);
+    if (*hit) return QK_OK;
+    const qk_status st = qk_quantize_q8_0(x, T, K, x_stride, qs, d, row_blocks, nullptr, stream);
+    return memo_record(memo, st, QK_MEMO_Q8_0, x, T, K, x_stride, qs, d, row_blocks, stream);
+}
+
+qk_status qk_image_memo_quantize_q8_1(qk_image_memo *memo, const float *x, int64_t T, int64_t K, int64_t x_stride,
+                                      void *img, int64_t img_row_blocks, int32_t *hit, qk_stream stream) {
+    REQUIRE(memo, QK_ERR_ARG, "memo is null");
+    if (!hit) {
+        qk_image_memo_clear(memo);
+        return fail(QK_ERR_ARG, "hit is null");
+    }
+    *hit = qk_image_memo_match(memo, QK_MEMO_Q8_1, x, T, K, x_stride, img, nullptr, img_row_blocks, stream);
+    if (*hit) return QK_OK;
+    const qk_status st = qk_quantize_q8_1(x, T, K, x_stride, img, img_row_blocks, nullptr, stream);
+    return memo_record(memo, st, QK_MEMO_Q8_1, x, T, K, x_stride, img, nullptr, img_row_blocks, stream);
+}
+
 // ------------------------------------------------------------------ producers
 qk_status qk_rmsnorm_q8_1(const float *x, int64_t T, int64_t K, int64_t x_stride, qk_norm_kind kind,
                           const float *w, const float *b, float scale, float eps, float *y,

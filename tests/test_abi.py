@@ -169,3 +169,50 @@ def test_glu_parameter_checks(lib):
     assert lib.qk_glu_q8_1_ex(7, 0, *args, 1.702, 7.0, None, None) == 1
     assert lib.qk_glu_q8_1(7, 0, *args, None, None) == 1
     assert lib.qk_glu_q8_1_ex(6, 0, *args, 1.702, -1.0, None, None) == 1    # SwiGLU-clamp reads limit too
+
+
+def _memo_match(lib, m, fmt=1, x=X, T=8, K=256, xs=256, d0=IMG, d1=Y, rb=8, s=None):
+    P = C.c_void_p
+    return lib.qk_image_memo_match(C.byref(m), fmt, P(x), T, K, xs, P(d0), P(d1) if d1 else None, rb,
+                                   P(s) if s else None)
+
+
+def _memo_fill(m):
+    """The key a successful Q8_0 quantise of X into (IMG, Y) on the null stream records."""
+    m.format, m.x, m.T, m.K, m.x_stride, m.row_blocks, m.dst0, m.dst1, m.stream = 1, X, 8, 256, 256, 8, IMG, Y, None
+
+
+def test_image_memo_hits_only_on_the_whole_key(lib):
+    """minfer doc 52 r49, section 3.1: the key is (source pointer, shape) plus the destination
+    pointers (the physical-pointer check) and the image form; any differing field is a miss."""
+    m = qk.qk_image_memo()
+    assert _memo_match(lib, m) == 0                      # empty
+    _memo_fill(m)
+    assert _memo_match(lib, m) == 1
+    for field, other in [("fmt", 2), ("x", X + 4096), ("T", 7), ("K", 224), ("xs", 320), ("d0", IMG + 4096),
+                         ("d1", Y + 4096), ("rb", 9), ("s", 0x1234)]:
+        assert _memo_match(lib, m, **{field: other}) == 0, field
+    lib.qk_image_memo_clear(C.byref(m))
+    assert m.format == 0 and _memo_match(lib, m) == 0
+
+
+def test_image_memo_hit_enqueues_nothing_and_errors_clear_it(lib):
+    P = C.c_void_p
+    m = qk.qk_image_memo()
+    _memo_fill(m)
+    hit = C.c_int32(-1)
+    n0 = lib.qk_launch_count()
+    # a hit returns at once (no device is touched, nothing is launched)
+    assert lib.qk_image_memo_quantize_q8_0(C.byref(m), P(X), 8, 256, 256, P(IMG), P(Y), 8, C.byref(hit), None) == 0
+    assert hit.value == 1 and lib.qk_launch_count() == n0 and m.format == 1
+    # a Q8_1 request never takes a Q8_0 record
+    assert lib.qk_image_memo_match(C.byref(m), 2, P(X), 8, 256, 256, P(IMG), None, 8, None) == 0
+    # a null hit pointer is refused and clears the memo
+    assert lib.qk_image_memo_quantize_q8_0(C.byref(m), P(X), 8, 256, 256, P(IMG), P(Y), 8, None, None) == 1
+    assert m.format == 0
+    # a miss that fails the quantiser's checks (x_stride < K) reports its error, hit = 0, memo cleared
+    _memo_fill(m)
+    assert lib.qk_image_memo_quantize_q8_0(C.byref(m), P(X), 8, 256, 128, P(IMG), P(Y), 8, C.byref(hit), None) == 2
+    assert hit.value == 0 and m.format == 0
+    # a null memo
+    assert lib.qk_image_memo_quantize_q8_1(None, P(X), 8, 256, 256, P(IMG), 8, C.byref(hit), None) == 1
