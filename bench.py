@@ -724,7 +724,7 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
     layers = [[packed(800 + 10 * r + i, n, DP) for i, n in enumerate(shapes)] for r in range(R4)]
     ys4 = [torch.empty((TP, n), dtype=torch.float32, device="cuda") for n in shapes]
     mk = lambda r, idx: [qk.make_proj("q4_0", layers[r][i], shapes[i], DP, ys4[i], shapes[i]) for i in idx]
-    ws4_n = qk.qk_mmq_workspace_bytes(TP, mk(0, (0,)))
+    ws4_n = max(qk.qk_mmq_workspace_bytes(TP, mk(0, idx)) for idx in ((0, 1, 2), (3, 4)))
     ws4 = torch.empty((ws4_n,), dtype=torch.uint8, device="cuda")
     mmq = lambda q_, d_, projs: qk.qk_mmq(q_, d_, rb, TP, projs, ws4, ws4_n)
 
@@ -831,7 +831,7 @@ def prefill_28(qk, torch, stream, peak_t) -> dict:
     qs = torch.empty((TP * rb * 32,), dtype=torch.int8, device="cuda")
     dh = torch.empty((TP * rb,), dtype=torch.int16, device="cuda")
     mk = lambda ws, idx: [qk.make_proj("q4_0", ws[i], shapes[i], DP, ys[i], shapes[i]) for i in idx]
-    wsn = qk.qk_mmq_workspace_bytes(TP, mk(layers[0][2], (0,)))
+    wsn = max(qk.qk_mmq_workspace_bytes(TP, mk(layers[0][2], idx)) for idx in ((0, 1, 2), (3, 4)))
     wsb = torch.empty((wsn,), dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
     quant_calls = [0]

@@ -145,8 +145,9 @@ def test_prefill_layers_with_fresh_seeds():
     T, K, rb, NFF = 3325, 3584, 112, 18944
     qs = torch.zeros((T * rb * 32,), dtype=torch.int8, device="cuda")
     d = torch.zeros((T * rb,), dtype=torch.int16, device="cuda")
-    kmax_projs = [qk.make_proj("q4_0", 16, 128, K, 16, 128)]
-    n = qk.qk_mmq_workspace_bytes(T, kmax_projs)
+    # one workspace for both launches: the larger of the two sizes (it depends on the projections)
+    n = max(qk.qk_mmq_workspace_bytes(T, [qk.make_proj("q4_0", 16, N, K, 16, N) for N in shapes])
+            for shapes in ((3584, 512, 512), (NFF, NFF)))
     ws = torch.empty((n,), dtype=torch.uint8, device="cuda")
     for layer in range(3):
         seed = 4000 + layer
