@@ -946,12 +946,20 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
     uint64_t *empty = full + SLOTS;
     int32_t *live_e = reinterpret_cast<int32_t *>(empty + SLOTS);   // [ID_MAX_E]
     int32_t *pass_pre = live_e + ID_MAX_E;                            // [ID_MAX_E + 1]
-    __shared__ int tok_img[8], tok_out[8], w_live[RW + 1], w_pass[RW + 1];
+    // token lists of the CTA's items, double-buffered by item parity: the consumers read the first
+    // item's themselves; lanes 1..8 of the producer warp write item k's (k >= 1) into buffer k & 1
+    // while item k - 1 runs (meta_full), and the consumers release a buffer after its item (meta_empty)
+    __shared__ int tok_img[2][8], tok_out[2][8], w_live[RW + 1], w_pass[RW + 1];
+    __shared__ __align__(8) uint64_t meta_full[2], meta_empty[2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t4 = lane & 3, g = lane >> 2;
     if (threadIdx.x == 0) {
         for (int s = 0; s < SLOTS; s++) {
             mbar_init(smem_addr(full + s), 1);
             mbar_init(smem_addr(empty + s), 4 * 32);   // the four warps that take a unit
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(smem_addr(meta_full + b), 8);   // the eight token-list lanes
+            mbar_init(smem_addr(meta_empty + b), 1);  // the consumers, once the item is stored
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1040,6 +1048,21 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
                     }
                 }
             }
+        } else if (lane <= 8) {   // lanes 1..8: slot lane - 1 of the token list of items 1, 2, ... ahead
+            const int q = lane - 1;
+            int k = 1;
+            for (int it = blockIdx.x + G; it < n_work; it += G, k++) {
+                const int b = k & 1;
+                if (k >= 2 && !mbar_wait(smem_addr(meta_empty + b), ((k >> 1) - 1) & 1u)) break;
+                const IdItem w = id_item(a, live_e, pass_pre, n_live, it);
+                const int n_items = __ldg(a.counts + w.e), item0 = __ldg(a.offsets + w.e);
+                const int idx = w.pass * 8 + q;
+                int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
+                if (p < 0 || p / a.k >= a.rows) p = -1;   // not a pair of this bucket: skip
+                tok_img[b][q] = p >= 0 ? (a.per_pair ? p : p / a.k) : -1;
+                tok_out[b][q] = p;
+                mbar_arrive(smem_addr(meta_full + b));
+            }
         }
         return;
     }
@@ -1048,23 +1071,29 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
     bool ok = true;
     const int jb = warp & 3, par = warp >> 2;
     uint32_t pos0 = 0;   // ring position of the current pass's first unit
-    for (int it = blockIdx.x; it < n_work; it += G) {
+    int k = 0;           // this CTA's item count so far (picks the token-list buffer)
+    for (int it = blockIdx.x; it < n_work; it += G, k++) {
         const IdItem w = id_item(a, live_e, pass_pre, n_live, it);
         const IdProj &P = a.p[w.j];
-        const int n_items = __ldg(a.counts + w.e), item0 = __ldg(a.offsets + w.e);
         const int Kb = P.K / QB, chunks = P.chunks;
         const int pp = (chunks + ID_PAR - 1) / ID_PAR * ID_PAR;
-        {
-            const int pass = w.pass;
+        const int mb = k & 1;
+        if (k == 0) {   // the first item's token list: no earlier item to hide its loads behind
             if (threadIdx.x < 8) {
-                const int idx = pass * 8 + threadIdx.x;
+                const int n_items = __ldg(a.counts + w.e), item0 = __ldg(a.offsets + w.e);
+                const int idx = w.pass * 8 + threadIdx.x;
                 int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
                 if (p < 0 || p / a.k >= a.rows) p = -1;   // not a pair of this bucket: skip
-                tok_img[threadIdx.x] = p >= 0 ? (a.per_pair ? p : p / a.k) : -1;
-                tok_out[threadIdx.x] = p;
+                tok_img[0][threadIdx.x] = p >= 0 ? (a.per_pair ? p : p / a.k) : -1;
+                tok_out[0][threadIdx.x] = p;
             }
             id_consumers_sync();
-            const int rB = tok_img[g], rS0 = tok_img[2 * t4], rS1 = tok_img[2 * t4 + 1];
+        } else if (ok) {   // later items': prefetched; buffer 1 holds items 1, 3, ..., buffer 0 items 2, 4, ...
+            const uint32_t phase = (k & 1) ? (uint32_t)(k >> 1) : (uint32_t)((k >> 1) - 1);
+            ok = mbar_wait(smem_addr(meta_full + mb), phase & 1u);
+        }
+        {
+            const int rB = tok_img[mb][g], rS0 = tok_img[mb][2 * t4], rS1 = tok_img[mb][2 * t4 + 1];
             const uint8_t *imgB = rB >= 0 ? a.img + (int64_t)rB * a.img_row_bytes : nullptr;
             const uint8_t *imgS0 = rS0 >= 0 ? a.img + (int64_t)rS0 * a.img_row_bytes : nullptr;
             const uint8_t *imgS1 = rS1 >= 0 ? a.img + (int64_t)rS1 * a.img_row_bytes : nullptr;
@@ -1105,10 +1134,11 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
                 int row, slot;
                 val_pos(t, row, slot);
                 row += w.rt * UNIT_ROWS;
-                const int orow = tok_out[slot];
+                const int orow = tok_out[mb][slot];
                 if (row < P.N && orow >= 0) P.y[(int64_t)orow * P.N + row] = sum;
             }
-            id_consumers_sync();   // tok_* and red are reused by the next item
+            id_consumers_sync();   // red is reused by the next item, the token list two items on
+            if (threadIdx.x == 0) mbar_arrive(smem_addr(meta_empty + mb));
         }
         pos0 += pp;
     }
