@@ -567,12 +567,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
         return;
     }
 
-    // Everything below reads what the previous kernel wrote (image, live count,
-    // workspace) or writes outputs, so it waits for that kernel first.
-    pdl_wait();
-    const int tl = live_rows(a.live, a.T);
-
     // ---------------- consumers
+    int tl = 0;   // live tokens: read after the wait on the previous kernel, below
     const int tid = threadIdx.x, p = warp & 3;
     bool ok = true;
 
@@ -672,12 +668,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
     const int q = warp >> 2, g = lane >> 2, t4 = lane & 3;
     const uint32_t recs_q = ring + S::RECS + (uint32_t)q * 2 * 4 * BREC;
 
-    // Image words of block p of this phase's units, IMG_AHEAD units ahead. The
-    // load cursor walks the phase's units (every fourth) with the current
-    // projection's sizes in registers.
-    const uint8_t *imgB = g < tl ? a.img + (int64_t)g * a.img_row_bytes : nullptr;
-    const uint8_t *imgS0 = 2 * t4 < tl ? a.img + (int64_t)(2 * t4) * a.img_row_bytes : nullptr;
-    const uint8_t *imgS1 = 2 * t4 + 1 < tl ? a.img + (int64_t)(2 * t4 + 1) * a.img_row_bytes : nullptr;
+    // The load cursor walks the phase's units (every fourth) with the current projection's sizes
+    // in registers.
     int lj = j, lrt = rt, lc = c, li = q;   // cursor at this phase's first unit
     int l_kb = 0, l_chunks = 1, l_rtiles = 1;
     if (n_units > 0) {
@@ -700,6 +692,17 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
         }
     };
     cursor_step(q);
+
+    // Everything above depends on the arguments only and overlaps the previous kernel's tail;
+    // everything below reads what that kernel wrote (image, live count, workspace) or writes
+    // outputs, so it waits for it first.
+    pdl_wait();
+    tl = live_rows(a.live, a.T);
+
+    // Image words of block p of this phase's units, IMG_AHEAD units ahead.
+    const uint8_t *imgB = g < tl ? a.img + (int64_t)g * a.img_row_bytes : nullptr;
+    const uint8_t *imgS0 = 2 * t4 < tl ? a.img + (int64_t)(2 * t4) * a.img_row_bytes : nullptr;
+    const uint8_t *imgS1 = 2 * t4 + 1 < tl ? a.img + (int64_t)(2 * t4 + 1) * a.img_row_bytes : nullptr;
     auto load_next = [&]() -> Raw {   // image words of block p of unit li; then li += NPH
         Raw r = {0u, 0u, 0u, 0u};
         if (li < n_units) {
