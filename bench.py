@@ -47,6 +47,10 @@ METRIC = "µs per fused component and weight-stream GB/s (% of HBM peak), Q4_0 T
 UNIT = "GB/s"
 
 
+WORKLOAD = ("shared-image attention projections, Qwen2-7B-like d=3584 T=8 (RMSNorm*w -> Q8_1 image -> q 3584x3584, "
+            "k/v 512x3584) + ordinary K=8192 N=8192 T=8 matvec")
+
+
 def weight_bytes(N: int, K: int) -> int:
     return N * (K // 32) * 18
 
@@ -429,9 +433,7 @@ def run_gpu(args, rank: int, world: int) -> dict | None:
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "q4_0 weights x q8_1 image (f16 MMA, f32 accum)",
         "data": "synthetic (seeded; N(0,1) activations, uniform-nibble Q4_0 weights with half scales U[0.002,0.02])",
-        "config": {"workload": "shared-image attention projections, Qwen2-7B-like d=3584 T=8 "
-                               "(RMSNorm*w -> Q8_1 image -> q 3584x3584, k/v 512x3584) + ordinary "
-                               "K=8192 N=8192 T=8 matvec",
+        "config": {"workload": WORKLOAD,
                    "weight_replicas": R, "weight_bytes_in_rotation": R * W_STEP,
                    "l2_policy": f"weights rotate over {R} replicas ({R * W_STEP / 1e6:.0f} MB > 3x L2 "
                                 f"{l2 / 1e6:.0f} MB); activations and images are small and stay resident",
@@ -1242,8 +1244,7 @@ def run_reference(args, rank: int) -> dict | None:
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulation (oracle)",
             "data": "synthetic (seeded)",
-            "config": {"workload": "shared-image attention projections d=3584 T=8 + ordinary K=8192 N=8192 T=8 "
-                                   "(CPU oracle sample)"},
+            "config": {"workload": WORKLOAD, "parallelism": "single host thread (bounded sample, see cpu_baseline)"},
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
