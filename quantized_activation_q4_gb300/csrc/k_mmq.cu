@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
         mbar_init(acc_empty, N_EPI * 32);   // the epilogue warps, once they have read it
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {   // tensor memory: the accumulator (256 columns) and A stages (5 x 32 columns)
+    if (warp == 1) {   // tensor memory: the accumulator (256 columns) and A stages (3 x 64 columns)
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
                      : "memory");

@@ -869,7 +869,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
 // none of their weights is read, the grid is sized once for the resident CTAs
 // whatever the live count, and round-robin over items of one size balances the
 // CTAs. A CTA streams its items' 128x128 units with TMA bulk copies into a
-// small ring (a producer warp), and RW consumer warps take the blocks: warp w
+// small ring (lane 0 of a producer warp, whose lanes 1..8 fetch each later
+// item's token list ahead), and RW consumer warps take the blocks: warp w
 // does block w & 3 of the units with index = w >> 2 mod RW/4, for all 128 rows
 // and the item's pairs. An item takes a whole number of RW/4 ring positions (a
 // dummy position completes its slot without a copy), so unit u of an item
