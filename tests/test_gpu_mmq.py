@@ -69,6 +69,25 @@ def test_mmq_small_full(T, N, K, rb):
     assert O.nmse(yg, O.proj_plain("q4_0", W, N, K, x)) <= NMSE_GATE
 
 
+def test_mmq_projections_of_different_k_in_one_launch():
+    """Several projections of one image with different K in one launch: B is dequantised for the
+    largest K and each projection reads only its own 128-K stages (a partial last stage meets the
+    weights' zero padding). Every output against the oracle's exact path."""
+    T, rb = 70, 12
+    x = synth.activations(7200, T, rb * 32)
+    qs, d = quantize_q8_0(x, rb * 32, rb)
+    specs = [(synth.q4_0_weight(7201, 200, 384), 200, 384), (synth.q4_0_weight(7202, 96, 160), 96, 160),
+             (synth.q4_0_weight(7203, 130, 256), 130, 256)]
+    outs, _ = run_mmq(qs, d, rb, T, specs)
+    qsh = host(qs).view(np.int8).reshape(T, -1)
+    dh = host(d).view(np.uint16).reshape(T, -1)
+    for (W, N, K), yg in zip(specs, outs):
+        assert not np.isnan(yg).any()
+        exact = O.proj_q8_0_sampled("q4_0", W, N, K, qsh, dh, rb, np.arange(T), np.arange(N))
+        assert_exact_path(yg, exact, NMSE_EXACT, REL_EXACT, what=f"mmq K={K}")
+        assert O.nmse(yg, O.proj_plain("q4_0", W, N, K, x[:, :K])) <= NMSE_GATE
+
+
 def _sampled_check(yg, W, N, K, qsh, dh, rb, x, seed, ncols=64, nrows=16):
     T = yg.shape[0]
     g = synth.rng(seed)
