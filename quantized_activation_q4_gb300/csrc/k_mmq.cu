@@ -73,8 +73,8 @@ constexpr uint32_t SUSPEND_NS = 20000;
 constexpr int OFF_B = 0;
 constexpr int OFF_U = OFF_B + NS * B_TILE;
 constexpr int OFF_BAR = OFF_U + NU * Q4_UNIT_BYTES;
-// full_a[NS] full_b[NS] empty[NS] ufull[NU] uempty[NU] acc_full acc_empty
-constexpr int N_BARS = 3 * NS + 2 * NU + 2;
+// full_a[NS] full_b[NS] empty[NS] ufull[NU] uempty[NU] acc_full acc_empty mma_done
+constexpr int N_BARS = 3 * NS + 2 * NU + 3;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + slack to align the base to 1024
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
     const uint32_t sbase = smem_u32(smem);
     const uint32_t full_a = sbase + OFF_BAR, full_b = full_a + NS * 8, empty = full_b + NS * 8;
     const uint32_t ufull = empty + NS * 8, uempty = ufull + NU * 8, acc_full = uempty + NU * 8,
-                   acc_empty = acc_full + 8;
+                   acc_empty = acc_full + 8, mma_done = acc_empty + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + N_BARS * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
         }
         mbar_init(acc_full, 1);      // the MMA commit after a tile's last stage
         mbar_init(acc_empty, N_EPI * 32);   // the epilogue warps, once they have read it
+        mbar_init(mma_done, 1);      // the MMA thread's last commit: all its MMAs are done
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {   // tensor memory: the accumulator (256 columns) and A stages (3 x 64 columns)
@@ -305,6 +306,13 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                     tma_2d(sbase + OFF_B + s * B_TILE + B_BOX, &a.bmap, kc * SK + KC, t.tok0, full_b + 8 * s);
                 }
             }
+            // Every copy this thread issued has landed before the CTA can exit, also after a wait
+            // above ran out: the last NS stages' B and the last NU units (a barrier whose phase
+            // completed long ago passes at once). A wait that runs out here ends the drain.
+            for (uint32_t x = g > NS ? g - NS : 0; x < g; x++)
+                if (!mbar_wait(full_b + 8 * (x % NS), (x / NS) & 1u)) break;
+            for (uint32_t x = gu > NU ? gu - NU : 0; x < gu; x++)
+                if (!mbar_wait(ufull + 8 * (x % NU), (x / NU) & 1u)) break;
         }
     } else if (warp == 1) {   // ---------------- MMA issue (one thread)
         if (lane == 0) {
@@ -331,6 +339,10 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_tc_kernel(const __grid_constan
                 }
                 if (ok) tc_commit(acc_full);   // the accumulator is final once its MMAs are done
             }
+            // every MMA issued here is complete before the tensor memory is freed (after a wait
+            // that ran out as well)
+            tc_commit(mma_done);
+            mbar_wait(mma_done, 0u);
         }
     } else if (warp < EPI0) {   // ---------------- warps 2..9: A conversion into tensor memory
         // A warp may only touch tensor-memory lanes 32 (warp % 4) .. +31: its rows are tile rows

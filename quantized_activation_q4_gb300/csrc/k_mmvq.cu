@@ -137,6 +137,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
     atomicOr(&g_qk_faults, 1u);
     return false;
 }
+// Before a producer thread leaves, every copy it issued into the ring has landed, also after
+// one of its waits ran out: ring positions issued - SLOTS .. issued - 1 are the last ones of
+// their slots (a barrier whose phase completed long ago passes at once). A wait that runs out
+// here ends the drain; the fault is already recorded.
+__device__ __forceinline__ void drain_ring(const uint64_t *full, int slots, int issued) {
+    for (int x = issued > slots ? issued - slots : 0; x < issued; x++)
+        if (!mbar_wait(smem_addr(full + x % slots), (uint32_t)(x / slots) & 1u)) break;
+}
 __device__ __forceinline__ uint64_t evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -549,9 +557,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
             // units of one projection are contiguous in its packed buffer
             const uint8_t *src = a.p[j].w + ((int64_t)rt * a.p[j].chunks + c) * L::UNIT;
             int64_t left_in_proj = a.p[j].unit_base + (int64_t)a.p[j].row_tiles * a.p[j].chunks - u0;
-            for (int i = 0; i < n_units; i++) {
-                const int slot = i % L::SLOTS;
-                const uint32_t n = (uint32_t)i / L::SLOTS;
+            int issued = 0;
+            for (; issued < n_units; issued++) {
+                const int slot = issued % L::SLOTS;
+                const uint32_t n = (uint32_t)issued / L::SLOTS;
                 if (n > 0 && !mbar_wait(smem_addr(empty + slot), (n - 1) & 1u)) break;
                 if (left_in_proj == 0) {   // next projection
                     j++;
@@ -563,6 +572,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) mmvq_sk_kernel(const __grid_con
                 src += L::UNIT;
                 left_in_proj--;
             }
+            drain_ring(full, L::SLOTS, issued);
         }
         return;
     }
@@ -1052,6 +1062,7 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
                     }
                 }
             }
+            drain_ring(full, SLOTS, (int)pos);
         } else if (lane <= 8) {   // lanes 1..8: slot lane - 1 of the token list of items 1, 2, ... ahead
             const int q = lane - 1;
             int k = 1;
