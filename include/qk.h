@@ -40,6 +40,10 @@
  *     their outputs are not written. NULL means every row is live. Grids are
  *     always sized for `rows`, so a captured CUDA graph stays valid while the
  *     count changes between replays.
+ *   - A row count of 0, where a call accepts it (the producers' T, the
+ *     routing calls' rows), enqueues nothing and writes nothing, except
+ *     qk_moe_plan and qk_route_plan, which write the zero counts and offsets
+ *     of an empty plan. The projections take T (rows) >= 1.
  *   - Results depend only on the input bytes and shape arguments (no state
  *     kept between calls, no cross-call caching; an image is rebuilt on every
  *     call and replay).
@@ -348,7 +352,7 @@ QK_API qk_status qk_mmvq_static_ws(const void *img, int64_t img_row_blocks, int6
  *   logits [rows][E] F32; ids [rows][k] int32; wts [rows][k] F32
  *   experts ranked by logit, larger first, equal logits to the lower index;
  *   ids in rank order; wts = softmax(logits)[id] (not renormalised).
- * Rows >= *d_live_rows keep their previous ids/wts bytes.
+ * Rows >= *d_live_rows keep their previous ids/wts bytes. rows = 0 launches nothing.
  * Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED (E > 256, k > 32, k > E).
  */
 QK_API qk_status qk_topk_route(const float *logits, int64_t rows, int32_t E, int32_t k,
@@ -364,8 +368,9 @@ QK_API qk_status qk_topk_route(const float *logits, int64_t rows, int32_t E, int
  *   offsets[E+1] exclusive scan of counts, offsets[E] = live*k
  *   items  [rows*k] positions 0..live*k-1 hold the pairs grouped by expert,
  *          ascending p within each expert; positions past live*k untouched
- * One launch for any width. Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED
- * (E > 1024), QK_ERR_ALIAS.
+ * One launch for any width, also for rows = 0 or a live count of 0 (zero
+ * counts and offsets). Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED (E > 1024),
+ * QK_ERR_ALIAS.
  */
 QK_API qk_status qk_moe_plan(const int32_t *ids, int64_t rows, int32_t k, int32_t E,
                       int32_t *counts, int32_t *offsets, int32_t *items,

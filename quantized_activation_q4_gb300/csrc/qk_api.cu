@@ -491,7 +491,7 @@ qk_status qk_route_plan(const float *logits, int64_t rows, int32_t E, int32_t k,
         REQUIRE(!overlap(outs[a], sl), QK_ERR_ALIAS, "an output overlaps logits");
         for (int b = 0; b < a; b++) REQUIRE(!overlap(outs[a], outs[b]), QK_ERR_ALIAS, "outputs overlap each other");
     }
-    if (rows == 0) return QK_OK;
+    // rows == 0 still launches: like qk_moe_plan, the plan of no pairs writes zero counts and offsets
     return launch_route_plan(logits, (int)rows, E, k, ids, wts, counts, offsets, items, d_live_rows,
                              (cudaStream_t)stream);
 }
