@@ -127,7 +127,9 @@ QK_API uint64_t qk_launch_count(void);
  * Device-side fault word of the current device, then cleared. Bit 0: a
  * kernel's bounded wait on a shared-memory barrier gave up (the kernel then
  * stopped early and its outputs are not valid). Covers qk_mmvq, qk_mmvq_id
- * and qk_mmq. Synchronises the device.
+ * and qk_mmq. Bit 1: a routed projection's counts held more passes than any
+ * plan of its bucket can (not the output of qk_moe_plan); it did no work.
+ * Synchronises the device.
  */
 QK_API qk_status qk_device_faults(uint32_t *faults);
 
@@ -405,10 +407,13 @@ typedef struct qk_proj_id {
  * offsets[e+1]): y[p][:] = W_e * image row (p / k), with the per-block
  * arithmetic of qk_mmvq. Experts with no items read no weights; pairs not in
  * the plan are not written. The plan (counts/offsets/items, device) is the
- * output of qk_moe_plan; ids is not needed.
+ * output of qk_moe_plan; ids is not needed. A plan from anywhere else gives
+ * unspecified outputs but no read outside counts, offsets and items: counts
+ * are clamped to [0, rows * k] and an item position outside items, or a pair
+ * outside the bucket, is skipped.
  *   rows: bucket rows (image rows >= rows never read); n_proj 1..8
  * Errors: QK_ERR_ARG, QK_ERR_UNSUPPORTED (n_experts > 1024), QK_ERR_SHAPE,
- * QK_ERR_ALIAS.
+ * QK_ERR_ALIAS (also an output over counts, offsets or items).
  */
 QK_API qk_status qk_mmvq_id(const void *img, int64_t img_row_blocks, int64_t rows, int32_t k,
                      int32_t n_proj, const qk_proj_id *projs,

@@ -950,6 +950,16 @@ __device__ __forceinline__ IdItem id_item(const IdArgs &a, const int32_t *live_e
     return r;
 }
 
+// Pair idx of expert e's planned pairs, or -1: past the expert's count, outside the items
+// array (offsets not from a plan of this bucket), or not a pair of this bucket.
+__device__ __forceinline__ int plan_pair(const IdArgs &a, int e, int idx) {
+    const int n_items = __ldg(a.counts + e);
+    const int64_t at = (int64_t)__ldg(a.offsets + e) + idx;
+    if (idx >= n_items || at < 0 || at >= (int64_t)a.rows * a.k) return -1;
+    const int p = __ldg(a.items + at);
+    return p < 0 || p / a.k >= a.rows ? -1 : p;
+}
+
 template <int WT>
 __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_constant__ IdArgs a) {
     using L = Layout<WT>;
@@ -987,7 +997,9 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
     const unsigned lt = (1u << lane) - 1u;
     auto expert_at = [&](int c, int &e, int &passes) {
         e = 32 * c + lane;
-        const int cnt = e < a.E ? __ldg(a.counts + e) : 0;
+        // a count outside [0, rows * k] (not from a plan of this bucket) is clamped, so the work
+        // stays bounded; plan_pair keeps every read inside items
+        const int cnt = e < a.E ? min(max(__ldg(a.counts + e), 0), a.rows * a.k) : 0;
         passes = cnt > 0 ? (cnt + 7) / 8 : 0;
     };
     {
@@ -1033,7 +1045,13 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
     __syncthreads();
     int n_live = 0;
     for (int w = 0; w <= RW; w++) n_live += w_live[w];
-    const int n_work = (n_live > 0 ? pass_pre[n_live] : 0) * a.tiles_per_expert, G = gridDim.x;
+    // No plan of this bucket has more passes than ceil(rows * k / 8) + (experts with pairs); a
+    // larger (or wrapped) total means counts that are not a plan: no work, and bit 1 of the
+    // fault word. The host keeps that bound times tiles_per_expert below 2^31.
+    const int64_t tot = n_live > 0 ? pass_pre[n_live] : 0;
+    const bool plan_ok = tot >= 0 && tot <= ((int64_t)a.rows * a.k + 7) / 8 + n_live;
+    if (!plan_ok && threadIdx.x == 0) atomicOr(&g_qk_faults, 2u);
+    const int n_work = plan_ok ? (int)tot * a.tiles_per_expert : 0, G = gridDim.x;
     const uint32_t ring = smem_addr(smem);
 
     if (warp == RW) {   // ---------------- producer
@@ -1070,10 +1088,7 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
                 const int b = k & 1;
                 if (k >= 2 && !mbar_wait(smem_addr(meta_empty + b), ((k >> 1) - 1) & 1u)) break;
                 const IdItem w = id_item(a, live_e, pass_pre, n_live, it);
-                const int n_items = __ldg(a.counts + w.e), item0 = __ldg(a.offsets + w.e);
-                const int idx = w.pass * 8 + q;
-                int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
-                if (p < 0 || p / a.k >= a.rows) p = -1;   // not a pair of this bucket: skip
+                const int p = plan_pair(a, w.e, w.pass * 8 + q);
                 tok_img[b][q] = p >= 0 ? (a.per_pair ? p : p / a.k) : -1;
                 tok_out[b][q] = p;
                 mbar_arrive(smem_addr(meta_full + b));
@@ -1095,10 +1110,7 @@ __global__ void __launch_bounds__(ID_THREADS, 2) mmvq_id_kernel(const __grid_con
         const int mb = k & 1;
         if (k == 0) {   // the first item's token list: no earlier item to hide its loads behind
             if (threadIdx.x < 8) {
-                const int n_items = __ldg(a.counts + w.e), item0 = __ldg(a.offsets + w.e);
-                const int idx = w.pass * 8 + threadIdx.x;
-                int p = idx < n_items ? __ldg(a.items + item0 + idx) : -1;
-                if (p < 0 || p / a.k >= a.rows) p = -1;   // not a pair of this bucket: skip
+                const int p = plan_pair(a, w.e, w.pass * 8 + threadIdx.x);
                 tok_img[0][threadIdx.x] = p >= 0 ? (a.per_pair ? p : p / a.k) : -1;
                 tok_out[0][threadIdx.x] = p;
             }

@@ -392,6 +392,10 @@ static qk_status mmvq_id_common(const void *img, int64_t img_row_blocks, int64_t
             "rows, k or img_row_blocks out of range");
     REQUIRE(n_proj >= 1 && n_proj <= 8, QK_ERR_UNSUPPORTED, "n_proj=%d not in 1..8", (int)n_proj);
     Span si = span(img, (size_t)((per_pair ? rows * k : rows) * img_row_blocks * Q8_1_BYTES));
+    // the plan is read while outputs are written: no output may overlap it
+    const int64_t E = projs[0].n_experts;
+    const Span plan[3] = {span(counts, (size_t)(E > 0 ? E : 0) * 4), span(offsets, (size_t)(E > 0 ? E + 1 : 0) * 4),
+                          span(items, (size_t)(rows * k * 4))};
     for (int j = 0; j < n_proj; j++) {
         const qk_proj_id &p = projs[j];
         qk_status st = check_proj_common(p.wtype, p.w, p.N, p.K, img_row_blocks);
@@ -402,10 +406,17 @@ static qk_status mmvq_id_common(const void *img, int64_t img_row_blocks, int64_t
         Span sy = span(p.y, (size_t)(rows * k * p.N * 4));
         Span sw = span(p.w, (size_t)packed_bytes(p.wtype, p.N, p.K) * p.n_experts);
         REQUIRE(!overlap(sy, si) && !overlap(sy, sw), QK_ERR_ALIAS, "projection %d: y overlaps img or w", j);
+        REQUIRE(!overlap(sy, plan[0]) && !overlap(sy, plan[1]) && !overlap(sy, plan[2]), QK_ERR_ALIAS,
+                "projection %d: y overlaps counts, offsets or items", j);
         for (int i = 0; i < j; i++)
             REQUIRE(!overlap(sy, span(projs[i].y, (size_t)(rows * k * projs[i].N * 4))), QK_ERR_ALIAS,
                     "outputs of projections %d and %d overlap", i, j);
     }
+    // the routed kernel counts its work items in int: (passes of any plan) x (row tiles) < 2^31
+    int64_t tiles = 0;
+    for (int j = 0; j < n_proj; j++) tiles += ceil_div(projs[j].N, UNIT_ROWS);
+    REQUIRE(((rows * k + 7) / 8 + E) * tiles < (1LL << 31), QK_ERR_UNSUPPORTED,
+            "rows * k * row tiles too large for one routed launch");
     for (int wt = QK_W_Q4_0; wt <= QK_W_Q8_0; wt++) {
         qk_proj_id group[8];
         int n = 0;

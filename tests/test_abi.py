@@ -145,6 +145,11 @@ def test_routed_ffn_checks(lib):
     arr9 = (qk.qk_proj_id * 9)(*[qk.qk_proj_id(0, 4, W, 128, 256, Y + i * (1 << 20)) for i in range(9)])
     assert lib.qk_mmvq_id_slots(P(IMG), rb, rows, k, 9, arr9, P(X), P(X + 64), P(X + 128), None) == 5
     assert lib.qk_mmvq_id_slots(P(IMG), rb, rows, 65, 1, arr, P(X), P(X + 64), P(X + 128), None) == 1
+    # an output may not overlap the plan it is read from (counts, offsets or items)
+    ok = (qk.qk_proj_id * 1)(qk.qk_proj_id(0, 4, W, 128, 256, Y))
+    for counts, offsets, items in ((Y + 64, X, X + 64), (X, Y + 4000, X + 64), (X, X + 64, Y + 8)):
+        for fn in (lib.qk_mmvq_id, lib.qk_mmvq_id_slots):
+            assert fn(P(IMG), rb, rows, k, 1, ok, P(counts), P(offsets), P(items), None) == 3
 
 
 def test_grid_limits_are_refused(lib):
