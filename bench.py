@@ -597,10 +597,22 @@ def other_configs(qk, synth, torch, dev, hbm: float, l2: int) -> dict:
     us_2 = _graph_us(torch, stream, [lambda r=r: (glu(), down(r)) for r in range(R2)], 10)
     us_2d = _graph_us(torch, stream, [lambda r=r: down(r) for r in range(R2)], 10)
     us_2g = _graph_us(torch, stream, [glu for _ in range(R2)], 10)
+    # every GLU kind in every input layout, each kernel alone back to back (16 launches per graph)
+    gsep, usep = a[:, :NF].contiguous(), a[:, NF:].contiguous()
+    glu_us = {}
+    for kind in ("swiglu", "geglu_tanh", "reglu", "geglu_erf", "geglu_quick", "swiglu_oai", "swiglu_clamp"):
+        for layout in ("separate", "packed", "packed_swapped"):
+            if layout == "separate":
+                f = lambda k=kind: qk.qk_glu_q8_1(k, "separate", gsep, NF, usep, NF, T, NF, gout, NF, gimg, NF // 32)
+            else:
+                f = lambda k=kind, l=layout: qk.qk_glu_q8_1(k, l, a, 2 * NF, None, 0, T, NF, gout, NF, gimg, NF // 32)
+            glu_us[f"{kind}/{layout}"] = round(_graph_us(torch, stream, [f] * 16, 10), 3)
+    del gsep, usep
     out["c2_glu_down"] = {"us": round(us_2, 3), "glu_us": round(us_2g, 3), "down_us": round(us_2d, 3),
                           "weight_bytes": W_DOWN, "weight_gbs": gb(W_DOWN, us_2),
                           "down_gbs": gb(W_DOWN, us_2d), "down_hbm_frac": round(W_DOWN / (us_2d * 1e-6) / 1e9 / hbm, 4),
-                          "replicas": R2}
+                          "replicas": R2, "glu_kinds_layouts_us": glu_us,
+                          "glu_bytes": T * NF * 4 * 3 + T * (NF // 32) * 36}
     del down_w
 
     # ---- config 3: routed MoE, RMS -> image; top-8 of 128; plan; gate/up 2560 -> 768 per expert
