@@ -56,7 +56,10 @@ def run_mmq(qs, d, rb, T, specs):
 
 
 @pytest.mark.parametrize("T,N,K,rb", [(100, 200, 384, 12), (65, 130, 160, 6), (1, 128, 128, 4), (64, 256, 256, 8),
-                                      (130, 64, 1056, 33)])
+                                      (130, 64, 1056, 33),
+                                      (1, 1, 32, 1),       # one token, one weight row, one block
+                                      (257, 129, 96, 3),   # a 1-token and a 1-row tail tile, K of 3 blocks
+                                      (3, 300, 32, 2)])    # K of one block inside a wider image row
 def test_mmq_small_full(T, N, K, rb):
     x = synth.activations(7000 + T + N, T, K)
     W = synth.q4_0_weight(7001 + N, N, K)
