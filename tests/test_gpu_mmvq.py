@@ -50,12 +50,16 @@ def check(yg, wtype, W, N, K, x, img_host, rb, rows_plain=None):
     assert_exact_path(yg, exact, NMSE_EXACT, what=f"{wtype} {N}x{K}")
     sel = np.arange(N) if rows_plain is None else rows_plain
     plain = O.proj_plain(wtype, W[sel], len(sel), K, x)
-    assert O.nmse(yg[:, sel], plain) <= NMSE_GATE
+    # the pages' bound is a statistic of the quantisation noise over a tensor; over a handful of
+    # outputs (one dot of 32 products can cancel to a small value) it says nothing, so it is
+    # checked from 64 outputs up; the exact-path comparison above holds at every size
+    if yg.shape[0] * len(sel) >= 64:
+        assert O.nmse(yg[:, sel], plain) <= NMSE_GATE
 
 
 @pytest.mark.parametrize("wtype", ["q4_0", "q8_0"])
 @pytest.mark.parametrize("T,N,K", [(1, 256, 256), (8, 512, 3584), (3, 33, 96), (8, 100, 160), (5, 16, 32),
-                                   (8, 48, 1056)])
+                                   (8, 48, 1056), (1, 1, 32), (2, 129, 64), (7, 257, 4128)])
 def test_mmvq_single(wtype, T, N, K):
     x = synth.activations(5000 + N + K, T, K)
     rb = K // 32 + 2
