@@ -320,24 +320,24 @@ QK_API qk_status qk_mmvq(const void *img, int64_t img_row_blocks, int64_t T,
  * (The pages this library follows have no counterpart for this call.)
  *
  * Some callers cannot call cudaMalloc at all or at the point where they
- * project: code that runs while a stream is being captured into a CUDA graph
- * (allocation is not allowed there), a plugin or kernel-library shim that is
- * handed only the tensors it reads and writes, or a latency-critical path
- * that must not touch the allocator. This entry point takes the same
+ * project: a plugin or kernel-library shim that is handed only the tensors it
+ * reads and writes (it owns no allocator and may not keep memory between
+ * calls), or a latency-critical path that must not touch the allocator
+ * (cudaMalloc can synchronise the device and take milliseconds). This entry point takes the same
  * arguments as qk_mmvq minus the workspace, and uses instead a fixed scratch
  * array of QK_MMVQ_STATIC_WS_BYTES bytes that lives in the library's own
  * device memory (every GPU that loads the library holds it until the process
  * exits). Inputs and outputs are still passed by the caller.
- *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - The first call on a device looks up the array's device address once,
+ *     with that device current; later calls on the device reuse it.
  *   - Every argument is checked as in qk_mmvq before anything is enqueued.
  *   - Calls whose workspace need (qk_mmvq_workspace_bytes) exceeds
  *     QK_MMVQ_STATIC_WS_BYTES are refused with QK_ERR_UNSUPPORTED.
  *   - Each call clears the array's completion counters (only those) on its
  *     stream before its kernels run; it allocates nothing.
  *   - All calls on a device share the one array, so calls that may overlap on
- *     the GPU (different streams, or graphs replayed concurrently) race and
- *     give wrong results; order them on one stream.
+ *     the GPU (for instance on different streams) race and give wrong
+ *     results; order them on one stream.
  */
 #define QK_MMVQ_STATIC_WS_BYTES (2u << 20)
 

@@ -1,9 +1,9 @@
 """qk_mmvq_static_ws: the projection entry point for callers that cannot allocate.
 
-Some callers of this library cannot call cudaMalloc where they project: code
-running while a stream is captured into a CUDA graph, a plugin that is handed
-only its input and output tensors, or a latency-critical path that must not
-touch the allocator. For them qk_mmvq_static_ws runs the same kernels as
+Some callers of this library cannot call cudaMalloc where they project: a
+plugin that is handed only its input and output tensors (it owns no allocator
+and may not keep memory between calls), or a latency-critical path that must
+not touch the allocator (cudaMalloc can synchronise the device). For them qk_mmvq_static_ws runs the same kernels as
 qk_mmvq, with the library's own fixed scratch array in place of a
 caller-supplied workspace (the scratch holds the partial sums of row tiles
 that several CTAs share, and their completion counters). This test calls it
