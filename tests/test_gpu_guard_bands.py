@@ -1,5 +1,5 @@
-"""Guard bands around every output of every entry point (a substitute for a
-memory checker, which is closed on this machine).
+"""Guard bands around every output of every entry point: out-of-bounds writes are
+caught from the outside, without a device-side memory checker.
 
 Each output buffer sits inside a larger allocation whose bytes before and after
 it are a canary pattern, and, where an output has a row stride wider than its
