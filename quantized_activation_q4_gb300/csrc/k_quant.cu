@@ -135,10 +135,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
 // One CTA per row; the row stays in registers between the sum of squares and
 // the output. The reference shape is 1024 threads (thread i holds columns
 // 4i + 4096*it for it < ITEMS, ITEMS = 1, 2, 4 or 8 by K, so K <= 32768). For
-// K <= 8192 and many rows a 256-thread CTA takes the row instead (four rows in
-// flight per SM): its thread j plays the reference threads j + 256m (m < 4)
-// and reduces their partial sums in the same order (one warp tree per m, then
-// the same 32-entry tree), so the bits are those of the 1024-thread shape.
+// many rows a smaller CTA takes the row instead (128 threads for K <= 4096,
+// eight rows in flight per SM; 256 threads for K <= 8192, four): its thread j
+// plays the reference threads j + NT*m (m < 1024 / NT) and reduces their
+// partial sums in the same order (one warp tree per m, then the same 32-entry
+// tree), so the bits are those of the 1024-thread shape.
 // With ITEMS <= 2 the weight and bias are loaded together with the row, before
 // the reduction.
 constexpr int RMS_THREADS = 1024;
@@ -148,7 +149,7 @@ constexpr int RMS_ROWS_FOR_SMALL = 256;   // rows from which the 256-thread shap
 // Q81: the image is Q8_1 blocks (img); else Q8_0 split planes (qs codes, dh half scales), the
 // prefill layout that qk_mmq reads.
 template <int NT, int ITEMS, bool Q81>
-__global__ void __launch_bounds__(NT, NT == RMS_THREADS ? 1 : 4) rmsnorm_q8_1_kernel(
+__global__ void __launch_bounds__(NT, RMS_THREADS / NT) rmsnorm_q8_1_kernel(
     const float *__restrict__ x, int K, int64_t x_stride, int kind, const float *__restrict__ w,
     const float *__restrict__ bias, float scale, float eps, float *__restrict__ y, int64_t y_stride,
     uint8_t *__restrict__ img, int8_t *__restrict__ qs, uint16_t *__restrict__ dh, int64_t row_blocks, int T,
@@ -358,9 +359,13 @@ static qk_status launch_rmsnorm(const float *x, int T, int K, int64_t x_stride, 
     if (T == 0) return QK_OK;
     const int per = 4 * RMS_THREADS;   // columns per item of the reference shape
     if (T >= RMS_ROWS_FOR_SMALL && K <= 2 * per) {   // 256 threads, four times the items
-        auto kernel = K <= per ? rmsnorm_q8_1_kernel<256, 4, Q81> : rmsnorm_q8_1_kernel<256, 8, Q81>;
-        return launch_pdl(Q81 ? "rmsnorm_q8_1" : "rmsnorm_q8_0", kernel, dim3((unsigned)T), dim3(256), 0, s, x,
-                          K, x_stride, kind, w, b, scale, eps, y, y_stride, img, qs, dh, row_blocks, T, live);
+        if (K <= per)   // 128 threads: eight rows in flight per SM
+            return launch_pdl(Q81 ? "rmsnorm_q8_1" : "rmsnorm_q8_0", rmsnorm_q8_1_kernel<128, 8, Q81>,
+                              dim3((unsigned)T), dim3(128), 0, s, x, K, x_stride, kind, w, b, scale, eps, y, y_stride,
+                              img, qs, dh, row_blocks, T, live);
+        return launch_pdl(Q81 ? "rmsnorm_q8_1" : "rmsnorm_q8_0", rmsnorm_q8_1_kernel<256, 8, Q81>, dim3((unsigned)T),
+                          dim3(256), 0, s, x, K, x_stride, kind, w, b, scale, eps, y, y_stride, img, qs, dh,
+                          row_blocks, T, live);
     }
     auto kernel = K <= per ? rmsnorm_q8_1_kernel<RMS_THREADS, 1, Q81>
                   : K <= 2 * per ? rmsnorm_q8_1_kernel<RMS_THREADS, 2, Q81>
