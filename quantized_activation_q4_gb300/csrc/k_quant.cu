@@ -89,14 +89,15 @@ __device__ __forceinline__ void put_q8_1(uint8_t *blk, int j8, float d, uint32_t
 }
 
 // ---------------------------------------------------------------- quantizers
-// grid (T, ceil(row_blocks / (32*QPB))), 256 threads: lane group m of warp w
-// handles blocks 32*QPB*blockIdx.y + 32*j + 4*w + m (j < QPB) of row blockIdx.x
-// (rows on x: up to 2^31-1). A lane loads its QPB float4s before it quantises,
-// so that large images keep several loads per thread in flight (QPB = 4), while
-// small ones spread over more CTAs (QPB = 1). Every block is quantised on its
-// own, so the bytes do not depend on QPB.
-template <bool Q81, int QPB>
-__global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__ x, int K,
+// grid (T, ceil(row_blocks / (G*QPB))), NT threads, G = NT / 8 lane groups: lane group m of
+// warp w handles blocks G*QPB*blockIdx.y + G*j + 4*w + m (j < QPB) of row blockIdx.x (rows on
+// x: up to 2^31-1). A lane loads its QPB float4s before it quantises, so that large images
+// keep several loads per thread in flight, while small ones spread over more CTAs (QPB = 1).
+// Large images with rows of at most 128 blocks take a 128-thread CTA per row with QPB =
+// ceil(row_blocks / 16) (more rows in flight per SM, few idle lanes), wider rows 256 threads
+// with QPB = 4. Every block is quantised on its own, so the bytes do not depend on the shape.
+template <bool Q81, int QPB, int NT = 256>
+__global__ void __launch_bounds__(NT) quantize_kernel(const float *__restrict__ x, int K,
                                                        int64_t x_stride, uint8_t *__restrict__ out,
                                                        int8_t *__restrict__ qs, uint16_t *__restrict__ dh,
                                                        int64_t row_blocks, int T, const int32_t *live) {
@@ -104,20 +105,21 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
     pdl_wait();
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31, j8 = lane & 7;
-    const int64_t b0 = (int64_t)blockIdx.y * 32 * QPB + (threadIdx.x >> 5) * 4 + (lane >> 3);
+    constexpr int G = NT / 8;
+    const int64_t b0 = (int64_t)blockIdx.y * G * QPB + (threadIdx.x >> 5) * 4 + (lane >> 3);
     float v[QPB][4];
     // the row's values are loaded together with the live count (row t < T is in the caller's
     // buffer even when it is padding), so the global reads overlap
 #pragma unroll
     for (int j = 0; j < QPB; j++) {
-        const int64_t b = b0 + 32 * j, col = b * QB + 4 * j8;
+        const int64_t b = b0 + G * j, col = b * QB + 4 * j8;
         v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
         if (b < row_blocks && col < K) load4(x + t * x_stride + col, (int)(K - col < 4 ? K - col : 4), v[j]);
     }
     if (t >= live_rows(live, T)) return;
 #pragma unroll
     for (int j = 0; j < QPB; j++) {
-        const int64_t b = b0 + 32 * j;
+        const int64_t b = b0 + G * j;
         uint32_t codes;
         int sum;
         const float d = q8_block(v[j], &codes, &sum);   // all lanes take part in the shuffles
@@ -334,10 +336,27 @@ constexpr int64_t QUANT_BIG_BLOCKS = 1 << 17;   // blocks per call from which QP
 
 }  // namespace
 
+// Large images with rows of at most 128 blocks: one 128-thread CTA per row (QPB = ceil(rb / 16)).
+template <bool Q81>
+static qk_status launch_quantize_rows128(const char *name, const float *x, int T, int K, int64_t x_stride,
+                                         uint8_t *img, int8_t *qs, uint16_t *d, int64_t row_blocks,
+                                         const int32_t *live, cudaStream_t s) {
+    const int qpb = (int)ceil_div(row_blocks, 16);
+    auto kernel = qpb <= 5   ? quantize_kernel<Q81, 5, 128>
+                  : qpb == 6 ? quantize_kernel<Q81, 6, 128>
+                  : qpb == 7 ? quantize_kernel<Q81, 7, 128>
+                             : quantize_kernel<Q81, 8, 128>;
+    return launch_pdl(name, kernel, dim3((unsigned)T, 1u), dim3(128), 0, s, x, K, x_stride, img, qs, d, row_blocks,
+                      T, live);
+}
+
 qk_status launch_quantize_q8_1(const float *x, int T, int K, int64_t x_stride, uint8_t *img,
                                int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
     const bool big = (int64_t)T * row_blocks >= QUANT_BIG_BLOCKS;
+    if (big && row_blocks > 64 && row_blocks <= 128)
+        return launch_quantize_rows128<true>("quantize_q8_1", x, T, K, x_stride, img, nullptr, nullptr, row_blocks,
+                                             live, s);
     dim3 grid((unsigned)T, (unsigned)ceil_div(row_blocks, big ? 128 : 32));
     return launch_pdl("quantize_q8_1", big ? quantize_kernel<true, 4> : quantize_kernel<true, 1>, grid, dim3(256),
                       0, s, x, K, x_stride, img, (int8_t *)nullptr, (uint16_t *)nullptr, row_blocks, T, live);
@@ -347,6 +366,9 @@ qk_status launch_quantize_q8_0(const float *x, int T, int K, int64_t x_stride, i
                                uint16_t *d, int64_t row_blocks, const int32_t *live, cudaStream_t s) {
     if (T == 0) return QK_OK;
     const bool big = (int64_t)T * row_blocks >= QUANT_BIG_BLOCKS;
+    if (big && row_blocks > 64 && row_blocks <= 128)
+        return launch_quantize_rows128<false>("quantize_q8_0", x, T, K, x_stride, nullptr, qs, d, row_blocks, live,
+                                              s);
     dim3 grid((unsigned)T, (unsigned)ceil_div(row_blocks, big ? 128 : 32));
     return launch_pdl("quantize_q8_0", big ? quantize_kernel<false, 4> : quantize_kernel<false, 1>, grid,
                       dim3(256), 0, s, x, K, x_stride, (uint8_t *)nullptr, qs, d, row_blocks, T, live);
