@@ -189,31 +189,40 @@ __device__ __forceinline__ uint4 a_word(uint32_t w, __half2 dw) {
 }
 
 // ------------------------------------------------------------------ B = dequantised image
-__device__ __forceinline__ uint32_t b_pair(uint32_t v, int k0, int k1, float da) {
-    const float x = (float)(int8_t)(v >> (8 * k0)), y = (float)(int8_t)(v >> (8 * k1));
-    const __half2 r = __floats2half2_rn(x * da, y * da);   // products exact in f32; one rounding
+// Two codes of word v (bytes k and k + 2, k = 0 or 1) -> f16 pair q * d_a. A code becomes an
+// exact half by placing its biased byte (q + 128) under the exponent of 1024 (PRMT); subtracting
+// 1152 leaves q exactly; the binary16 multiply by d_a rounds the exact product once, as the
+// binary32 product rounded to binary16 would.
+__device__ __forceinline__ uint32_t b_pair(uint32_t u, uint32_t sel, __half2 d2) {
+    uint32_t h;
+    asm("prmt.b32 %0, %1, 0x64646464, %2;" : "=r"(h) : "r"(u), "r"(sel));
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+    const __half2 r = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&h), bias), d2);
     return *reinterpret_cast<const uint32_t *>(&r);
 }
+// four codes (one word, elements e .. e+3) -> halves in the order e, e+2, e+1, e+3
+__device__ __forceinline__ uint2 b_word(uint32_t v, __half2 d2) {
+    const uint32_t u = v ^ 0x80808080u;   // q + 128 in each byte
+    return make_uint2(b_pair(u, 0x4240u, d2), b_pair(u, 0x4341u, d2));
+}
 
-// One thread per (token, block, word w): 8 codes -> f16 q * d_a at columns
-// 2w, 2w+1 (low word) and 8+2w, 9+2w (high word) of the block, the K order of
-// the A stages.
+// grid (T, ceil(4 kb / 256)), tokens on x: thread j of CTA (t, y) takes word w = j & 3 of block
+// b = 64 y + j / 4 of token t: codes 4w .. 4w+3 and 16+4w .. 16+4w+3 -> f16 q * d_a at columns
+// 2w, 2w+1 (halves 4w .. 4w+3) and 8+2w, 9+2w (halves 16+4w ..), the K order of the A stages.
 __global__ void __launch_bounds__(256) dequant_b_kernel(const int8_t *__restrict__ qs, const uint16_t *__restrict__ d,
                                                         int64_t row_blocks, int T, int kb, __half *__restrict__ B) {
     pdl_trigger();
     pdl_wait();
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)T * kb * 4) return;
-    const int w = (int)(i & 3);
-    const int64_t tb = i >> 2;
-    const int t = (int)(tb / kb), b = (int)(tb % kb);
+    const int t = blockIdx.x, w = threadIdx.x & 3, b = blockIdx.y * 64 + (threadIdx.x >> 2);
+    if (b >= kb) return;
     const int8_t *src = qs + ((int64_t)t * row_blocks + b) * QB;
     const uint32_t lo = __ldg(reinterpret_cast<const unsigned int *>(src + 4 * w));
     const uint32_t hi = __ldg(reinterpret_cast<const unsigned int *>(src + 16 + 4 * w));
-    const float da = __half2float(__ushort_as_half(__ldg(d + (int64_t)t * row_blocks + b)));
+    const __half dah = __ushort_as_half(__ldg(d + (int64_t)t * row_blocks + b));
+    const __half2 d2 = __halves2half2(dah, dah);
     __half *dst = B + ((int64_t)t * kb + b) * QB;
-    *reinterpret_cast<uint2 *>(dst + 4 * w) = make_uint2(b_pair(lo, 0, 2, da), b_pair(lo, 1, 3, da));
-    *reinterpret_cast<uint2 *>(dst + 16 + 4 * w) = make_uint2(b_pair(hi, 0, 2, da), b_pair(hi, 1, 3, da));
+    *reinterpret_cast<uint2 *>(dst + 4 * w) = b_word(lo, d2);
+    *reinterpret_cast<uint2 *>(dst + 16 + 4 * w) = b_word(hi, d2);
 }
 
 // ------------------------------------------------------------------ the GEMM
@@ -497,9 +506,8 @@ qk_status launch_mmq(const int8_t *qs, const uint16_t *d, int64_t row_blocks, in
     if (r != CUDA_SUCCESS) return fail(QK_ERR_CUDA, "mmq: tensor map encoding failed (%d)", (int)r);
 
     const int kb = kmax / QB;
-    const int64_t nthr = (int64_t)T * kb * 4;
-    qk_status st = launch_pdl("mmq_dequant_b", dequant_b_kernel, dim3((unsigned)ceil_div(nthr, 256)), dim3(256), 0, s,
-                              qs, d, row_blocks, T, kb, static_cast<__half *>(ws));
+    qk_status st = launch_pdl("mmq_dequant_b", dequant_b_kernel, dim3((unsigned)T, (unsigned)ceil_div(kb, 64)),
+                              dim3(256), 0, s, qs, d, row_blocks, T, kb, static_cast<__half *>(ws));
     if (st != QK_OK) return st;
     static bool configured = false;
     if (!configured) {

@@ -72,6 +72,28 @@ def test_mmq_small_full(T, N, K, rb):
     assert O.nmse(yg, O.proj_plain("q4_0", W, N, K, x)) <= NMSE_GATE
 
 
+def test_mmq_b_operand_is_each_code_times_its_scale_rounded_once():
+    """The dequantised B operand the call leaves in its workspace: every code times its block's
+    scale, the exact product rounded once to binary16, in the K order of the tensor-memory A
+    stages (halves 4w .. 4w+3 of a 16-element half-block hold elements 4w, 4w+2, 4w+1, 4w+3),
+    against numpy's float64 product rounded to float16; bit for bit, including subnormal
+    products of tiny blocks."""
+    T, K, rb, N = 70, 384, 13, 64
+    x = synth.activations(7400, T, K) * np.float32(3.0)
+    x[5, :64] *= np.float32(1e-5)            # tiny scales: subnormal binary16 products
+    x[6, 32:64] = 0.0                        # a zero block: d = 0
+    W = synth.q4_0_weight(7401, N, K)
+    qs, d = quantize_q8_0(x, K, rb)
+    _, keep = run_mmq(qs, d, rb, T, [(W, N, K)])
+    kb = K // 32
+    B = host(keep[-1])[:T * kb * 32 * 2].view(np.uint16).reshape(T, kb, 32)
+    q = host(qs).view(np.int8).reshape(T, rb, 32)[:, :kb].astype(np.float64)
+    dd = host(d).view(np.float16).reshape(T, rb)[:, :kb].astype(np.float64)
+    order = [16 * (p // 16) + 4 * (p % 16 // 4) + (0, 2, 1, 3)[p % 4] for p in range(32)]
+    want = (q[:, :, order] * dd[:, :, None]).astype(np.float16).view(np.uint16)
+    assert np.array_equal(B, want)
+
+
 def test_mmq_projections_of_different_k_in_one_launch():
     """Several projections of one image with different K in one launch: B is dequantised for the
     largest K and each projection reads only its own 128-K stages (a partial last stage meets the
